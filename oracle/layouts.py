@@ -1,0 +1,85 @@
+"""Scale-factor arrangements used by the quantizer's outputs (test side).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Two arrangements exist for every quantized operand:
+
+* compact: one E8M0 byte per block, indexed naturally
+    - 1x32 along head_dim:      [T, H, D/32]
+    - 32 along tokens:          [Tp/32, H, D]
+    - 32x32 (tokens, head_dim): [Tp/32, H, D/32]
+  where token-blocked arrays index tokens in the padded scale-row space below.
+* MMA-ready: the layout the tensor core reads scale factors in, per 128-row
+  operand tile: 128 operand rows x 4 contraction blocks (128 contraction
+  elements) = 512 bytes, where operand row r and contraction block kb sit at
+  byte (r % 32) * 16 + (r // 32) * 4 + kb.  Tiles are stored [Tp/128, H, 512].
+  "Operand rows" are tokens for K-major use (contraction over head_dim) and
+  head_dim channels for MN-major use (contraction over tokens).
+
+Padded scale rows (the jagged module of "Low Precision Flash Attention 4",
+paragraph 2): FP8 data stays at unpadded token positions; scale rows of
+sequence s start at the 128-aligned row sf_start[s] = sum_{t<s} ceil(L_t/128)
+* 128, so every 128-token tile of every sequence owns whole 512-byte scale
+tiles.  Unused bytes are zero.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def sf_row_starts(cu_seqlens) -> np.ndarray:
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    lens = np.diff(cu)
+    padded = -(-lens // 128) * 128
+    return np.concatenate([[0], np.cumsum(padded)]).astype(np.int64)
+
+
+def atom_offset(r, kb):
+    r = np.asarray(r); kb = np.asarray(kb)
+    return (r % 32) * 16 + (r // 32) * 4 + kb
+
+
+def mma_from_row_blocks(row_sc, cu_seqlens):
+    """K-major arrangement from per-token scales row_sc [T, H, nkb]
+    (nkb = D/32 <= 4).  Returns uint8 [Tp/128, H, 512]."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    sfs = sf_row_starts(cu)
+    T, H, nkb = row_sc.shape
+    out = np.zeros((sfs[-1] // 128, H, 512), dtype=np.uint8)
+    for s in range(len(cu) - 1):
+        for i in range(cu[s + 1] - cu[s]):
+            pr = sfs[s] + i
+            for kb in range(nkb):
+                out[pr // 128, :, atom_offset(pr % 128, kb)] = row_sc[cu[s] + i, :, kb]
+    return out
+
+
+def mma_from_token_blocks(col_sc, cu_seqlens, D):
+    """MN-major arrangement from 32-token-block scales col_sc [Tp/32, H, D]
+    (one scale per (token block, head_dim channel)).  Operand rows are the
+    head_dim channels, contraction blocks the 4 token blocks of a tile."""
+    nblk, H, d = col_sc.shape
+    assert d == D
+    ntile = -(-nblk // 4)
+    out = np.zeros((ntile, H, 512), dtype=np.uint8)
+    for tb in range(nblk):
+        for ch in range(D):
+            out[tb // 4, :, atom_offset(ch, tb % 4)] = col_sc[tb, :, ch]
+    return out
+
+
+def square_to_row(sq_sc, cu_seqlens):
+    """Per-token view [T, H, D/32] of square scales [Tp/32, H, D/32]."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    sfs = sf_row_starts(cu)
+    T = cu[-1]
+    out = np.zeros((T,) + sq_sc.shape[1:], dtype=np.uint8)
+    for s in range(len(cu) - 1):
+        for i in range(cu[s + 1] - cu[s]):
+            out[cu[s] + i] = sq_sc[(sfs[s] + i) // 32]
+    return out
+
+
+def square_to_col(sq_sc, D):
+    """Per-(token block, channel) view [Tp/32, H, D] of square scales."""
+    return np.repeat(sq_sc, 32, axis=2)[:, :, :D]

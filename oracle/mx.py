@@ -1,0 +1,206 @@
+"""MXFP8 codec and block quantizers, written from the format definitions (fp64).
+
+TEST INFRASTRUCTURE ONLY.  This package is the CPU oracle that the CUDA path is
+checked against.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import it; the
+product path never does, and it shares no code with the CUDA sources.
+
+What it follows
+---------------
+* "Low-Precision FlashAttention-4: End-to-End Block-Scaled Attention for NVIDIA
+  Blackwell", section "Understanding OCP MXFP8 Microscaling on Blackwell": a
+  block of 32 contiguous elements shares one 8-bit E8M0 scale
+  s = 2^(E8M0 - 127); each element is an E4M3 value v_i, and the block decodes
+  to s * v_i.
+* "Low Precision Flash Attention 4: End-to-End Block-Scaled Attention for
+  Blackwell", paragraphs 2-3: the backward pass quantizes in square [32, 32]
+  blocks so that the E4M3 payload is transpose-invariant.
+* The E4M3 element format itself (OCP 8-bit floating point, the "fn" variant
+  the pages name): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+  exponent field 0 holds subnormals 2^-6 * m/8; S.1111.111 is NaN; there is no
+  infinity; the largest finite magnitude is 448.
+
+Readings where the pages are silent (each one is listed in the design notes):
+* Scale exponent: e = floor(log2(amax)) - 8, i.e. the largest power of two that
+  keeps amax * 2^-e below 2 * 2^8 (8 = the exponent of E4M3's largest binade),
+  clamped to [-127, 127].  amax = 0 gives e = -127 (code 0) with zero
+  payloads; a block holding Inf or NaN gives scale code 0xFF and payload 0x7F.
+* Element rounding: round to nearest, ties to even; magnitudes above 448 are
+  saturated to 448 (no NaN is produced from a finite input); the sign of zero
+  is kept (-tiny encodes as 0x80).
+
+Parity pins for this module live in ``tests/test_oracle_mx.py``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+E4M3_MAX = 448.0
+E4M3_NAN = 0x7F
+E8M0_NAN = 0xFF
+E8M0_BIAS = 127
+EMAX_E4M3 = 8
+
+
+def _e4m3_value(code: int) -> float:
+    sign = -1.0 if code & 0x80 else 1.0
+    exp_field = (code >> 3) & 0xF
+    mant = code & 0x7
+    if exp_field == 0xF and mant == 0x7:
+        return float("nan")
+    if exp_field == 0:
+        return sign * (mant / 8.0) * 2.0 ** -6
+    return sign * (1.0 + mant / 8.0) * 2.0 ** (exp_field - 7)
+
+
+#: decoded value of every E4M3 code 0..255 (fp64, exact)
+E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+# non-negative finite magnitudes, codes 0..126, strictly increasing
+_POS = E4M3_TABLE[:127].copy()
+assert np.all(np.diff(_POS) > 0)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e8m0_decode(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.int64)
+    out = np.ldexp(1.0, c - E8M0_BIAS)
+    return np.where(c == E8M0_NAN, np.nan, out)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round fp64 values to E4M3 codes: RNE, saturate to 448, keep the sign."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    finite_or_inf = ~np.isnan(a)
+    a_safe = np.where(finite_or_inf, a, 0.0)
+    lo = np.searchsorted(_POS, a_safe, side="right") - 1   # largest <= a
+    lo = np.clip(lo, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    mid = 0.5 * (_POS[lo] + _POS[hi])   # exact: both are short dyadics
+    pick_hi = (hi != lo) & ((a_safe > mid) | ((a_safe == mid) & (hi % 2 == 0)))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+    code = np.where(finite_or_inf, code, np.uint8(E4M3_NAN)).astype(np.uint8)
+    return code
+
+
+def scale_exponent(amax) -> tuple:
+    """(e, code) for block maxima amax >= 0: e = floor(log2 amax) - 8, clamped
+    to [-127, 127]; amax == 0 -> e = -127; non-finite amax -> code 0xFF."""
+    amax = np.asarray(amax, dtype=np.float64)
+    finite = np.isfinite(amax)
+    safe = np.where(finite & (amax > 0), amax, 1.0)
+    _, fexp = np.frexp(safe)           # safe = f * 2^fexp, f in [0.5, 1)
+    floor_log2 = fexp - 1
+    e = floor_log2 - EMAX_E4M3
+    e = np.where(finite & (amax > 0), e, -E8M0_BIAS)
+    e = np.clip(e, -127, 127)
+    code = np.where(finite, e + E8M0_BIAS, E8M0_NAN).astype(np.uint8)
+    return e.astype(np.int64), code
+
+
+def _quantize_grouped(xg: np.ndarray):
+    """Quantize blocks laid out as the last axis of ``xg`` (shape [..., n]).
+    Returns (payload codes [..., n], scale codes [...])."""
+    amax = np.max(np.abs(xg), axis=-1) if xg.shape[-1] else np.zeros(xg.shape[:-1])
+    e, code = scale_exponent(amax)
+    scaled = np.ldexp(xg, -e[..., None])       # exact power-of-two scaling
+    payload = e4m3_encode(scaled)
+    bad = code == E8M0_NAN
+    if np.any(bad):
+        payload = np.where(bad[..., None], np.uint8(E4M3_NAN), payload)
+    return payload.astype(np.uint8), code
+
+
+def quantize_1x32(x) -> tuple:
+    """1x32 blocks along the last axis (length a multiple of 32).
+
+    Returns (payload uint8 same shape, scale codes [..., n/32])."""
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[-1]
+    assert n % 32 == 0
+    xg = x.reshape(*x.shape[:-1], n // 32, 32)
+    payload, code = _quantize_grouped(xg)
+    return payload.reshape(x.shape), code
+
+
+def quantize_along_rows(x, block: int = 32) -> tuple:
+    """Blocks of ``block`` consecutive rows (axis 0) per column, starting at
+    row 0; the last block may be short (ragged sequence end).
+
+    x: [R, ...]. Returns (payload [R, ...], scale codes [ceil(R/block), ...])."""
+    x = np.asarray(x, dtype=np.float64)
+    r = x.shape[0]
+    nb = -(-r // block)
+    pad = nb * block - r
+    xp = np.concatenate([x, np.zeros((pad,) + x.shape[1:])], 0) if pad else x
+    # zero padding cannot raise a block's amax; padded outputs are dropped
+    xg = np.moveaxis(xp.reshape(nb, block, *x.shape[1:]), 1, -1)
+    payload, code = _quantize_grouped(xg)
+    payload = np.moveaxis(payload, -1, 1).reshape(nb * block, *x.shape[1:])[:r]
+    return payload, code
+
+
+def quantize_32x32(x) -> tuple:
+    """Square 32x32 blocks over the first two axes of x [R, C, ...]; blocks
+    start at (0, 0); the last row-block may be short, C must be a multiple
+    of 32.  Returns (payload [R, C, ...], scales [ceil(R/32), C/32, ...])."""
+    x = np.asarray(x, dtype=np.float64)
+    r, c = x.shape[:2]
+    assert c % 32 == 0
+    nb = -(-r // 32)
+    pad = nb * 32 - r
+    xp = np.concatenate([x, np.zeros((pad,) + x.shape[1:])], 0) if pad else x
+    rest = x.shape[2:]
+    # [nb, 32, C/32, 32, ...] -> [nb, C/32, ..., 32*32]
+    xg = xp.reshape(nb, 32, c // 32, 32, *rest)
+    xg = np.moveaxis(xg, (1, 3), (-2, -1))
+    xg = xg.reshape(nb, c // 32, *rest, 1024)
+    payload, code = _quantize_grouped(xg)
+    payload = payload.reshape(nb, c // 32, *rest, 32, 32)
+    payload = np.moveaxis(payload, (-2, -1), (1, 3)).reshape(nb * 32, c, *rest)
+    return payload[:r], code
+
+
+def dequantize(payload, scale_codes, expand) -> np.ndarray:
+    """Decode payload * 2^(scale - 127); ``expand`` maps the scale array to
+    the payload's shape (e.g. a repeat along the block axis)."""
+    return e4m3_decode(payload) * expand(e8m0_decode(scale_codes))
+
+
+def dq_1x32(payload, sc):
+    return dequantize(payload, sc, lambda s: np.repeat(s, 32, axis=-1))
+
+
+def dq_rows(payload, sc, block: int = 32):
+    r = payload.shape[0]
+    return dequantize(payload, sc,
+                      lambda s: np.repeat(s, block, axis=0)[:r])
+
+
+def dq_32x32(payload, sc):
+    r = payload.shape[0]
+    return dequantize(payload, sc,
+                      lambda s: np.repeat(np.repeat(s, 32, axis=0), 32, axis=1)[:r])
+
+
+def fake_quant_1x32(x):
+    return dq_1x32(*quantize_1x32(x))
+
+
+def fake_quant_rows(x):
+    return dq_rows(*quantize_along_rows(x))
+
+
+def fake_quant_32x32(x):
+    return dq_32x32(*quantize_32x32(x))
+
+
+def mx_gemm(a_payload, a_sc, b_payload, b_sc) -> np.ndarray:
+    """D = A @ B^T with A [M, K], B [N, K] both 1x32-blocked along K (the
+    block-scaled MMA's contraction).  Every product of two decoded operands is
+    exact in fp64, so this is the dense GEMM of the dequantized operands."""
+    return dq_1x32(a_payload, a_sc) @ dq_1x32(b_payload, b_sc).T
