@@ -1,0 +1,236 @@
+/*
+ * lpfa — MXFP8 block-scaled FlashAttention (forward and backward) for
+ * NVIDIA GB300 (sm_103a).  C ABI.
+ *
+ * Sources of the operations (page title, section):
+ *  [P1] "Low Precision Flash Attention 4: End-to-End Block-Scaled Attention
+ *       for Blackwell" — paragraph 2 (tcgen05 block-scaled MMA; TMEM budget
+ *       for scale factors; online square-block quantization of dS with a
+ *       warp max-abs reduction; FP8 outputs with dual scale layouts; jagged
+ *       inputs with FP8 data unpadded and 128-aligned scale rows), paragraph
+ *       3 (forward softmax in FP32 with P converted to MXFP8 reusing the
+ *       softmax max; backward Q, K, dO in square [32, 32] blocks; FP16 dQ
+ *       with a static scale).
+ *  [P2] "Low-Precision FlashAttention-4: End-to-End Block-Scaled Attention
+ *       for NVIDIA Blackwell" — "Understanding OCP MXFP8 Microscaling on
+ *       Blackwell" (32-element blocks sharing an E8M0 scale
+ *       s = 2^(E8M0-127), E4M3 elements), "Key Algorithmic Innovations"
+ *       (both GEMMs block-scaled, FP32 running max/sum with 1/sqrt(d_k)
+ *       folded in), "PyTorch Integration & Implementation Example" (BSHD
+ *       tensors; q, k, v, their scales, softmax_scale, causal).
+ *  [P3] "FlashAttention-4 Adds Low-Precision Blackwell Support" — "Technical
+ *       Deep Dive" (TMEM/tcgen05 data flow, selective rescaling), "Hardware
+ *       Portability Gate" (datacenter Blackwell only).
+ *
+ * Conventions for every call
+ *  - All pointers named *_dev (or documented as device) are CUDA device
+ *    pointers owned by the caller; the library never allocates or frees
+ *    memory and keeps no state between calls.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is enqueued asynchronously on it.
+ *  - Argument errors are detected on the host before any launch and return
+ *    LPFA_ERR_INVALID_ARG / LPFA_ERR_UNSUPPORTED; launch failures return
+ *    LPFA_ERR_CUDA.  Kernels never trap: a bounded wait that expires records
+ *    an error word in the caller's workspace, which lpfa_check() turns into
+ *    LPFA_ERR_TIMEOUT.
+ *  - Token-major data layout: a tensor is [T, H, D] with rows (tokens)
+ *    contiguous in H*D elements.  Dense BSHD [B, S, H, D] is the special case
+ *    T = B*S with B sequences of S tokens (lpfa_seqs with cu_seqlens NULL).
+ *  - Scale rows (see lpfa_seqs): scale tensors index tokens in a padded row
+ *    space where every sequence starts at a multiple of 128 rows; FP8 data
+ *    are never padded ([P1] paragraph 2, jagged module).
+ */
+#ifndef LPFA_H_
+#define LPFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LPFA_VERSION 1
+
+typedef enum lpfa_status {
+  LPFA_OK = 0,
+  LPFA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape or size  */
+  LPFA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, GPU)   */
+  LPFA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed           */
+  LPFA_ERR_TIMEOUT = 4       /* a kernel's bounded wait expired (lpfa_check) */
+} lpfa_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* lpfa_status_string(lpfa_status s);
+
+/* LPFA_VERSION of the built library. */
+int lpfa_version(void);
+
+/* Returns LPFA_OK when the current device is datacenter Blackwell with
+ * tensor memory (compute capability 10.x: sm_100/sm_103), else
+ * LPFA_ERR_UNSUPPORTED ([P3] "Hardware Portability Gate"; consumer SM120
+ * has no TMEM). */
+lpfa_status lpfa_device_supported(void);
+
+/* ------------------------------------------------------------------------
+ * Sequences.  Dense: nseq sequences of `seqlen` tokens each, cu_seqlens and
+ * cu_sf_rows NULL.  Jagged ([P1] paragraph 2): cu_seqlens (device int32,
+ * nseq+1 prefix offsets into the packed tokens) and cu_sf_rows (device
+ * int32, nseq+1) with cu_sf_rows[s] = sum_{t<s} ceil(L_t/128)*128, the first
+ * padded scale row of sequence s (lpfa_varlen_sf_rows computes it);
+ * `seqlen` is then the maximum sequence length.
+ * total_tokens = T, total_sf_rows = Tp = cu_sf_rows[nseq] (dense:
+ * nseq * ceil(seqlen/128) * 128).
+ * ---------------------------------------------------------------------- */
+typedef struct lpfa_seqs {
+  int64_t nseq;
+  int64_t seqlen;
+  int64_t total_tokens;
+  int64_t total_sf_rows;
+  const int32_t* cu_seqlens;   /* device, nseq+1, or NULL (dense) */
+  const int32_t* cu_sf_rows;   /* device, nseq+1, or NULL (dense) */
+} lpfa_seqs;
+
+/* Fill cu_sf_rows[0..nseq] (device int32) from cu_seqlens (device int32):
+ * cu_sf_rows[s] = sum_{t<s} ceil((cu_seqlens[t+1]-cu_seqlens[t])/128)*128.
+ * One small kernel on `stream`.  nseq in [1, 2^20]. */
+lpfa_status lpfa_varlen_sf_rows(const int32_t* cu_seqlens, int64_t nseq,
+                                int32_t* cu_sf_rows, void* stream);
+
+/* ------------------------------------------------------------------------
+ * MX quantizer ([P2] "Understanding OCP MXFP8 Microscaling on Blackwell";
+ * [P1] paragraphs 2-3).
+ *
+ * x: bf16 [T, heads, head_dim] (device, 16-byte aligned), head_dim in
+ * {64, 128}.  Every block of 32 elements (or 32x32) gets
+ *   amax = max |x|, e = clamp(floor(log2 amax) - 8, -127, 127),
+ *   scale code = e + 127 (E8M0; amax == 0 -> code 0; Inf/NaN -> 0xFF with
+ *   payloads 0x7F),
+ *   payload = E4M3(x * 2^-e), round to nearest even, saturating to +-448.
+ *
+ * Block shapes (lpfa_block):
+ *  LPFA_BLK_1X32   32 consecutive head_dim channels of one token (forward
+ *                  Q and K; backward V).
+ *  LPFA_BLK_32X1   32 consecutive tokens of one channel, blocks starting at
+ *                  each sequence start, the last one possibly short
+ *                  (forward V: the PV product contracts over keys).
+ *  LPFA_BLK_32X32  32 tokens x 32 channels, transpose-invariant (backward
+ *                  Q, K, dO).
+ *
+ * Outputs (device, caller-allocated; any of the scale outputs may be NULL):
+ *  out_e4m3    uint8 [T, heads, head_dim], same positions as x (unpadded).
+ *  out_sf      compact E8M0 scales:
+ *                1X32:  [T, heads, head_dim/32]
+ *                32X1:  [Tp/32, heads, head_dim]
+ *                32X32: [Tp/32, heads, head_dim/32]
+ *              (token blocks indexed in the padded scale-row space).
+ *  out_sf_mma  tensor-core scale layout for use with the contraction over
+ *              head_dim (1X32, 32X32) or over tokens (32X1):
+ *              [Tp/128, heads, 512] bytes; in each 512-byte tile operand row
+ *              r (token, or channel for 32X1) and contraction block kb sit at
+ *              byte (r%32)*16 + (r/32)*4 + kb.
+ *  out_sf_mma_t (32X32 only) the same square scales arranged for use with
+ *              the contraction over tokens (operand rows = channels):
+ *              [Tp/128, heads, 512].  With out_sf_mma this is the pair of
+ *              scale layouts of one quantized payload ([P1] paragraph 2).
+ * Padding bytes of the scale outputs are written as 0.
+ * ---------------------------------------------------------------------- */
+typedef enum lpfa_block {
+  LPFA_BLK_1X32 = 0,
+  LPFA_BLK_32X1 = 1,
+  LPFA_BLK_32X32 = 2
+} lpfa_block;
+
+lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
+                             int64_t heads, int64_t head_dim, lpfa_block blk,
+                             void* out_e4m3, void* out_sf, void* out_sf_mma,
+                             void* out_sf_mma_t, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Block-scaled MXFP8 GEMM (measures the dense MX MMA rate in the same run as
+ * the attention kernels; also the tcgen05 block-scale bring-up).
+ *   D[M, N] (fp32, row-major, ldd = N) = A[M, K] * B[N, K]^T
+ * A, B: e4m3, K contiguous (row-major [M, K] / [N, K]); sfa_mma, sfb_mma:
+ * tensor-core scale layout of their 1x32 (along K) scales,
+ * [M/128][K/128][512] and [N/128][K/128][512] bytes (tile (i, kt) holds rows
+ * 128i.. and contraction blocks 4kt..4kt+3).  M, N multiples of 128, K a
+ * multiple of 128.  Persistent kernel, one CTA per SM.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
+                         const void* sfb_mma, float* d, int64_t M, int64_t N,
+                         int64_t K, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Attention descriptor.
+ *  heads_q % heads_kv == 0 (GQA: query head h reads kv head
+ *  h / (heads_q/heads_kv)); head_dim in {64, 128}.
+ *  softmax_scale c: logits are c * q.k ([P2] "PyTorch Integration" example,
+ *  default 1/sqrt(head_dim)).
+ *  causal: key j visible to query i iff j <= i within a sequence.
+ *  rescale_threshold (log2 units, >= 0): selective rescaling ([P3]
+ *  "Technical Deep Dive"): the running reference max of a row moves to a
+ *  key tile's max only when that exceeds it by more than the threshold; P
+ *  is quantized against the reference max in force ([P1] paragraph 3).
+ *  dq_static_scale: power of two multiplying dQ partials before the FP16
+ *  accumulation ([P1] paragraph 3); lpfa_bwd divides it out at the end.
+ * ---------------------------------------------------------------------- */
+typedef struct lpfa_attn_desc {
+  lpfa_seqs seqs;
+  int64_t heads_q;
+  int64_t heads_kv;
+  int64_t head_dim;
+  float softmax_scale;
+  int32_t causal;
+  float rescale_threshold;
+  float dq_static_scale;
+} lpfa_attn_desc;
+
+/* Bytes of device workspace lpfa_fwd / lpfa_bwd need (>= 256; the first 16
+ * bytes hold the error word read by lpfa_check). */
+size_t lpfa_fwd_workspace_size(const lpfa_attn_desc* desc);
+size_t lpfa_bwd_workspace_size(const lpfa_attn_desc* desc);
+
+/* Forward ([P1] paragraphs 2-3, [P2] "Key Algorithmic Innovations" 1-2).
+ *  q8 [T, Hq, D], k8 [T, Hkv, D]: e4m3 payloads of 1X32 quantization;
+ *  sfq_mma [Tp/128, Hq, 512], sfk_mma [Tp/128, Hkv, 512]: their out_sf_mma.
+ *  v8 [T, Hkv, D]: e4m3 payload of 32X1 quantization; sfv_mma
+ *  [Tp/128, Hkv, 512]: its out_sf_mma.
+ *  o: bf16 [T, Hq, D] = softmax(c q k^T) v (normalised).
+ *  lse: fp32 [Hq, T], natural-log sum_j exp(c q_i.k_j).
+ *  workspace: >= lpfa_fwd_workspace_size bytes, 256-byte aligned; zeroed
+ *  by the call before use.
+ * All data pointers 16-byte aligned. */
+lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
+                     const void* sfq_mma, const void* k8, const void* sfk_mma,
+                     const void* v8, const void* sfv_mma, void* o, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward ([P1] paragraphs 2-3).
+ *  q8, k8, do8: e4m3 payloads of 32X32 quantization, with both scale
+ *  arrangements (sf*_mma: contraction over head_dim; sf*_mma_t: contraction
+ *  over tokens).  v8/sfv_mma: 1X32 quantization of V.
+ *  o (bf16 [T, Hq, D]) and dout (bf16 [T, Hq, D]) give D_i = sum_d dO*O;
+ *  lse: the forward's fp32 [Hq, T].
+ *  dq: fp16 [T, Hq, D] (zeroed and accumulated by the call; holds dQ after
+ *  the call, the static scale divided out); dk, dv: bf16 [T, Hkv, D].
+ *  workspace: >= lpfa_bwd_workspace_size bytes. */
+lpfa_status lpfa_bwd(const lpfa_attn_desc* desc,
+                     const void* q8, const void* sfq_mma, const void* sfq_mma_t,
+                     const void* k8, const void* sfk_mma, const void* sfk_mma_t,
+                     const void* v8, const void* sfv_mma,
+                     const void* do8, const void* sfdo_mma,
+                     const void* sfdo_mma_t,
+                     const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, reads the error word of a workspace used by
+ * lpfa_fwd / lpfa_bwd and returns LPFA_ERR_TIMEOUT if a kernel recorded an
+ * expired wait, LPFA_ERR_CUDA if the stream holds an error, else LPFA_OK. */
+lpfa_status lpfa_check(const void* workspace, void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* LPFA_H_ */

@@ -1,0 +1,13 @@
+"""lpfa: MXFP8 block-scaled FlashAttention (forward and backward) for GB300.
+
+The compute path is the CUDA library ``liblpfa.so`` (C ABI, include/lpfa.h);
+this package holds its sources (``csrc/``), its build script (``build.py``)
+and a thin ctypes binding (``lpfa.py``).  ``import
+mxfp8_block_scaled_quantizer_gb300.lpfa`` raises if the library is missing.
+"""
+__all__ = ["build"]
+
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    from .build import build as _build
+    return _build(verbose=verbose, force=force)

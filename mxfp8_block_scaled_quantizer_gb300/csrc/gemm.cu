@@ -1,0 +1,277 @@
+// Block-scaled MXFP8 GEMM on tcgen05: D[M,N] (fp32) = A[M,K] * B[N,K]^T.
+//
+// Purpose: the dense MX MMA rate of this GPU, measured in the same run as the
+// attention kernels ("Low Precision Flash Attention 4 ...", paragraph 2:
+// tcgen05.mma.block_scale on MXFP8 operands), and the bring-up of the
+// descriptors, TMEM scale layout and pipelines the attention kernels reuse.
+//
+// Design (one CTA per SM, persistent over 128x256 output tiles):
+//   warp 0      TMA producer: A tile 128x128 B, B tile 256x128 B (128-byte
+//               swizzle, K-major) + three 512-byte scale tiles per stage.
+//   warp 1      TMEM allocator and MMA issuer: per stage copies the scale
+//               tiles into TMEM (tcgen05.cp) and issues 4 MMAs of K = 32.
+//   warps 2-5   epilogue: TMEM -> registers -> fp32 global stores; the
+//               accumulator is released as soon as it has been read so the
+//               next tile's main loop overlaps the stores.
+#include <cuda_runtime.h>
+
+#include "lpfa_device.cuh"
+#include "lpfa_internal.h"
+
+namespace lpfa {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;            // bytes = fp8 elements per stage
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK;  // 16 KB
+constexpr int kBBytes = kBN * kBK;  // 32 KB
+constexpr int kSfBytes = 512;
+constexpr int kStageTx = kABytes + kBBytes + 3 * kSfBytes;   // bytes landed
+constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;   // 1024-aligned
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr int kSfCol0 = 256;        // TMEM scale buffers after the accumulator
+constexpr int kSfColsPerStage = 12; // 4 (A) + 8 (B, two 128-row tiles)
+
+struct GemmArgs {
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  float* d;
+  int32_t M, N, K;
+  int32_t tiles_m, tiles_n, kt;
+  uint32_t* err;
+};
+
+struct __align__(8) GemmSmem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full;
+  uint64_t acc_empty;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                   const __grid_constant__ CUtensorMap tma_b,
+                   const GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // stage buffers start 1024-aligned (128-byte swizzle atoms)
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GemmSmem* sh = reinterpret_cast<GemmSmem*>(stage_base + kStages * kStageBytes);
+  volatile int* abort = &sh->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ntiles = g.tiles_m * g.tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->acc_full, 1);
+    mbar_init(&sh->acc_empty, 4);
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int issued[kStages];     // parity of the last load issued per stage
+      for (int s = 0; s < kStages; ++s) issued[s] = -1;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+        const int tm = t % g.tiles_m, tn = t / g.tiles_m;
+        for (int kt = 0; kt < g.kt && ok; ++kt) {
+          ok = mbar_wait(&sh->empty[stage], phase ^ 1, g.err, abort, 1);
+          if (!ok) break;
+          uint8_t* buf = stage_base + stage * kStageBytes;
+          uint64_t* bar = &sh->full[stage];
+          mbar_arrive_expect_tx(bar, kStageTx);
+          tma_load_2d(buf, &tma_a, kt * kBK, tm * kBM, bar);
+          tma_load_2d(buf + kABytes, &tma_b, kt * kBK, tn * kBN, bar);
+          uint8_t* sfbuf = buf + kABytes + kBBytes;
+          bulk_load(sfbuf, g.sfa + (static_cast<int64_t>(tm) * g.kt + kt) * kSfBytes,
+                    kSfBytes, bar);
+          bulk_load(sfbuf + kSfBytes,
+                    g.sfb + (static_cast<int64_t>(2 * tn) * g.kt + kt) * kSfBytes,
+                    kSfBytes, bar);
+          bulk_load(sfbuf + 2 * kSfBytes,
+                    g.sfb + (static_cast<int64_t>(2 * tn + 1) * g.kt + kt) * kSfBytes,
+                    kSfBytes, bar);
+          issued[stage] = static_cast<int>(phase);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+      }
+      // on abort: wait (bounded) until every issued load has landed
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s] >= 0)
+            mbar_wait(&sh->full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_mxf8(kBM, kBN, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++local) {
+        if (local > 0) {
+          ok = mbar_wait(&sh->acc_empty, acc_phase ^ 1, g.err, abort, 2);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < g.kt; ++kt) {
+          ok = mbar_wait(&sh->full[stage], phase, g.err, abort, 3);
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* buf = stage_base + stage * kStageBytes;
+          const uint32_t a_addr = smem_u32(buf);
+          const uint32_t b_addr = smem_u32(buf + kABytes);
+          const uint32_t sf_addr = smem_u32(buf + kABytes + kBBytes);
+          const uint32_t sfa_t = tmem + kSfCol0 + stage * kSfColsPerStage;
+          const uint32_t sfb_t = sfa_t + 4;
+          tc_cp_32x128b_warpx4(sfa_t, sf_tile_desc(sf_addr));
+          tc_cp_32x128b_warpx4(sfb_t, sf_tile_desc(sf_addr + kSfBytes));
+          tc_cp_32x128b_warpx4(sfb_t + 4, sf_tile_desc(sf_addr + 2 * kSfBytes));
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint64_t ad = make_sdesc(a_addr + kb * 32, 16, 1024, 2);
+            const uint64_t bd = make_sdesc(b_addr + kb * 32, 16, 1024, 2);
+            mma_mxf8_ss(tmem, ad, bd, idesc_sf_ids(idesc, kb, kb), sfa_t, sfb_t,
+                        (kt | kb) != 0);
+          }
+          tc_commit(&sh->empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit(&sh->acc_full);
+        acc_phase ^= 1;
+      }
+      if (!ok) *abort = 1;
+      // every issued MMA has completed before TMEM is released
+      tc_commit(&sh->drain);
+      mbar_wait(&sh->drain, 0, nullptr, nullptr, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+      const int tm = t % g.tiles_m, tn = t / g.tiles_m;
+      ok = mbar_wait(&sh->acc_full, acc_phase, g.err, abort, 4);
+      if (!ok) break;
+      acc_phase ^= 1;
+      tc_fence_after();
+      const int row = tm * kBM + q * 32 + lane;
+      float* drow = g.d + static_cast<int64_t>(row) * g.N + tn * kBN;
+      uint32_t r[32];
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        tmem_ld32(tmem_addr(tmem, q * 32, c * 32), r);
+        tmem_ld_wait();
+        if (c == kBN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->acc_empty);
+        }
+        float4* dst = reinterpret_cast<float4*>(drow + c * 32);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+}  // namespace lpfa
+
+using namespace lpfa;
+
+extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
+                                    const void* b8, const void* sfb_mma,
+                                    float* d, int64_t M, int64_t N, int64_t K,
+                                    void* stream) {
+  LPFA_CHECK_ARG(a8 && sfa_mma && b8 && sfb_mma && d);
+  LPFA_CHECK_ARG(aligned16(a8) && aligned16(b8) && aligned16(sfa_mma) &&
+                 aligned16(sfb_mma) && aligned16(d));
+  LPFA_CHECK_ARG(M > 0 && N > 0 && K > 0);
+  if (M % kBM != 0 || N % kBN != 0 || K % kBK != 0) return LPFA_ERR_UNSUPPORTED;
+  LPFA_CHECK_ARG(M < (1 << 20) && N < (1 << 20) && K < (1 << 20));
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap ta, tb;
+  {
+    uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    uint64_t strides[1] = {static_cast<uint64_t>(K)};
+    uint32_t box[2] = {kBK, kBM};
+    lpfa_status st = encode_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a8, dims,
+                                 strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != LPFA_OK) return st;
+  }
+  {
+    uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+    uint64_t strides[1] = {static_cast<uint64_t>(K)};
+    uint32_t box[2] = {kBK, kBN};
+    lpfa_status st = encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b8, dims,
+                                 strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != LPFA_OK) return st;
+  }
+  GemmArgs g;
+  g.sfa = static_cast<const uint8_t*>(sfa_mma);
+  g.sfb = static_cast<const uint8_t*>(sfb_mma);
+  g.d = d;
+  g.M = static_cast<int32_t>(M);
+  g.N = static_cast<int32_t>(N);
+  g.K = static_cast<int32_t>(K);
+  g.tiles_m = static_cast<int32_t>(M / kBM);
+  g.tiles_n = static_cast<int32_t>(N / kBN);
+  g.kt = static_cast<int32_t>(K / kBK);
+  g.err = nullptr;
+
+  const size_t smem = kStages * kStageBytes + sizeof(GemmSmem) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    LPFA_CHECK_CUDA(cudaFuncSetAttribute(
+        mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(smem)));
+    attr_set = true;
+  }
+  const int ntiles = g.tiles_m * g.tiles_n;
+  const int grid = ntiles < num_sms() ? ntiles : num_sms();
+  mx_gemm_kernel<<<grid, kThreads, smem, cs>>>(ta, tb, g);
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}

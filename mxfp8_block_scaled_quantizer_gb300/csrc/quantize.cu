@@ -1,0 +1,207 @@
+// MX quantizer: bf16 -> E4M3 payload + E8M0 scales (compact and tensor-core
+// layouts).
+//
+// Rule ("Low-Precision FlashAttention-4 ...", "Understanding OCP MXFP8
+// Microscaling on Blackwell"; block shapes from "Low Precision Flash
+// Attention 4 ...", paragraphs 2-3): per block, amax = max|x|, scale code =
+// floor(log2 amax) - 8 + 127 clamped at 0 (taken from amax's exponent bits),
+// payload = RNE-satfinite E4M3 of x * 2^-e.
+//
+// One warp owns a 32-token x 32-channel tile of one head; lane i holds token
+// row i (64 contiguous bytes).  The block shape only changes how amax is
+// grouped: per lane (1x32), per column across lanes (32x1), or the whole
+// tile (32x32).  The kernel is a single pass over HBM: 2 bytes read and
+// 1 + 1/32 (+1/32 per extra scale layout) bytes written per element.
+#include <cuda_runtime.h>
+
+#include "lpfa_device.cuh"
+#include "lpfa_internal.h"
+#include "lpfa_seq.cuh"
+
+namespace lpfa {
+namespace {
+
+struct QuantArgs {
+  SeqView seqs;
+  const __nv_bfloat16* x;
+  uint8_t* out;
+  uint8_t* sf;        // compact
+  uint8_t* sf_mma;    // K-major tensor-core layout (32X1: contraction over tokens)
+  uint8_t* sf_mma_t;  // 32X32 only: contraction over tokens
+  int32_t H;
+  int32_t D;
+  int64_t ntiles;     // (Tp/32) * H * (D/32)
+};
+
+constexpr int kWarpsPerBlock = 8;
+
+__device__ __forceinline__ uint32_t abs_bits(float f) {
+  return __float_as_uint(f) & 0x7FFFFFFFu;
+}
+
+// Quantize 32 floats with one scale code into 32 bytes (8 words).
+__device__ __forceinline__ void quant_row(const float (&f)[32],
+                                          const uint32_t (&code)[32],
+                                          uint32_t (&w)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float a = f[4 * j + 0] * inv_scale_from_code(code[4 * j + 0]);
+    float b = f[4 * j + 1] * inv_scale_from_code(code[4 * j + 1]);
+    float c = f[4 * j + 2] * inv_scale_from_code(code[4 * j + 2]);
+    float d = f[4 * j + 3] * inv_scale_from_code(code[4 * j + 3]);
+    w[j] = cvt_e4m3x4(a, b, c, d);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (code[4 * j + q] == 0xFFu) w[j] = (w[j] & ~(0xFFu << (8 * q))) | (0x7Fu << (8 * q));
+  }
+}
+
+template <int kMode>  // 0: 1x32, 1: 32x1, 2: 32x32
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    mx_quantize_kernel(const QuantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tile =
+      static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (tile >= a.ntiles) return;
+  const int ncb = a.D >> 5;
+  const int cb = static_cast<int>(tile % ncb);
+  const int64_t t2 = tile / ncb;
+  const int h = static_cast<int>(t2 % a.H);
+  const int64_t rb = t2 / a.H;
+  const int64_t pr0 = rb * 32;  // first padded scale row of the block
+
+  const int s = seq_of_sf_row(a.seqs, pr0);
+  const SeqInfo si = seq_info(a.seqs, s);
+  const int64_t off = pr0 - si.sf_start;           // token offset in sequence
+  const int64_t nvalid64 = static_cast<int64_t>(si.len) - off;
+  const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : static_cast<int>(nvalid64));
+  const bool valid = lane < nvalid;
+  const int64_t tok = si.start + off + lane;
+  const int64_t elem0 = (tok * a.H + h) * a.D + 32 * cb;
+
+  float f[32];
+  {
+    uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
+                  make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (valid) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + elem0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __ldcs(src + i);
+    }
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      f[2 * i + 0] = __uint_as_float(u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  }
+
+  uint32_t code[32];
+  if (kMode == 0) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
+    const uint32_t c = e8m0_code_from_amax_bits(m);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) code[j] = c;
+  } else if (kMode == 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      code[j] = e8m0_code_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(f[j])));
+  } else {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
+    const uint32_t c = e8m0_code_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, m));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) code[j] = c;
+  }
+
+  if (valid) {
+    uint32_t w[8];
+    quant_row(f, code, w);
+    uint4* dst = reinterpret_cast<uint4*>(a.out + elem0);
+    __stcs(dst + 0, make_uint4(w[0], w[1], w[2], w[3]));
+    __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
+  }
+
+  // ---- scales
+  const int64_t tile128 = (rb >> 2) * a.H + h;   // [Tp/128, H] index
+  const int kb_row = static_cast<int>(rb & 3);   // token block within tile
+  if (kMode == 0) {
+    const uint8_t c = static_cast<uint8_t>(code[0]);
+    if (a.sf != nullptr && valid) a.sf[(tok * a.H + h) * (a.D >> 5) + cb] = c;
+    if (a.sf_mma != nullptr)
+      a.sf_mma[tile128 * 512 + lane * 16 + kb_row * 4 + cb] = valid ? c : 0;
+  } else if (kMode == 1) {
+    // lane j reports channel 32*cb + j
+    uint32_t cj = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cj = (lane == j) ? code[j] : cj;
+    if (a.sf != nullptr) a.sf[(rb * a.H + h) * a.D + 32 * cb + lane] = static_cast<uint8_t>(cj);
+    if (a.sf_mma != nullptr)
+      a.sf_mma[tile128 * 512 + lane * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(cj);
+  } else {
+    const uint8_t c = static_cast<uint8_t>(code[0]);
+    if (a.sf != nullptr && lane == 0) a.sf[(rb * a.H + h) * (a.D >> 5) + cb] = c;
+    if (a.sf_mma != nullptr)
+      a.sf_mma[tile128 * 512 + lane * 16 + kb_row * 4 + cb] = valid ? c : 0;
+    if (a.sf_mma_t != nullptr)
+      a.sf_mma_t[tile128 * 512 + lane * 16 + cb * 4 + kb_row] = c;
+  }
+}
+
+}  // namespace
+}  // namespace lpfa
+
+using namespace lpfa;
+
+extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
+                                        int64_t heads, int64_t head_dim,
+                                        lpfa_block blk, void* out_e4m3,
+                                        void* out_sf, void* out_sf_mma,
+                                        void* out_sf_mma_t, void* stream) {
+  SeqView sv;
+  lpfa_status st = make_seq_view(seqs, &sv);
+  if (st != LPFA_OK) return st;
+  LPFA_CHECK_ARG(x != nullptr && out_e4m3 != nullptr);
+  LPFA_CHECK_ARG(aligned16(x) && aligned16(out_e4m3));
+  LPFA_CHECK_ARG(heads >= 1 && heads <= 4096);
+  LPFA_CHECK_ARG(blk == LPFA_BLK_1X32 || blk == LPFA_BLK_32X1 ||
+                 blk == LPFA_BLK_32X32);
+  LPFA_CHECK_ARG(out_sf_mma_t == nullptr || blk == LPFA_BLK_32X32);
+  if (head_dim != 64 && head_dim != 128) return LPFA_ERR_UNSUPPORTED;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (sv.total_tokens == 0) return LPFA_OK;
+
+  const int64_t Tp = sv.total_sf_rows;
+  const int64_t mma_bytes = (Tp / 128) * heads * 512;
+  // head_dim 64 leaves half of each tensor-core scale tile unused: zero it.
+  if (head_dim < 128) {
+    if (out_sf_mma != nullptr)
+      LPFA_CHECK_CUDA(cudaMemsetAsync(out_sf_mma, 0, mma_bytes, cs));
+    if (out_sf_mma_t != nullptr)
+      LPFA_CHECK_CUDA(cudaMemsetAsync(out_sf_mma_t, 0, mma_bytes, cs));
+  }
+
+  QuantArgs a;
+  a.seqs = sv;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.out = static_cast<uint8_t*>(out_e4m3);
+  a.sf = static_cast<uint8_t*>(out_sf);
+  a.sf_mma = static_cast<uint8_t*>(out_sf_mma);
+  a.sf_mma_t = static_cast<uint8_t*>(out_sf_mma_t);
+  a.H = static_cast<int32_t>(heads);
+  a.D = static_cast<int32_t>(head_dim);
+  a.ntiles = (Tp / 32) * heads * (head_dim / 32);
+  const int64_t blocks = ceil_div(a.ntiles, kWarpsPerBlock);
+  LPFA_CHECK_ARG(blocks < (1ll << 31));
+  dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
+  switch (blk) {
+    case LPFA_BLK_1X32: mx_quantize_kernel<0><<<grid, block, 0, cs>>>(a); break;
+    case LPFA_BLK_32X1: mx_quantize_kernel<1><<<grid, block, 0, cs>>>(a); break;
+    case LPFA_BLK_32X32: mx_quantize_kernel<2><<<grid, block, 0, cs>>>(a); break;
+  }
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}

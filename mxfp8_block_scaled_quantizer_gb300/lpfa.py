@@ -1,0 +1,251 @@
+"""Thin ctypes binding of liblpfa.so (the C ABI in include/lpfa.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  torch supplies device memory and the current
+stream.  Importing this module fails loudly when liblpfa.so has not been
+built; there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblpfa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with "
+        "`python -m mxfp8_block_scaled_quantizer_gb300.build` (needs nvcc).")
+_lib = ctypes.CDLL(LIB_PATH)
+
+LPFA_OK, LPFA_ERR_INVALID_ARG, LPFA_ERR_UNSUPPORTED, LPFA_ERR_CUDA, \
+    LPFA_ERR_TIMEOUT = range(5)
+LPFA_BLK_1X32, LPFA_BLK_32X1, LPFA_BLK_32X32 = range(3)
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class lpfa_seqs(ctypes.Structure):
+    _fields_ = [("nseq", _i64), ("seqlen", _i64), ("total_tokens", _i64),
+                ("total_sf_rows", _i64), ("cu_seqlens", _vp),
+                ("cu_sf_rows", _vp)]
+
+
+class lpfa_attn_desc(ctypes.Structure):
+    _fields_ = [("seqs", lpfa_seqs), ("heads_q", _i64), ("heads_kv", _i64),
+                ("head_dim", _i64), ("softmax_scale", ctypes.c_float),
+                ("causal", ctypes.c_int32),
+                ("rescale_threshold", ctypes.c_float),
+                ("dq_static_scale", ctypes.c_float)]
+
+
+def _sig(name, restype, *argtypes):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_status_string = _sig("lpfa_status_string", ctypes.c_char_p, ctypes.c_int)
+lpfa_version = _sig("lpfa_version", ctypes.c_int)
+_device_supported = _sig("lpfa_device_supported", ctypes.c_int)
+_varlen_sf_rows = _sig("lpfa_varlen_sf_rows", ctypes.c_int, _vp, _i64, _vp, _vp)
+_mx_quantize = _sig("lpfa_mx_quantize", ctypes.c_int,
+                    ctypes.POINTER(lpfa_seqs), _vp, _i64, _i64, ctypes.c_int,
+                    _vp, _vp, _vp, _vp, _vp)
+_mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                _i64, _i64, _i64, _vp)
+_fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
+               ctypes.POINTER(lpfa_attn_desc))
+_bwd_ws = _sig("lpfa_bwd_workspace_size", ctypes.c_size_t,
+               ctypes.POINTER(lpfa_attn_desc))
+_fwd = _sig("lpfa_fwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
+            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
+_bwd = _sig("lpfa_bwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
+            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+            _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
+_check = _sig("lpfa_check", ctypes.c_int, _vp, _vp)
+
+#: every symbol include/lpfa.h declares
+EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
+            "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_mx_gemm",
+            "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
+            "lpfa_bwd", "lpfa_check")
+
+
+class LpfaError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {lpfa_status_string(status)}")
+
+
+def lpfa_status_string(status: int) -> str:
+    return _status_string(status).decode()
+
+
+def _ok(status: int, call: str):
+    if status != LPFA_OK:
+        raise LpfaError(status, call)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+# ---------------------------------------------------------------- sequences
+@dataclass
+class Seqs:
+    """Sequence layout of token-major tensors (see lpfa_seqs)."""
+    nseq: int
+    seqlen: int
+    total_tokens: int
+    total_sf_rows: int
+    cu_seqlens: Optional[torch.Tensor] = None   # device int32 [nseq+1]
+    cu_sf_rows: Optional[torch.Tensor] = None   # device int32 [nseq+1]
+
+    def c(self) -> lpfa_seqs:
+        return lpfa_seqs(self.nseq, self.seqlen, self.total_tokens,
+                         self.total_sf_rows, _ptr(self.cu_seqlens),
+                         _ptr(self.cu_sf_rows))
+
+
+def dense_seqs(batch: int, seqlen: int) -> Seqs:
+    pad = -(-seqlen // 128) * 128
+    return Seqs(batch, seqlen, batch * seqlen, batch * pad)
+
+
+def varlen_seqs(cu_seqlens: torch.Tensor, lengths=None) -> Seqs:
+    """cu_seqlens: int32 prefix offsets (device or host).  The padded scale
+    row offsets are computed on the device by lpfa_varlen_sf_rows; the total
+    padded row count comes from the host copy of the lengths."""
+    cu_host = cu_seqlens.detach().to("cpu", torch.int64)
+    lens = cu_host[1:] - cu_host[:-1]
+    nseq = int(lens.numel())
+    total_sf = int(((lens + 127) // 128 * 128).sum())
+    cu_dev = cu_seqlens.to(device="cuda", dtype=torch.int32).contiguous()
+    cu_sf = torch.empty(nseq + 1, dtype=torch.int32, device="cuda")
+    lpfa_varlen_sf_rows(cu_dev, nseq, cu_sf)
+    return Seqs(nseq, int(lens.max()), int(cu_host[-1]), total_sf, cu_dev,
+                cu_sf)
+
+
+def lpfa_varlen_sf_rows(cu_seqlens: torch.Tensor, nseq: int,
+                        cu_sf_rows: torch.Tensor, stream=None):
+    _ok(_varlen_sf_rows(_ptr(cu_seqlens), nseq, _ptr(cu_sf_rows),
+                        _stream(stream)), "lpfa_varlen_sf_rows")
+
+
+def lpfa_device_supported() -> bool:
+    return _device_supported() == LPFA_OK
+
+
+# ---------------------------------------------------------------- quantizer
+@dataclass
+class MXTensor:
+    """E4M3 payload plus its E8M0 scales (compact and tensor-core layouts)."""
+    data: torch.Tensor          # uint8 [T, H, D]
+    sf: Optional[torch.Tensor]
+    sf_mma: Optional[torch.Tensor]
+    sf_mma_t: Optional[torch.Tensor]
+    block: int
+    seqs: Seqs
+
+
+def lpfa_mx_quantize(seqs: Seqs, x: torch.Tensor, block: int,
+                     out: torch.Tensor, sf=None, sf_mma=None, sf_mma_t=None,
+                     stream=None):
+    """Raw call: x bf16 [T, H, D] (contiguous, CUDA); outputs preallocated."""
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    T, H, D = x.shape
+    sc = seqs.c()
+    _ok(_mx_quantize(ctypes.byref(sc), _ptr(x), H, D, block, _ptr(out),
+                     _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _stream(stream)),
+        "lpfa_mx_quantize")
+
+
+def mx_quantize(x: torch.Tensor, block: int, seqs: Optional[Seqs] = None,
+                compact: bool = True, mma: bool = True,
+                stream=None) -> MXTensor:
+    """Quantize bf16 [B, S, H, D] or packed [T, H, D] (with ``seqs``)."""
+    if x.dim() == 4:
+        B, S, H, D = x.shape
+        if seqs is None:
+            seqs = dense_seqs(B, S)
+        x = x.reshape(B * S, H, D)
+    T, H, D = x.shape
+    x = x.contiguous()
+    Tp = seqs.total_sf_rows
+    dev = x.device
+    out = torch.empty((T, H, D), dtype=torch.uint8, device=dev)
+    sf = sf_mma = sf_mma_t = None
+    if compact:
+        shape = {LPFA_BLK_1X32: (T, H, D // 32), LPFA_BLK_32X1: (Tp // 32, H, D),
+                 LPFA_BLK_32X32: (Tp // 32, H, D // 32)}[block]
+        sf = torch.empty(shape, dtype=torch.uint8, device=dev)
+    if mma:
+        sf_mma = torch.empty((Tp // 128, H, 512), dtype=torch.uint8, device=dev)
+        if block == LPFA_BLK_32X32:
+            sf_mma_t = torch.empty((Tp // 128, H, 512), dtype=torch.uint8,
+                                   device=dev)
+    lpfa_mx_quantize(seqs, x, block, out, sf, sf_mma, sf_mma_t, stream)
+    return MXTensor(out, sf, sf_mma, sf_mma_t, block, seqs)
+
+
+# ---------------------------------------------------------------- GEMM
+def lpfa_mx_gemm(a8, sfa_mma, b8, sfb_mma, d, stream=None):
+    M, K = a8.shape
+    N = b8.shape[0]
+    _ok(_mx_gemm(_ptr(a8), _ptr(sfa_mma), _ptr(b8), _ptr(sfb_mma), _ptr(d),
+                 M, N, K, _stream(stream)), "lpfa_mx_gemm")
+
+
+# ---------------------------------------------------------------- attention
+def attn_desc(seqs: Seqs, heads_q: int, heads_kv: int, head_dim: int,
+              causal: bool, softmax_scale: Optional[float] = None,
+              rescale_threshold: float = 8.0,
+              dq_static_scale: float = 1.0) -> lpfa_attn_desc:
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(head_dim)
+    return lpfa_attn_desc(seqs.c(), heads_q, heads_kv, head_dim,
+                          softmax_scale, int(bool(causal)), rescale_threshold,
+                          dq_static_scale)
+
+
+def fwd_workspace_size(desc: lpfa_attn_desc) -> int:
+    return int(_fwd_ws(ctypes.byref(desc)))
+
+
+def bwd_workspace_size(desc: lpfa_attn_desc) -> int:
+    return int(_bwd_ws(ctypes.byref(desc)))
+
+
+def lpfa_fwd(desc, q8, sfq, k8, sfk, v8, sfv, o, lse, ws, stream=None):
+    _ok(_fwd(ctypes.byref(desc), _ptr(q8), _ptr(sfq), _ptr(k8), _ptr(sfk),
+             _ptr(v8), _ptr(sfv), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+             _stream(stream)), "lpfa_fwd")
+
+
+def lpfa_bwd(desc, q8, sfq, sfq_t, k8, sfk, sfk_t, v8, sfv, do8, sfdo,
+             sfdo_t, o, dout, lse, dq, dk, dv, ws, stream=None):
+    _ok(_bwd(ctypes.byref(desc), _ptr(q8), _ptr(sfq), _ptr(sfq_t), _ptr(k8),
+             _ptr(sfk), _ptr(sfk_t), _ptr(v8), _ptr(sfv), _ptr(do8),
+             _ptr(sfdo), _ptr(sfdo_t), _ptr(o), _ptr(dout), _ptr(lse),
+             _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+             _stream(stream)), "lpfa_bwd")
+
+
+def lpfa_check(ws: torch.Tensor, stream=None):
+    _ok(_check(_ptr(ws), _stream(stream)), "lpfa_check")

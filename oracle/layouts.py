@@ -39,47 +39,88 @@ def atom_offset(r, kb):
     return (r % 32) * 16 + (r // 32) * 4 + kb
 
 
+def _token_rows(cu_seqlens):
+    """(sequence id, padded scale row) of every token."""
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    lens = np.diff(cu)
+    sfs = sf_row_starts(cu)
+    seq = np.repeat(np.arange(len(lens)), lens)
+    i = np.arange(cu[-1]) - cu[seq]
+    return seq, sfs[seq] + i
+
+
 def mma_from_row_blocks(row_sc, cu_seqlens):
     """K-major arrangement from per-token scales row_sc [T, H, nkb]
     (nkb = D/32 <= 4).  Returns uint8 [Tp/128, H, 512]."""
     cu = np.asarray(cu_seqlens, dtype=np.int64)
     sfs = sf_row_starts(cu)
     T, H, nkb = row_sc.shape
-    out = np.zeros((sfs[-1] // 128, H, 512), dtype=np.uint8)
-    for s in range(len(cu) - 1):
-        for i in range(cu[s + 1] - cu[s]):
-            pr = sfs[s] + i
-            for kb in range(nkb):
-                out[pr // 128, :, atom_offset(pr % 128, kb)] = row_sc[cu[s] + i, :, kb]
-    return out
+    _, pr = _token_rows(cu)
+    out = np.zeros((sfs[-1] // 128, 512, H), dtype=np.uint8)
+    for kb in range(nkb):
+        out[pr // 128, atom_offset(pr % 128, kb), :] = row_sc[:, :, kb]
+    return np.ascontiguousarray(np.moveaxis(out, 2, 1))
 
 
-def mma_from_token_blocks(col_sc, cu_seqlens, D):
+def mma_from_token_blocks(col_sc, D):
     """MN-major arrangement from 32-token-block scales col_sc [Tp/32, H, D]
     (one scale per (token block, head_dim channel)).  Operand rows are the
     head_dim channels, contraction blocks the 4 token blocks of a tile."""
     nblk, H, d = col_sc.shape
     assert d == D
-    ntile = -(-nblk // 4)
-    out = np.zeros((ntile, H, 512), dtype=np.uint8)
-    for tb in range(nblk):
-        for ch in range(D):
-            out[tb // 4, :, atom_offset(ch, tb % 4)] = col_sc[tb, :, ch]
-    return out
+    out = np.zeros((-(-nblk // 4), 512, H), dtype=np.uint8)
+    tb, ch = np.meshgrid(np.arange(nblk), np.arange(D), indexing="ij")
+    out[tb // 4, atom_offset(ch, tb % 4), :] = col_sc[tb, :, ch]
+    return np.ascontiguousarray(np.moveaxis(out, 2, 1))
 
 
 def square_to_row(sq_sc, cu_seqlens):
     """Per-token view [T, H, D/32] of square scales [Tp/32, H, D/32]."""
-    cu = np.asarray(cu_seqlens, dtype=np.int64)
-    sfs = sf_row_starts(cu)
-    T = cu[-1]
-    out = np.zeros((T,) + sq_sc.shape[1:], dtype=np.uint8)
-    for s in range(len(cu) - 1):
-        for i in range(cu[s + 1] - cu[s]):
-            out[cu[s] + i] = sq_sc[(sfs[s] + i) // 32]
-    return out
+    _, pr = _token_rows(cu_seqlens)
+    return sq_sc[pr // 32]
 
 
 def square_to_col(sq_sc, D):
     """Per-(token block, channel) view [Tp/32, H, D] of square scales."""
     return np.repeat(sq_sc, 32, axis=2)[:, :, :D]
+
+
+def oracle_quantize(x, cu_seqlens, block):
+    """Oracle quantization of a token-major tensor x [T, H, D] with the
+    library's output layouts.  block: "1x32", "32x1" or "32x32".
+    Returns dict(payload [T,H,D] uint8, sf (compact), sf_mma, sf_mma_t)."""
+    from . import mx
+    x = np.asarray(x, dtype=np.float64)
+    T, H, D = x.shape
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    sfs = sf_row_starts(cu)
+    out = {"sf_mma_t": None}
+    if block == "1x32":
+        p, sc = mx.quantize_1x32(x)
+        out.update(payload=p, sf=sc, sf_mma=mma_from_row_blocks(sc, cu))
+        return out
+    payload = np.zeros((T, H, D), dtype=np.uint8)
+    if block == "32x1":
+        sc = np.zeros((sfs[-1] // 32, H, D), dtype=np.uint8)
+        for s in range(len(cu) - 1):
+            a, b = cu[s], cu[s + 1]
+            if b == a:
+                continue
+            p, c = mx.quantize_along_rows(x[a:b])
+            payload[a:b] = p
+            sc[sfs[s] // 32: sfs[s] // 32 + c.shape[0]] = c
+        out.update(payload=payload, sf=sc, sf_mma=mma_from_token_blocks(sc, D))
+        return out
+    assert block == "32x32"
+    sc = np.zeros((sfs[-1] // 32, H, D // 32), dtype=np.uint8)
+    for s in range(len(cu) - 1):
+        a, b = cu[s], cu[s + 1]
+        if b == a:
+            continue
+        p, c = mx.quantize_32x32(np.moveaxis(x[a:b], 2, 1))   # [L, D, H]
+        payload[a:b] = np.moveaxis(p, 1, 2)
+        sc[sfs[s] // 32: sfs[s] // 32 + c.shape[0]] = np.moveaxis(c, 1, 2)
+    row = square_to_row(sc, cu)
+    out.update(payload=payload, sf=sc, sf_mma=mma_from_row_blocks(row, cu),
+               sf_mma_t=mma_from_token_blocks(square_to_col(sc, D), D))
+    return out
