@@ -1,7 +1,7 @@
 """lpfa: MXFP8 block-scaled FlashAttention (forward and backward) for GB300.
 
 The compute path is the CUDA library ``liblpfa.so`` (C ABI, include/lpfa.h);
-this package holds its sources (``csrc/``), its build script (``build.py``)
+this package holds its sources (``csrc/``), its build script (``_builder.py``)
 and a thin ctypes binding (``lpfa.py``).  ``import
 mxfp8_block_scaled_quantizer_gb300.lpfa`` raises if the library is missing.
 """
@@ -9,5 +9,5 @@ __all__ = ["build"]
 
 
 def build(verbose: bool = False, force: bool = False) -> str:
-    from .build import build as _build
+    from ._builder import build as _build
     return _build(verbose=verbose, force=force)

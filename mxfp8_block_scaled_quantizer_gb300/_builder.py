@@ -1,6 +1,6 @@
 """Build liblpfa.so (the C-ABI CUDA library) in-tree for sm_103a.
 
-Usage: python -m mxfp8_block_scaled_quantizer_gb300.build [--verbose]
+Usage: python -m mxfp8_block_scaled_quantizer_gb300._builder [--verbose]
 
 Each translation unit under csrc/ is compiled in parallel with nvcc, then
 linked into mxfp8_block_scaled_quantizer_gb300/liblpfa.so.  Objects go to

@@ -1,0 +1,662 @@
+// MXFP8 block-scaled attention backward on tcgen05.
+//
+// Method ("Low Precision Flash Attention 4: End-to-End Block-Scaled Attention
+// for Blackwell", paragraphs 2-3): Q, K, dO arrive quantized in square 32x32
+// blocks, so one E4M3 payload serves both orientations of every GEMM (only
+// the scale arrangement differs); V in 1x32 blocks along head_dim.  Per key
+// tile the kernel recomputes P from the forward LSE, forms
+// dS = P o (dP - D) with D_i = rowsum(dO o O), quantizes P and dS online in
+// 32x32 blocks (per-lane max, then the warp-wide redux.sync.max.abs.f32), and
+// accumulates
+//   dV += P^T dO,  dK += dS^T Q   (TMEM-resident over the query loop)
+//   dQ^T = K^T dS^T               (per query step; scaled by softmax_scale *
+//                                  dq_static_scale, rounded to FP16 and added
+//                                  to the FP16 dQ in global memory with bulk
+//                                  reduce-adds)
+//
+// CTA = one 128-key tile of one (sequence, kv head); it loops over the query
+// heads of its GQA group and over 64-query steps (causal: from the diagonal).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
+// compute (thread = key row for S^T/dP^T, = head_dim channel for dQ^T).
+//
+// TMEM (512 columns):
+//   [  0,128) dK      [128,256) dV      [256,320) S^T -> P^T fp8 (16 cols)
+//   [320,384) dP^T -> dS^T fp8 (16 cols)   [384,448) dQ^T
+//   [448,512) scale factors (see kCol* below)
+#include <cuda_runtime.h>
+
+#include "lpfa_device.cuh"
+#include "lpfa_internal.h"
+#include "lpfa_seq.cuh"
+
+namespace lpfa {
+namespace {
+
+constexpr int kD = 128;          // head_dim of this kernel
+constexpr int kBN = 128;         // keys per CTA
+constexpr int kBQ = 64;          // queries per step
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320,
+                   kColDQ = 384;
+constexpr uint32_t kColSFK = 448, kColSFV = 452, kColSFKt = 456,
+                   kColSFQ = 460, kColSFdO = 464, kColSFQt = 468,
+                   kColSFdOt = 472, kColSFP = 476, kColSFdS = 480,
+                   kColSFdSB = 484;
+
+// shared memory layout (bytes from a 1024-aligned base)
+constexpr int kSmK = 0;                          // 128 x 128 B (SW128)
+constexpr int kSmV = kSmK + kBN * kD;            // 128 x 128 B
+constexpr int kSmStage0 = kSmV + kBN * kD;       // per stage: Q, dO, SFs, LSE2, Delta
+constexpr int kStQ = 0;
+constexpr int kStdO = kStQ + kBQ * kD;           // 8 KB each
+constexpr int kStSF = kStdO + kBQ * kD;          // SFQ, SFQt, SFdO, SFdOt (4 x 512)
+constexpr int kStLse = kStSF + 4 * 512;          // 64 floats
+constexpr int kStDelta = kStLse + kBQ * 4;       // 64 floats
+constexpr int kStageBytes = ((kStDelta + kBQ * 4) + 1023) / 1024 * 1024;
+constexpr int kSmDS = kSmStage0 + kStages * kStageBytes;   // 128 x 64 B (SW64)
+constexpr int kSmSFdS = kSmDS + kBN * kBQ;                 // 512 B
+constexpr int kSmSFkv = kSmSFdS + 512;                     // SFK, SFKt, SFV
+constexpr int kSmDQ = kSmSFkv + 3 * 512;                   // 2 x [64][128] fp16
+constexpr int kSmBar = kSmDQ + 2 * kBQ * kD * 2;
+constexpr int kSmTotal = kSmBar + 256;
+
+struct BwdParams {
+  SeqView seqs;
+  const uint8_t* sfq;    // [Tp/128, Hq, 512] contraction over head_dim
+  const uint8_t* sfq_t;  // contraction over tokens
+  const uint8_t* sfk;
+  const uint8_t* sfk_t;
+  const uint8_t* sfv;
+  const uint8_t* sfdo;
+  const uint8_t* sfdo_t;
+  const float* lse2;     // [Hq, Tp]  LSE * log2(e), padded rows
+  const float* delta;    // [Hq, Tp]
+  __half* dq;            // [T, Hq, D] fp16, accumulated
+  __nv_bfloat16* dk;     // [T, Hkv, D]
+  __nv_bfloat16* dv;
+  uint32_t* err;
+  int32_t hq, hkv, group;
+  int32_t causal;
+  float scale_log2;      // softmax_scale * log2(e)
+  float softmax_scale;
+  float dq_mult;         // softmax_scale * dq_static_scale
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[kStages];
+  uint64_t q_empty[kStages];
+  uint64_t st_ready;
+  uint64_t ds_ready;
+  uint64_t dq_full;
+  uint64_t dq_free;
+  uint64_t acc_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+struct KvItem {
+  int seq, ktile, kvh;
+  int64_t start;
+  int32_t len;
+  int64_t sf_tile0;   // first padded 128-row tile of the sequence
+};
+
+__device__ __forceinline__ KvItem kv_item(const BwdParams& p) {
+  KvItem w;
+  const int64_t idx = blockIdx.x;
+  w.kvh = static_cast<int>(idx % p.hkv);
+  const int64_t t = idx / p.hkv;       // padded tile index
+  w.seq = seq_of_sf_row(p.seqs, t * 128);
+  const SeqInfo si = seq_info(p.seqs, w.seq);
+  w.ktile = static_cast<int>((t * 128 - si.sf_start) / 128);
+  w.start = si.start;
+  w.len = si.len;
+  w.sf_tile0 = si.sf_start / 128;
+  return w;
+}
+
+// Quantize 32 values (one thread's row of a 32x32 block) with the block's
+// warp-wide amax.  Returns the E8M0 code; writes 8 packed words.
+__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&w)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+  const float amax = warp_max_abs(m);
+  const uint32_t code = e8m0_code_from_amax_bits(__float_as_uint(amax));
+  const float inv = inv_scale_from_code(code);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = cvt_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
+                      v[4 * i + 3] * inv);
+  if (code == 0xFFu) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
+  }
+  return code;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_attn_bwd_kernel(const __grid_constant__ CUtensorMap tma_q,
+                       const __grid_constant__ CUtensorMap tma_k,
+                       const __grid_constant__ CUtensorMap tma_v,
+                       const __grid_constant__ CUtensorMap tma_do,
+                       const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sm + kSmBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const KvItem w = kv_item(p);
+  const int k0 = w.ktile * kBN;                    // first key (in sequence)
+  if (k0 >= w.len) return;
+  const int qstep0 = p.causal ? (k0 / kBQ) : 0;    // first 64-query step
+  const int nqsteps = (w.len + kBQ - 1) / kBQ;
+  const int steps_per_head = nqsteps - qstep0;
+  const int nsteps = steps_per_head * p.group;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 1);
+    }
+    mbar_init(&bars->st_ready, 1);
+    mbar_init(&bars->ds_ready, 4);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 4);
+    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  // step i -> (query head, first query of the step)
+  auto step_head = [&](int i) { return w.kvh * p.group + i / steps_per_head; };
+  auto step_q0 = [&](int i) { return (qstep0 + i % steps_per_head) * kBQ; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tma_q);
+      tma_prefetch_desc(&tma_k);
+      tma_prefetch_desc(&tma_v);
+      tma_prefetch_desc(&tma_do);
+      const int32_t row_k = static_cast<int32_t>(w.start + k0);
+      const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * kBN * kD + 3 * 512);
+      tma_load_3d(sm + kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
+      tma_load_3d(sm + kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
+      bulk_load(sm + kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
+      bulk_load(sm + kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
+      bulk_load(sm + kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+      bool ok = true;
+      int issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = -1;
+      for (int i = 0; i < nsteps; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        ok = mbar_wait(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
+        if (!ok) break;
+        const int h = step_head(i), q0 = step_q0(i);
+        uint8_t* st = sm + kSmStage0 + s * kStageBytes;
+        uint64_t* bar = &bars->q_full[s];
+        mbar_arrive_expect_tx(bar, 2 * kBQ * kD + 4 * 512 + 2 * kBQ * 4);
+        const int32_t row_q = static_cast<int32_t>(w.start + q0);
+        tma_load_3d(st + kStQ, &tma_q, 0, h, row_q, bar);
+        tma_load_3d(st + kStdO, &tma_do, 0, h, row_q, bar);
+        const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
+        const int64_t qsf = (pr / 128) * p.hq + h;
+        bulk_load(st + kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
+        bulk_load(st + kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
+        bulk_load(st + kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
+        bulk_load(st + kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+        const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
+        bulk_load(st + kStLse, p.lse2 + rowoff, kBQ * 4, bar);
+        bulk_load(st + kStDelta, p.delta + rowoff, kBQ * 4, bar);
+        issued[s] = static_cast<int>(ph);
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s] >= 0)
+            mbar_wait(&bars->q_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+        mbar_wait(&bars->kv_full, 0, nullptr, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_st = idesc_mxf8(128, kBQ, 0, 0);     // S^T, dP^T
+      const uint32_t id_acc = idesc_mxf8(128, kD, 0, 1);     // dV, dK (B MN-major)
+      const uint32_t id_dq = idesc_mxf8(128, kBQ, 1, 1);     // dQ^T (A, B MN-major)
+      const uint32_t k_addr = smem_u32(sm + kSmK);
+      const uint32_t v_addr = smem_u32(sm + kSmV);
+      const uint32_t ds_addr = smem_u32(sm + kSmDS);
+      bool ok = mbar_wait(&bars->kv_full, 0, p.err, abort, 50);
+      if (ok) {
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + kColSFK, sf_tile_desc(smem_u32(sm + kSmSFkv)));
+        tc_cp_32x128b_warpx4(tmem + kColSFKt, sf_tile_desc(smem_u32(sm + kSmSFkv + 512)));
+        tc_cp_32x128b_warpx4(tmem + kColSFV, sf_tile_desc(smem_u32(sm + kSmSFkv + 1024)));
+      }
+      for (int i = 0; i < nsteps && ok; ++i) {
+        const int s = i % kStages;
+        ok = mbar_wait(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51);
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* st = sm + kSmStage0 + s * kStageBytes;
+        const uint32_t q_addr = smem_u32(st + kStQ);
+        const uint32_t do_addr = smem_u32(st + kStdO);
+        const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
+        tc_cp_32x128b_warpx4(tmem + kColSFQ, sf_tile_desc(smem_u32(st + kStSF)));
+        tc_cp_32x128b_warpx4(tmem + kColSFdO, sf_tile_desc(smem_u32(st + kStSF + 1024)));
+        // S^T = K Q^T and dP^T = V dO^T (contraction over head_dim)
+#pragma unroll
+        for (int kb = 0; kb < kD / 32; ++kb) {
+          mma_mxf8_ss(tmem + kColS, make_sdesc(k_addr + 32 * kb, 16, 1024, 2),
+                      make_sdesc(q_addr + 32 * kb, 16, 1024, 2),
+                      idesc_sf_ids(id_st, kb, kb), tmem + kColSFK,
+                      tmem + kColSFQ + 2 * half, kb > 0);
+        }
+#pragma unroll
+        for (int kb = 0; kb < kD / 32; ++kb) {
+          mma_mxf8_ss(tmem + kColDP, make_sdesc(v_addr + 32 * kb, 16, 1024, 2),
+                      make_sdesc(do_addr + 32 * kb, 16, 1024, 2),
+                      idesc_sf_ids(id_st, kb, kb), tmem + kColSFV,
+                      tmem + kColSFdO + 2 * half, kb > 0);
+        }
+        tc_commit(&bars->st_ready);
+        ok = mbar_wait(&bars->ds_ready, i & 1, p.err, abort, 52);
+        if (!ok) break;
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + kColSFQt, sf_tile_desc(smem_u32(st + kStSF + 512)));
+        tc_cp_32x128b_warpx4(tmem + kColSFdOt, sf_tile_desc(smem_u32(st + kStSF + 1536)));
+        tc_cp_32x128b_warpx4(tmem + kColSFdSB, sf_tile_desc(smem_u32(sm + kSmSFdS)));
+        // dV += P^T dO, dK += dS^T Q (contraction over the 64 queries)
+#pragma unroll
+        for (int kb = 0; kb < kBQ / 32; ++kb) {
+          const uint32_t sfb = kb + 2 * half;
+          mma_mxf8_ts(tmem + kColDV, tmem + kColS + 8 * kb,
+                      make_sdesc(do_addr + 32 * kD * kb, 16, 1024, 2),
+                      idesc_sf_ids(id_acc, kb, sfb), tmem + kColSFP,
+                      tmem + kColSFdOt, (i > 0) || (kb > 0));
+          mma_mxf8_ts(tmem + kColDK, tmem + kColDP + 8 * kb,
+                      make_sdesc(q_addr + 32 * kD * kb, 16, 1024, 2),
+                      idesc_sf_ids(id_acc, kb, sfb), tmem + kColSFdS,
+                      tmem + kColSFQt, (i > 0) || (kb > 0));
+        }
+        // dQ^T = K^T dS^T (contraction over the 128 keys)
+        if (i > 0) {
+          ok = mbar_wait(&bars->dq_free, (i - 1) & 1, p.err, abort, 53);
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kb = 0; kb < kBN / 32; ++kb) {
+          mma_mxf8_ss(tmem + kColDQ, make_sdesc(k_addr + 32 * kD * kb, 16, 1024, 2),
+                      make_sdesc(ds_addr + 32 * kBQ * kb, 16, 8 * kBQ, 4),
+                      idesc_sf_ids(id_dq, kb, kb), tmem + kColSFKt,
+                      tmem + kColSFdSB, kb > 0);
+        }
+        tc_commit(&bars->q_empty[s]);
+        tc_commit(&bars->dq_full);
+      }
+      if (ok) tc_commit(&bars->acc_done);
+      if (!ok) *abort = 1;
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr, nullptr, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- compute
+    const int quad = warp & 3;
+    const int m = quad * 32 + lane;               // key row (and channel for dQ^T)
+    const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
+    const int key = k0 + m;
+    const int ctid = threadIdx.x - 64;            // 0..127 among compute threads
+    bool ok = true;
+    for (int i = 0; i < nsteps && ok; ++i) {
+      const int s = i % kStages;
+      const int h = step_head(i), q0 = step_q0(i);
+      const float* lse2 = reinterpret_cast<const float*>(sm + kSmStage0 + s * kStageBytes + kStLse);
+      const float* dlt = reinterpret_cast<const float*>(sm + kSmStage0 + s * kStageBytes + kStDelta);
+      ok = mbar_wait(&bars->st_ready, i & 1, p.err, abort, 60);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t pw[16], dw[16];
+      uint32_t sfp = 0, sfds = 0;
+      uint8_t* ds_row = sm + kSmDS + m * kBQ;      // 64-byte row, 64B swizzle
+#pragma unroll
+      for (int jb = 0; jb < kBQ / 32; ++jb) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tmem + lb + kColS + 32 * jb, rs);
+        tmem_ld32(tmem + lb + kColDP + 32 * jb, rd);
+        tmem_ld_wait();
+        float pv[32], dsv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int qq = q0 + 32 * jb + j;
+          const bool masked = (key >= w.len) || (qq >= w.len) || (p.causal && key > qq);
+          const float x = fmaf(__uint_as_float(rs[j]), p.scale_log2, -lse2[32 * jb + j]);
+          const float pj = masked ? 0.f : ex2(x);
+          pv[j] = pj;
+          dsv[j] = pj * (__uint_as_float(rd[j]) - dlt[32 * jb + j]);
+        }
+        uint32_t wq[8];
+        const uint32_t cp_ = quant_block32(pv, wq);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) pw[8 * jb + t] = wq[t];
+        const uint32_t cd = quant_block32(dsv, wq);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) dw[8 * jb + t] = wq[t];
+        sfp |= cp_ << (8 * jb);
+        sfds |= cd << (8 * jb);
+        // dS^T row chunk -> shared memory (two 16-byte chunks of 64)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = 2 * jb + c;
+          const int phys = chunk ^ ((m >> 1) & 3);
+          *reinterpret_cast<uint4*>(ds_row + 16 * phys) =
+              make_uint4(wq[4 * c], wq[4 * c + 1], wq[4 * c + 2], wq[4 * c + 3]);
+        }
+        // B-operand scale of dQ^T: (query n = 32 jb + lane, key block quad)
+        sm[kSmSFdS + lane * 16 + jb * 4 + quad] = static_cast<uint8_t>(cd);
+      }
+      // P^T and dS^T (fp8) into TMEM over the consumed S^T / dP^T columns;
+      // their A-operand scales at lane m, column base + m/32
+      {
+        uint32_t r16[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) r16[t] = pw[t];
+        tmem_st16(tmem + lb + kColS, r16);
+#pragma unroll
+        for (int t = 0; t < 16; ++t) r16[t] = dw[t];
+        tmem_st16(tmem + lb + kColDP, r16);
+      }
+      tmem_st1(tmem + lb + kColSFP + quad, sfp);
+      tmem_st1(tmem + lb + kColSFdS + quad, sfds);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->ds_ready);
+
+      // dQ^T readout: thread = channel m, 64 queries
+      ok = mbar_wait(&bars->dq_full, i & 1, p.err, abort, 61);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t rq[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(tmem + lb + kColDQ, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rq[j] = r[j];
+        tmem_ld32(tmem + lb + kColDQ + 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rq[32 + j] = r[j];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->dq_free);
+      // stage fp16 rows [q][d] and reduce-add them into global dQ
+      __half* stg = reinterpret_cast<__half*>(sm + kSmDQ + (i & 1) * kBQ * kD * 2);
+      if (ctid == 0) bulk_wait_read_le1();
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int j = 0; j < kBQ; ++j)
+        stg[j * kD + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (ctid == 0) {
+        for (int j = 0; j < kBQ; ++j) {
+          const int qq = q0 + j;
+          if (qq >= w.len) break;
+          __half* gdst = p.dq + ((w.start + qq) * p.hq + h) * kD;
+          bulk_reduce_add_f16(gdst, stg + j * kD, kD * 2);
+        }
+        bulk_commit();
+      }
+    }
+    if (ctid == 0) bulk_wait0();
+    // epilogue: dK (times softmax_scale) and dV -> bf16
+    if (ok) ok = mbar_wait(&bars->acc_done, 0, p.err, abort, 62);
+    if (ok) {
+      tc_fence_after();
+      const bool valid = key < w.len;
+      const int64_t tok = w.start + key;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? kColDK : kColDV;
+        const float mul = which == 0 ? p.softmax_scale : 1.f;
+        __nv_bfloat16* out = (which == 0 ? p.dk : p.dv) + (tok * p.hkv + w.kvh) * kD;
+        uint4* dst = reinterpret_cast<uint4*>(out);
+        uint32_t r[32];
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          tmem_ld32(tmem + lb + col + 32 * c, r);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * t + 2 * k]) * mul,
+                                                          __uint_as_float(r[8 * t + 2 * k + 1]) * mul);
+                wv[k] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              dst[4 * c + t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// D_i = sum_d dO_id * O_id and LSE in log2 units, in the padded row layout.
+// One warp per (token, head).
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const SeqView sv, const __nv_bfloat16* __restrict__ o,
+                          const __nv_bfloat16* __restrict__ dout,
+                          const float* __restrict__ lse, float* __restrict__ lse2,
+                          float* __restrict__ delta, int32_t hq, int32_t d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= sv.total_tokens * hq) return;
+  const int64_t tok = row / hq;
+  const int h = static_cast<int>(row % hq);
+  float acc = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + row * d + c);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + row * d + c);
+    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 fa = __bfloat1622float2(a2[k]);
+      const float2 fb = __bfloat1622float2(b2[k]);
+      acc = fmaf(fa.x, fb.x, acc);
+      acc = fmaf(fa.y, fb.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    // padded row of this token
+    int s;
+    if (sv.cu_seqlens == nullptr) {
+      s = static_cast<int>(tok / sv.seqlen);
+    } else {
+      int lo = 0, hi = sv.nseq - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(sv.cu_seqlens + mid) <= tok) lo = mid; else hi = mid - 1;
+      }
+      s = lo;
+    }
+    const SeqInfo si = seq_info(sv, s);
+    const int64_t pr = si.sf_start + (tok - si.start);
+    const int64_t idx = static_cast<int64_t>(h) * sv.total_sf_rows + pr;
+    delta[idx] = acc;
+    lse2[idx] = lse[static_cast<int64_t>(h) * sv.total_tokens + tok] * 1.4426950408889634f;
+  }
+}
+
+__global__ void dq_unscale_kernel(__half2* __restrict__ dq, int64_t n2, float inv) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n2) {
+    float2 f = __half22float2(dq[i]);
+    dq[i] = __floats2half2_rn(f.x * inv, f.y * inv);
+  }
+}
+
+}  // namespace
+}  // namespace lpfa
+
+using namespace lpfa;
+
+namespace {
+size_t bwd_ws_bytes(const lpfa_attn_desc* desc) {
+  return 256 + 2 * static_cast<size_t>(desc->heads_q) *
+                   static_cast<size_t>(desc->seqs.total_sf_rows) * sizeof(float);
+}
+}  // namespace
+
+extern "C" size_t lpfa_bwd_workspace_size(const lpfa_attn_desc* desc) {
+  if (desc == nullptr) return 0;
+  return bwd_ws_bytes(desc);
+}
+
+extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
+                                const void* sfq_mma, const void* sfq_mma_t,
+                                const void* k8, const void* sfk_mma,
+                                const void* sfk_mma_t, const void* v8,
+                                const void* sfv_mma, const void* do8,
+                                const void* sfdo_mma, const void* sfdo_mma_t,
+                                const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  SeqView sv;
+  lpfa_status st = validate_attn(desc, &sv);
+  if (st != LPFA_OK) return st;
+  LPFA_CHECK_ARG(q8 && sfq_mma && sfq_mma_t && k8 && sfk_mma && sfk_mma_t && v8 &&
+                 sfv_mma && do8 && sfdo_mma && sfdo_mma_t && o && dout && lse &&
+                 dq && dk && dv);
+  const void* ptrs[] = {q8, sfq_mma, sfq_mma_t, k8, sfk_mma, sfk_mma_t, v8, sfv_mma,
+                        do8, sfdo_mma, sfdo_mma_t, o, dout, lse, dq, dk, dv};
+  for (const void* ptr : ptrs) LPFA_CHECK_ARG(aligned16(ptr));
+  LPFA_CHECK_ARG(workspace != nullptr &&
+                 (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0);
+  LPFA_CHECK_ARG(workspace_bytes >= bwd_ws_bytes(desc));
+  if (desc->head_dim != 128) return LPFA_ERR_UNSUPPORTED;
+  LPFA_CHECK_ARG(desc->dq_static_scale > 0.f);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (sv.total_tokens == 0) return LPFA_OK;
+  const int64_t hq = desc->heads_q, hkv = desc->heads_kv, D = desc->head_dim;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);
+  float* lse2 = reinterpret_cast<float*>(ws + 256);
+  float* delta = lse2 + hq * sv.total_sf_rows;
+  LPFA_CHECK_CUDA(cudaMemsetAsync(ws, 0, bwd_ws_bytes(desc), cs));
+  LPFA_CHECK_CUDA(cudaMemsetAsync(dq, 0, sv.total_tokens * hq * D * 2, cs));
+
+  {
+    const int64_t rows = sv.total_tokens * hq;
+    bwd_preprocess_kernel<<<static_cast<unsigned>(ceil_div(rows, 8)), 256, 0, cs>>>(
+        sv, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+        lse, lse2, delta, static_cast<int32_t>(hq), static_cast<int32_t>(D));
+    LPFA_CHECK_CUDA(cudaGetLastError());
+  }
+
+  CUtensorMap tq, tk, tv, tdo;
+  auto make = [&](CUtensorMap* m, const void* base, int64_t heads, uint32_t rows) {
+    uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
+                        static_cast<uint64_t>(sv.total_tokens)};
+    uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads * D)};
+    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, rows};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  if ((st = make(&tq, q8, hq, kBQ)) != LPFA_OK) return st;
+  if ((st = make(&tdo, do8, hq, kBQ)) != LPFA_OK) return st;
+  if ((st = make(&tk, k8, hkv, kBN)) != LPFA_OK) return st;
+  if ((st = make(&tv, v8, hkv, kBN)) != LPFA_OK) return st;
+
+  BwdParams p;
+  p.seqs = sv;
+  p.sfq = static_cast<const uint8_t*>(sfq_mma);
+  p.sfq_t = static_cast<const uint8_t*>(sfq_mma_t);
+  p.sfk = static_cast<const uint8_t*>(sfk_mma);
+  p.sfk_t = static_cast<const uint8_t*>(sfk_mma_t);
+  p.sfv = static_cast<const uint8_t*>(sfv_mma);
+  p.sfdo = static_cast<const uint8_t*>(sfdo_mma);
+  p.sfdo_t = static_cast<const uint8_t*>(sfdo_mma_t);
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.dq = static_cast<__half*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.err = err;
+  p.hq = static_cast<int32_t>(hq);
+  p.hkv = static_cast<int32_t>(hkv);
+  p.group = static_cast<int32_t>(hq / hkv);
+  p.causal = desc->causal ? 1 : 0;
+  p.scale_log2 = desc->softmax_scale * 1.4426950408889634f;
+  p.softmax_scale = desc->softmax_scale;
+  p.dq_mult = desc->softmax_scale * desc->dq_static_scale;
+
+  const int64_t nblocks = (sv.total_sf_rows / 128) * hkv;
+  LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
+  const size_t smem = kSmTotal + 1024;
+  static bool attr = false;
+  if (!attr) {
+    LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem)));
+    attr = true;
+  }
+  mx_attn_bwd_kernel<<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, tdo, p);
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  if (desc->dq_static_scale != 1.0f) {
+    const int64_t n2 = sv.total_tokens * hq * D / 2;
+    dq_unscale_kernel<<<static_cast<unsigned>(ceil_div(n2, 256)), 256, 0, cs>>>(
+        static_cast<__half2*>(dq), n2, 1.0f / desc->dq_static_scale);
+    LPFA_CHECK_CUDA(cudaGetLastError());
+  }
+  return LPFA_OK;
+}

@@ -1,0 +1,535 @@
+// MXFP8 block-scaled attention forward on tcgen05.
+//
+// Method ("Low Precision Flash Attention 4: End-to-End Block-Scaled Attention
+// for Blackwell", paragraphs 2-3; "Low-Precision FlashAttention-4 ...",
+// "Key Algorithmic Innovations" 1-2; "FlashAttention-4 Adds Low-Precision
+// Blackwell Support", "Technical Deep Dive"):
+//   S = Q K^T           block-scaled MXFP8 MMA into TMEM (fp32)
+//   online softmax      FP32 running reference max m and sum l per row, the
+//                       softmax scale folded into one FMA in log2 units;
+//                       m moves only when a tile's max exceeds it by more
+//                       than the rescale threshold (selective rescaling)
+//   P -> MXFP8          1x32 blocks along keys; each block's scale comes from
+//                       the block's logit maximum already computed for the
+//                       row max (amax(P) = exp2(max x - m)), so no extra pass
+//   O += P V            block-scaled MMA, P read from TMEM as the A operand
+//   epilogue            O / l -> bf16, LSE = (m + log2 l) ln 2
+//
+// CTA = one 128-query tile of one (sequence, head).  Warp roles:
+//   warp 0     TMA producer: Q tile once, then K_j, V_j and their scale tiles
+//              through a 3-stage shared-memory ring.
+//   warp 1     TMEM owner and MMA issuer (one thread).
+//   warps 2-5  softmax: thread i owns query row i = TMEM lane i.
+// TMEM columns (512): S double buffer [0,128) [128,256); O [256,256+D);
+// scale factors from column 384: SFQ (4), SFK per stage (4 each), SFV per
+// stage (4 each), SFP per S buffer (4 each).  P (fp8) overwrites the first
+// 32 columns of its S buffer after the row has been read.
+#include <cuda_runtime.h>
+
+#include "lpfa_device.cuh"
+#include "lpfa_internal.h"
+#include "lpfa_seq.cuh"
+
+namespace lpfa {
+namespace {
+
+constexpr int kBlockM = 128;   // queries per CTA
+constexpr int kBlockN = 128;   // keys per tile
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColSF = 384;
+constexpr uint32_t kColSFQ = kColSF;
+constexpr uint32_t kColSFK = kColSF + 4;                     // + 4*stage
+constexpr uint32_t kColSFV = kColSFK + 4 * kStages;          // + 4*stage
+constexpr uint32_t kColSFP = kColSFV + 4 * kStages;          // + 4*buffer
+
+struct FwdParams {
+  SeqView seqs;
+  const uint8_t* sfq;   // [Tp/128, Hq, 512]
+  const uint8_t* sfk;   // [Tp/128, Hkv, 512]
+  const uint8_t* sfv;   // [Tp/128, Hkv, 512]
+  __nv_bfloat16* o;     // [T, Hq, D]
+  float* lse;           // [Hq, T]
+  uint32_t* err;
+  int32_t hq, hkv, group;
+  int32_t ntile_q;      // dense: q tiles per sequence
+  int32_t causal;
+  float scale_log2;     // softmax_scale * log2(e)
+  float threshold;      // log2 units
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTile = kBlockN * D;          // bytes of one fp8 tile
+  static constexpr int kQ = 0;
+  static constexpr int kStage0 = kQ + kBlockM * D;   // stage s: K, V
+  static constexpr int kStageBytes = 2 * kTile;
+  static constexpr int kSf0 = kStage0 + kStages * kStageBytes;  // SFQ, then per stage SFK, SFV
+  static constexpr int kBar = kSf0 + 512 * (1 + 2 * kStages);
+  static constexpr int kTotal = kBar + 256;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+      "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]),
+      "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+      "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Work item of this CTA: (sequence, q tile, head); heavy causal tiles first.
+struct WorkItem {
+  int seq, qtile, head;
+  int64_t start;      // first token of the sequence
+  int32_t len;
+  int64_t sf_tile;    // padded 128-row tile index of this q tile
+};
+
+__device__ __forceinline__ WorkItem work_item(const FwdParams& p) {
+  WorkItem w;
+  const int64_t idx = blockIdx.x;
+  w.head = static_cast<int>(idx % p.hq);
+  const int64_t rest = idx / p.hq;
+  if (p.seqs.cu_seqlens == nullptr) {
+    const int nseq = p.seqs.nseq;
+    w.seq = static_cast<int>(rest % nseq);
+    w.qtile = p.ntile_q - 1 - static_cast<int>(rest / nseq);
+  } else {
+    // padded tile space enumerates every (sequence, q tile)
+    const int64_t t = rest;
+    w.seq = seq_of_sf_row(p.seqs, t * 128);
+    const SeqInfo si = seq_info(p.seqs, w.seq);
+    w.qtile = static_cast<int>((t * 128 - si.sf_start) / 128);
+  }
+  const SeqInfo si = seq_info(p.seqs, w.seq);
+  w.start = si.start;
+  w.len = si.len;
+  w.sf_tile = si.sf_start / 128 + w.qtile;
+  return w;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_attn_fwd_kernel(const __grid_constant__ CUtensorMap tma_q,
+                       const __grid_constant__ CUtensorMap tma_k,
+                       const __grid_constant__ CUtensorMap tma_v,
+                       const FwdParams p) {
+  using L = FwdSmem<D>;
+  constexpr uint32_t kSw = (D == 128) ? 2u : 4u;     // 128B / 64B swizzle
+  constexpr uint32_t kSbo = 8 * D;                    // 8 rows of D bytes
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  FwdBars* bars = reinterpret_cast<FwdBars*>(sm + L::kBar);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WorkItem w = work_item(p);
+  const int kvh = w.head / p.group;
+  const int q0 = w.qtile * kBlockM;                 // first query (in sequence)
+  if (q0 >= w.len) return;                          // uniform for the CTA
+  const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
+  const int ntiles = (kv_len + kBlockN - 1) / kBlockN;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->p_full[b], 4);
+      mbar_init(&bars->pv_done[b], 1);
+    }
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tma_q);
+      tma_prefetch_desc(&tma_k);
+      tma_prefetch_desc(&tma_v);
+      const int32_t row_q = static_cast<int32_t>(w.start + q0);
+      mbar_arrive_expect_tx(&bars->q_full, kBlockM * D + 512);
+      tma_load_3d(sm + L::kQ, &tma_q, 0, w.head, row_q, &bars->q_full);
+      bulk_load(sm + L::kSf0, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
+                &bars->q_full);
+      const int64_t kv_sf_tile0 = w.sf_tile - w.qtile;   // first tile of sequence
+      bool ok = true;
+      int issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = -1;
+      for (int j = 0; j < ntiles; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        ok = mbar_wait(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
+        if (!ok) break;
+        uint8_t* kbuf = sm + L::kStage0 + s * L::kStageBytes;
+        uint64_t* bar = &bars->kv_full[s];
+        mbar_arrive_expect_tx(bar, 2 * L::kTile + 1024);
+        const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
+        tma_load_3d(kbuf, &tma_k, 0, kvh, row_k, bar);
+        tma_load_3d(kbuf + L::kTile, &tma_v, 0, kvh, row_k, bar);
+        const int64_t sft = (kv_sf_tile0 + j) * p.hkv + kvh;
+        bulk_load(sm + L::kSf0 + 512 * (1 + s), p.sfk + sft * 512, 512, bar);
+        bulk_load(sm + L::kSf0 + 512 * (1 + kStages + s), p.sfv + sft * 512, 512, bar);
+        issued[s] = static_cast<int>(ph);
+      }
+      if (!ok) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s] >= 0)
+            mbar_wait(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+        mbar_wait(&bars->q_full, 0, nullptr, nullptr, 0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
+      const uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sm + L::kQ);
+      bool ok = mbar_wait(&bars->q_full, 0, p.err, abort, 20);
+      if (ok) {
+        tc_fence_after();
+        tc_cp_32x128b_warpx4(tmem + kColSFQ, sf_tile_desc(smem_u32(sm + L::kSf0)));
+      }
+      // issue S_j = Q K_j^T into S buffer j%2
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kStages;
+        if (!mbar_wait(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21)) return false;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes);
+        const uint32_t sfk_t = tmem + kColSFK + 4 * s;
+        tc_cp_32x128b_warpx4(sfk_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (1 + s))));
+        const uint32_t d_t = tmem + kColS0 + 128 * (j & 1);
+#pragma unroll
+        for (int kb = 0; kb < D / 32; ++kb) {
+          mma_mxf8_ss(d_t, make_sdesc(q_addr + 32 * kb, 16, kSbo, kSw),
+                      make_sdesc(k_addr + 32 * kb, 16, kSbo, kSw),
+                      idesc_sf_ids(idesc_s, kb, kb), tmem + kColSFQ, sfk_t, kb > 0);
+        }
+        tc_commit(&bars->s_full[j & 1]);
+        return true;
+      };
+      // issue O += P_j V_j
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j % kStages, b = j & 1;
+        if (!mbar_wait(&bars->p_full[b], (j >> 1) & 1, p.err, abort, 22)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes + L::kTile);
+        const uint32_t sfv_t = tmem + kColSFV + 4 * s;
+        tc_cp_32x128b_warpx4(sfv_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (1 + kStages + s))));
+        const uint32_t p_t = tmem + kColS0 + 128 * b;
+#pragma unroll
+        for (int kb = 0; kb < kBlockN / 32; ++kb) {
+          mma_mxf8_ts(tmem + kColO, p_t + 8 * kb,
+                      make_sdesc(v_addr + 32 * D * kb, 16, kSbo, kSw),
+                      idesc_sf_ids(idesc_o, kb, kb), tmem + kColSFP + 4 * b, sfv_t,
+                      (j > 0) || (kb > 0));
+        }
+        tc_commit(&bars->kv_empty[s]);
+        tc_commit(&bars->pv_done[b]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 1; j < ntiles && ok; ++j) {
+        ok = issue_s(j);
+        if (ok) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(ntiles - 1);
+      if (!ok) *abort = 1;
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, nullptr, nullptr, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int quad = warp & 3;                    // TMEM lane quarter
+    const int row = quad * 32 + lane;             // query row within tile
+    const int qi = q0 + row;                      // query index in sequence
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float c2 = p.scale_log2;
+    float m_ref = -INFINITY;                      // log2 units
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int b = j & 1;
+      ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, p.err, abort, 30);
+      if (!ok) break;
+      tc_fence_after();
+      float s[kBlockN];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          tmem_ld32(tmem + lane_base + kColS0 + 128 * b + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
+        }
+      }
+      // masking: keys beyond the sequence, and causal j > i
+      const int k0 = j * kBlockN;
+      const bool need_mask = (k0 + kBlockN > w.len) || (p.causal && k0 + kBlockN - 1 > q0);
+      if (need_mask) {
+        const int lim = p.causal ? min(w.len, qi + 1) : w.len;
+#pragma unroll
+        for (int i = 0; i < kBlockN; ++i)
+          if (k0 + i >= lim) s[i] = -INFINITY;
+      }
+      // chunk and tile maxima (raw logits; c2 > 0 so the order is kept)
+      float cmax[kBlockN / 32];
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        float mx = s[32 * c];
+#pragma unroll
+        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[32 * c + i]);
+        cmax[c] = mx;
+      }
+      float tmax = cmax[0];
+#pragma unroll
+      for (int c = 1; c < kBlockN / 32; ++c) tmax = fmaxf(tmax, cmax[c]);
+      const float mt = __fmul_rn(tmax, c2);
+      float m_new = m_ref;
+      if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
+      const bool moved = (m_new != m_ref);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
+      // P = exp2(x - m) with x = fl(s*c2) rounded on its own (no fused
+      // multiply-add), so the element that defines m gives exactly 2^0 and
+      // the block holding it gets the scale of amax = 1.  Quantized per
+      // 32-key block; the block amax reuses the chunk maxima of the row max.
+      uint32_t pw[32];
+      uint32_t sfp = 0;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c) {
+        const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
+        const uint32_t code = e8m0_code_from_amax_bits(__float_as_uint(amax));
+        const float inv = inv_scale_from_code(code);
+        sfp |= code << (8 * c);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float p0 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 0], c2), m_use));
+          const float p1 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 1], c2), m_use));
+          const float p2 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 2], c2), m_use));
+          const float p3 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 3], c2), m_use));
+          lsum += (p0 + p1) + (p2 + p3);
+          pw[8 * c + i / 4] = cvt_e4m3x4(p0 * inv, p1 * inv, p2 * inv, p3 * inv);
+        }
+      }
+      // P and its scales into TMEM (S columns [0,32) of this buffer; the
+      // A-operand scale of row r sits at lane r, column SFP + r/32)
+      tmem_st32(tmem + lane_base + kColS0 + 128 * b, pw);
+      tmem_st1(tmem + lane_base + kColSFP + 4 * b + quad, sfp);
+      tmem_st_wait();
+      // selective rescale of O (and l): only warps holding a moved row
+      if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
+        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err, abort, 31);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[32];
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          const uint32_t ta = tmem + lane_base + kColO + 32 * c;
+          tmem_ld32(ta, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          tmem_st32(ta, r);
+        }
+        tmem_st_wait();
+      }
+      l = l * alpha + lsum;
+      m_ref = m_new;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+    }
+    // epilogue: O / l -> bf16, LSE
+    if (ok) {
+      const int jl = ntiles - 1;
+      ok = mbar_wait(&bars->pv_done[jl & 1], (jl >> 1) & 1, p.err, abort, 32);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const bool valid = qi < w.len;
+      const int64_t tok = w.start + qi;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D);
+      uint32_t r[32];
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tmem + lane_base + kColO + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                  __uint_as_float(r[8 * i + 2 * k]) * inv_l,
+                  __uint_as_float(r[8 * i + 2 * k + 1]) * inv_l);
+              wv[k] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+      }
+      if (valid) {
+        const float lse2 = m_ref + __log2f(l);
+        p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
+            lse2 * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
+                       const void* q8, const void* sfq, const void* k8,
+                       const void* sfk, const void* v8, const void* sfv,
+                       void* o, float* lse, uint32_t* err, cudaStream_t cs) {
+  const CUtensorMapSwizzle sw =
+      D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap tq, tk, tv;
+  auto make = [&](CUtensorMap* m, const void* base, int64_t heads) {
+    uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
+                        static_cast<uint64_t>(sv.total_tokens)};
+    uint64_t strides[2] = {static_cast<uint64_t>(D),
+                           static_cast<uint64_t>(heads * D)};
+    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, 128u};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides,
+                       box, sw);
+  };
+  lpfa_status st;
+  if ((st = make(&tq, q8, desc->heads_q)) != LPFA_OK) return st;
+  if ((st = make(&tk, k8, desc->heads_kv)) != LPFA_OK) return st;
+  if ((st = make(&tv, v8, desc->heads_kv)) != LPFA_OK) return st;
+
+  FwdParams p;
+  p.seqs = sv;
+  p.sfq = static_cast<const uint8_t*>(sfq);
+  p.sfk = static_cast<const uint8_t*>(sfk);
+  p.sfv = static_cast<const uint8_t*>(sfv);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = err;
+  p.hq = static_cast<int32_t>(desc->heads_q);
+  p.hkv = static_cast<int32_t>(desc->heads_kv);
+  p.group = p.hq / p.hkv;
+  p.ntile_q = static_cast<int32_t>(ceil_div(sv.seqlen, kBlockM));
+  p.causal = desc->causal ? 1 : 0;
+  p.scale_log2 = desc->softmax_scale * 1.4426950408889634f;
+  p.threshold = desc->rescale_threshold;
+
+  const int64_t qtiles = sv.cu_seqlens == nullptr
+                             ? static_cast<int64_t>(sv.nseq) * p.ntile_q
+                             : sv.total_sf_rows / 128;
+  const int64_t nblocks = qtiles * p.hq;
+  LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
+  const size_t smem = FwdSmem<D>::kTotal + 1024;
+  static bool attr = false;
+  if (!attr) {
+    LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_fwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem)));
+    attr = true;
+  }
+  mx_attn_fwd_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, p);
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}
+
+}  // namespace
+
+lpfa_status validate_attn(const lpfa_attn_desc* desc, SeqView* sv) {
+  LPFA_CHECK_ARG(desc != nullptr);
+  lpfa_status st = make_seq_view(&desc->seqs, sv);
+  if (st != LPFA_OK) return st;
+  LPFA_CHECK_ARG(desc->heads_q >= 1 && desc->heads_kv >= 1 &&
+                 desc->heads_q <= 1024 && desc->heads_q % desc->heads_kv == 0);
+  if (desc->head_dim != 64 && desc->head_dim != 128) return LPFA_ERR_UNSUPPORTED;
+  LPFA_CHECK_ARG(desc->softmax_scale > 0.f);
+  LPFA_CHECK_ARG(desc->rescale_threshold >= 0.f);
+  return LPFA_OK;
+}
+
+}  // namespace lpfa
+
+using namespace lpfa;
+
+extern "C" size_t lpfa_fwd_workspace_size(const lpfa_attn_desc* desc) {
+  (void)desc;
+  return 256;
+}
+
+extern "C" lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
+                                const void* sfq_mma, const void* k8,
+                                const void* sfk_mma, const void* v8,
+                                const void* sfv_mma, void* o, float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  SeqView sv;
+  lpfa_status st = validate_attn(desc, &sv);
+  if (st != LPFA_OK) return st;
+  LPFA_CHECK_ARG(q8 && sfq_mma && k8 && sfk_mma && v8 && sfv_mma && o && lse);
+  LPFA_CHECK_ARG(aligned16(q8) && aligned16(k8) && aligned16(v8) &&
+                 aligned16(sfq_mma) && aligned16(sfk_mma) && aligned16(sfv_mma) &&
+                 aligned16(o));
+  LPFA_CHECK_ARG(workspace != nullptr && workspace_bytes >= 256 &&
+                 (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0);
+  if (desc->causal && sv.cu_seqlens == nullptr) {
+    // Sq == Sk by construction (self-attention over the same sequences)
+  }
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (sv.total_tokens == 0) return LPFA_OK;
+  LPFA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 256, cs));
+  uint32_t* err = static_cast<uint32_t*>(workspace);
+  if (desc->head_dim == 128)
+    return launch_fwd<128>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err, cs);
+  return launch_fwd<64>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err, cs);
+}

@@ -53,6 +53,9 @@ struct SeqView {
 
 lpfa_status make_seq_view(const lpfa_seqs* s, SeqView* out);
 
+// Validates an attention descriptor and builds its sequence view.
+lpfa_status validate_attn(const lpfa_attn_desc* desc, SeqView* sv);
+
 // Number of SMs of the current device (cached per device).
 int num_sms();
 

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "liblpfa.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing: build it with "
-        "`python -m mxfp8_block_scaled_quantizer_gb300.build` (needs nvcc).")
+        "`python -m mxfp8_block_scaled_quantizer_gb300._builder` (needs nvcc).")
 _lib = ctypes.CDLL(LIB_PATH)
 
 LPFA_OK, LPFA_ERR_INVALID_ARG, LPFA_ERR_UNSUPPORTED, LPFA_ERR_CUDA, \
@@ -249,3 +249,58 @@ def lpfa_bwd(desc, q8, sfq, sfq_t, k8, sfk, sfk_t, v8, sfv, do8, sfdo,
 
 def lpfa_check(ws: torch.Tensor, stream=None):
     _ok(_check(_ptr(ws), _stream(stream)), "lpfa_check")
+
+
+# ------------------------------------------------------- convenience layer
+def _as_tokens(x: torch.Tensor):
+    """[B, S, H, D] -> ([B*S, H, D], B, S); [T, H, D] -> (x, None, None)."""
+    if x.dim() == 4:
+        B, S = x.shape[:2]
+        return x.reshape(B * S, *x.shape[2:]).contiguous(), B, S
+    return x.contiguous(), None, None
+
+
+def quantize_forward_operands(q, k, v, seqs: Seqs, stream=None):
+    """MX-quantize Q, K (1x32 along head_dim) and V (32 along tokens)."""
+    mq = mx_quantize(q, LPFA_BLK_1X32, seqs, compact=False, stream=stream)
+    mk = mx_quantize(k, LPFA_BLK_1X32, seqs, compact=False, stream=stream)
+    mv = mx_quantize(v, LPFA_BLK_32X1, seqs, compact=False, stream=stream)
+    return mq, mk, mv
+
+
+def attention_forward_mx(mq: MXTensor, mk: MXTensor, mv: MXTensor,
+                         desc: lpfa_attn_desc, out=None, lse=None, ws=None,
+                         stream=None):
+    """lpfa_fwd on already-quantized operands.  Returns (o, lse, ws)."""
+    T, Hq, D = mq.data.shape
+    dev = mq.data.device
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(fwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    lpfa_fwd(desc, mq.data, mq.sf_mma, mk.data, mk.sf_mma, mv.data, mv.sf_mma,
+             out, lse, ws, stream)
+    return out, lse, ws
+
+
+def mx_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
+                         cu_seqlens: Optional[torch.Tensor] = None,
+                         rescale_threshold: float = 8.0, check: bool = True):
+    """Quantize and run the MXFP8 forward.  q [B,S,Hq,D] (or packed [T,Hq,D]
+    with ``cu_seqlens``), k/v with Hkv heads, all bf16 CUDA tensors.
+    Returns (o shaped like q, lse [Hq, T])."""
+    shape = q.shape
+    qt, B, S = _as_tokens(q)
+    kt, _, _ = _as_tokens(k)
+    vt, _, _ = _as_tokens(v)
+    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    T, Hq, D = qt.shape
+    desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
+                     rescale_threshold)
+    mq, mk, mv = quantize_forward_operands(qt, kt, vt, seqs)
+    o, lse, ws = attention_forward_mx(mq, mk, mv, desc)
+    if check:
+        lpfa_check(ws)
+    return o.reshape(shape), lse

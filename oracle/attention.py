@@ -73,7 +73,19 @@ def to_f64(t) -> np.ndarray:
     return np.asarray(t, dtype=np.float64)
 
 
-def as_packed(x: np.ndarray, cu_seqlens):
+def _lazy(t):
+    """Keep torch tensors as they are (sliced before conversion to fp64);
+    other inputs become fp64 arrays."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            return t.detach().cpu()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(t, dtype=np.float64)
+
+
+def as_packed(x, cu_seqlens):
     """[B, S, H, D] -> ([B*S, H, D], cu_seqlens); [T, H, D] passes through."""
     if x.ndim == 4:
         b, s = x.shape[:2]
@@ -231,16 +243,15 @@ def mx_attention_fwd(q, k, v, *, causal, softmax_scale, cu_seqlens=None,
     ``heads`` / ``seqs`` / ``rows`` restrict the work to a sample (query heads,
     sequence indices, query rows within each sequence); entries outside the
     sample are NaN.  Returns {"o": like q, "lse": [Hq, T]}."""
-    q = to_f64(q); k = to_f64(k); v = to_f64(v)
-    shape_q = q.shape
-    qp, cu = as_packed(q, cu_seqlens)
-    kp, _ = as_packed(k, cu_seqlens)
-    vp, _ = as_packed(v, cu_seqlens)
-    qd, kd, vd = quantize_fwd_operands(qp, kp, vp, cu, quantize)
-    hq, hkv = qp.shape[1], kp.shape[1]
+    shape_q = tuple(q.shape)
+    hq, hkv = q.shape[-2], k.shape[-2]
     grp = hq // hkv
-    o = np.full_like(qp, np.nan)
-    lse = np.full((hq, qp.shape[0]), np.nan)
+    qp, cu = as_packed(_lazy(q), cu_seqlens)
+    kp, _ = as_packed(_lazy(k), cu_seqlens)
+    vp, _ = as_packed(_lazy(v), cu_seqlens)
+    T = qp.shape[0]
+    o = np.full((T, hq, qp.shape[2]), np.nan)
+    lse = np.full((hq, T), np.nan)
     heads = range(hq) if heads is None else heads
     seqs = range(len(cu) - 1) if seqs is None else seqs
     for s in seqs:
@@ -249,7 +260,12 @@ def mx_attention_fwd(q, k, v, *, causal, softmax_scale, cu_seqlens=None,
             [i for i in rows if i < b - a], dtype=np.int64)
         for h in heads:
             kh = h // grp
-            oh, lh = mx_fwd_head(qd[a:b, h], kd[a:b, kh], vd[a:b, kh],
+            # operands of this (sequence, head) only; quantization acts per
+            # row (Q, K) or per 32-token block of one sequence (V)
+            qd, kd, vd = quantize_fwd_operands(
+                to_f64(qp[a:b, h:h + 1]), to_f64(kp[a:b, kh:kh + 1]),
+                to_f64(vp[a:b, kh:kh + 1]), np.array([0, b - a]), quantize)
+            oh, lh = mx_fwd_head(qd[:, 0], kd[:, 0], vd[:, 0],
                                  causal=causal, scale=softmax_scale,
                                  kv_tile=kv_tile,
                                  rescale_threshold=rescale_threshold,
@@ -375,20 +391,19 @@ def mx_attention_bwd(q, k, v, o, do, lse, *, causal, softmax_scale,
     (with all their query heads), ``seqs`` to sequences, ``q_rows``/``k_rows``
     to whole 32-row blocks within each sequence.  Entries outside the sample
     are NaN.  Returns {"dq", "dk", "dv"} shaped like q/k/v."""
-    q = to_f64(q); k = to_f64(k); v = to_f64(v); o = to_f64(o)
-    do = to_f64(do); lse = to_f64(lse)
-    shape_q, shape_k = q.shape, k.shape
-    qp, cu = as_packed(q, cu_seqlens)
-    kp, _ = as_packed(k, cu_seqlens)
-    vp, _ = as_packed(v, cu_seqlens)
-    op, _ = as_packed(o, cu_seqlens)
-    dop, _ = as_packed(do, cu_seqlens)
-    qd, kd, vd, dod = quantize_bwd_operands(qp, kp, vp, dop, cu, quantize)
+    shape_q, shape_k = tuple(q.shape), tuple(k.shape)
+    lse = to_f64(lse)
+    qp, cu = as_packed(_lazy(q), cu_seqlens)
+    kp, _ = as_packed(_lazy(k), cu_seqlens)
+    vp, _ = as_packed(_lazy(v), cu_seqlens)
+    op, _ = as_packed(_lazy(o), cu_seqlens)
+    dop, _ = as_packed(_lazy(do), cu_seqlens)
     hq, hkv = qp.shape[1], kp.shape[1]
     grp = hq // hkv
-    dq = np.full_like(qp, np.nan)
-    dk = np.full_like(kp, np.nan)
-    dv = np.full_like(vp, np.nan)
+    T, D = qp.shape[0], qp.shape[2]
+    dq = np.full((T, hq, D), np.nan)
+    dk = np.full((T, hkv, D), np.nan)
+    dv = np.full((T, hkv, D), np.nan)
     kv_heads = range(hkv) if heads is None else heads
     seqs = range(len(cu) - 1) if seqs is None else seqs
     for s in seqs:
@@ -398,12 +413,17 @@ def mx_attention_bwd(q, k, v, o, do, lse, *, causal, softmax_scale,
             [i for i in q_rows if i < L], dtype=np.int64)
         kr = np.arange(L) if k_rows is None else np.asarray(
             [i for i in k_rows if i < L], dtype=np.int64)
+        one = np.array([0, L])
         for kh in kv_heads:
-            dk_acc = np.zeros((len(kr), kp.shape[2]))
-            dv_acc = np.zeros((len(kr), kp.shape[2]))
+            dk_acc = np.zeros((len(kr), D))
+            dv_acc = np.zeros((len(kr), D))
             for h in range(kh * grp, (kh + 1) * grp):
-                g = mx_bwd_head(qd[a:b, h], kd[a:b, kh], vd[a:b, kh],
-                                dod[a:b, h], dop[a:b, h], op[a:b, h],
+                qd, kd, vd, dod = quantize_bwd_operands(
+                    to_f64(qp[a:b, h:h + 1]), to_f64(kp[a:b, kh:kh + 1]),
+                    to_f64(vp[a:b, kh:kh + 1]), to_f64(dop[a:b, h:h + 1]),
+                    one, quantize)
+                g = mx_bwd_head(qd[:, 0], kd[:, 0], vd[:, 0], dod[:, 0],
+                                to_f64(dop[a:b, h]), to_f64(op[a:b, h]),
                                 lse[h, a:b], causal=causal,
                                 scale=softmax_scale, quantize=quantize,
                                 kv_tile=kv_tile,
