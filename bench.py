@@ -1,0 +1,416 @@
+"""Benchmark of the MXFP8 attention training step (forward + backward).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lpfa|reference]
+
+A step is one pass of the whole hot path on one batch of synthetic input of
+the B8 H32 S8192 D128 causal LLM training shape: MX quantization of Q, K (1x32)
+and V (32 along tokens), the forward kernel, MX quantization of Q, K, dO
+(32x32) and V (1x32), and the backward (D_i preprocess, main kernel).  Inputs
+(512 MiB per bf16 tensor) are larger than L2, so no flush is needed.
+
+Multi-GPU: every rank runs its own replica of the step on its own seeded
+inputs (the path shards over (batch, head) with no exchange step); the time
+is the max over ranks and the value counts the work of all ranks (weak
+scaling).  --impl reference times the fp64 CPU oracle on a bounded sample of
+the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MXFP8 attn fwd/bwd PFLOP/s (B8 H32 S8192 D128 causal); % of FP8 MMA peak"
+WORKLOAD = "llm"
+FP8_OVER_BF16 = 2.0      # nominal dense fp8 : bf16 tensor-core ratio
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1])); smax.append(float(f[2]))
+                    power.append(float(f[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample(rows: int, seed: int = 2):
+    """Time the fp64 oracle (forward + backward) on one head of the workload
+    restricted to the last ``rows`` queries (which see every earlier key) and
+    the last ``rows`` keys.  Returns (flops of the sample, seconds, text)."""
+    import numpy as np
+    from oracle import attention as A
+    w = workloads.get_config(WORKLOAD)
+    g = torch.Generator().manual_seed(seed)
+    S, D = w.seqlen, w.head_dim
+    q, k, v, do = (torch.randn(1, S, 1, D, generator=g).to(torch.bfloat16)
+                   for _ in range(4))
+    r = np.arange(S - rows, S)
+    t0 = time.perf_counter()
+    fw = A.mx_attention_fwd(q, k, v, causal=True, softmax_scale=w.softmax_scale,
+                            rows=r)
+    o16 = torch.from_numpy(np.nan_to_num(fw["o"])).to(torch.bfloat16)
+    A.mx_attention_bwd(q, k, v, o16, do, np.nan_to_num(fw["lse"]), causal=True,
+                       softmax_scale=w.softmax_scale, q_rows=r, k_rows=r)
+    dt = time.perf_counter() - t0
+    visible = float(sum(i + 1 for i in r))          # (query, key) pairs
+    flops = (4.0 + 10.0) * D * visible              # fwd + bwd convention
+    text = (f"one head (b0,h0) of B8 H32 S8192 D128 causal: last {rows} query rows "
+            f"(fwd, dQ) and last {rows} key rows (dK, dV), fp64 numpy oracle; "
+            f"flops = 14*D*#(query,key) pairs of those rows")
+    return flops, dt, text
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    rows = 512
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    tot_f = tot_t = 0.0
+    for _ in range(args.steps):
+        f, t, text = oracle_sample(rows)
+        tot_f += f; tot_t += t
+    value = tot_f / tot_t / 1e15
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "PFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": "llm: B8 H32 S8192 D128 causal, bounded sample",
+                   "global_batch": 8, "seq_len": 8192, "parallelism": "none"},
+        "cpu_baseline": {"value": value, "unit": "PFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": text},
+        "e2e": {"value": value, "unit": "PFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_lpfa(args, world, rank, local):
+    from mxfp8_block_scaled_quantizer_gb300 import build
+    build()
+    from mxfp8_block_scaled_quantizer_gb300 import lpfa as L
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.get_config(WORKLOAD)
+    B, S, H, Hkv, D = w.batch, w.seqlen, w.heads_q, w.heads_kv, w.head_dim
+    T = B * S
+    # seeded synthetic inputs (workloads recipe), one replica per rank
+    wr = workloads.custom(**{**w.__dict__, "seed": w.seed + rank})
+    x = workloads.make_inputs(wr)
+    host = {n: x[n].reshape(T, -1, D).contiguous().pin_memory()
+            for n in ("q", "k", "v", "do")}
+    q, k, v, do = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+    torch.cuda.synchronize()
+    seqs = L.dense_seqs(B, S)
+    desc = L.attn_desc(seqs, H, Hkv, D, w.causal, w.softmax_scale)
+    fwd_flops, bwd_flops = workloads.attn_flops(w)
+
+    # persistent buffers
+    o = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev)
+    fws = torch.empty(L.fwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    dq = torch.empty((T, H, D), dtype=torch.float16, device=dev)
+    dk = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    bws = torch.empty(L.bwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    launches_per_step = 3 + 1 + 4 + 2      # quantize x3, fwd, quantize x4, bwd x2
+
+    def step(times=None):
+        e = [ev() for _ in range(6)] if times is not None else None
+        if e: e[0].record()
+        mq, mk, mv = L.quantize_forward_operands(q, k, v, seqs)
+        if e: e[1].record()
+        L.attention_forward_mx(mq, mk, mv, desc, o, lse, fws)
+        if e: e[2].record()
+        bq, bk, bv, bdo = L.quantize_backward_operands(q, k, v, do, seqs)
+        if e: e[3].record()
+        L.attention_backward_mx(bq, bk, bv, bdo, o, do, lse, desc, dq, dk, dv, bws)
+        if e:
+            e[4].record()
+            times.append(e)
+
+    for _ in range(args.warmup):
+        step()
+    L.lpfa_check(fws)
+    L.lpfa_check(bws)
+    torch.cuda.synchronize()
+
+    parts = []
+    with ClockSampler(local) as clk:
+        _barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = ev(), ev()
+        t0.record()
+        for _ in range(args.steps):
+            step(parts)
+        t1.record()
+        torch.cuda.synchronize()
+        _barrier(world)
+    L.lpfa_check(fws)
+    L.lpfa_check(bws)
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_max = _max_over_ranks(ms, world)
+    qf = statistics.mean(p[0].elapsed_time(p[1]) for p in parts)
+    fw = statistics.mean(p[1].elapsed_time(p[2]) for p in parts)
+    qb = statistics.mean(p[2].elapsed_time(p[3]) for p in parts)
+    bw = statistics.mean(p[3].elapsed_time(p[4]) for p in parts)
+
+    # ---- end to end through the public API with host buffers
+    out_host = {"o": torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory(),
+                "dq": torch.empty((T, H, D), dtype=torch.float16).pin_memory(),
+                "dk": torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory(),
+                "dv": torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory()}
+
+    def e2e_step():
+        dq_, dk_, dv_ = None, None, None
+        qd, kd, vd, dod = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+        shp = lambda t, h: t.view(B, S, h, D)
+        o_, lse_ = L.mx_attention_forward(shp(qd, H), shp(kd, Hkv), shp(vd, Hkv),
+                                          causal=w.causal, softmax_scale=w.softmax_scale,
+                                          check=False)
+        dq_, dk_, dv_ = L.mx_attention_backward(shp(qd, H), shp(kd, Hkv), shp(vd, Hkv), o_,
+                                                shp(dod, H), lse_, causal=w.causal,
+                                                softmax_scale=w.softmax_scale, check=False)
+        out_host["o"].copy_(o_.view(T, H, D), non_blocking=True)
+        out_host["dq"].copy_(dq_.view(T, H, D), non_blocking=True)
+        out_host["dk"].copy_(dk_.view(T, Hkv, D), non_blocking=True)
+        out_host["dv"].copy_(dv_.view(T, Hkv, D), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    e0, e1 = ev(), ev()
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    # ---- in-run MX MMA rate (block-scaled GEMM 8192^3) and cuBLAS reference
+    mma = {}
+    try:
+        M = N = K = 8192
+        a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+        b = torch.randn(N, K, device=dev, dtype=torch.bfloat16)
+        qa = L.mx_quantize(a.view(M, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, M), compact=False)
+        qb = L.mx_quantize(b.view(N, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, N), compact=False)
+        dmat = torch.empty(M, N, device=dev, dtype=torch.float32)
+        A8, B8 = qa.data.view(M, K), qb.data.view(N, K)
+        for _ in range(3):
+            L.lpfa_mx_gemm(A8, qa.sf_mma, B8, qb.sf_mma, dmat)
+        torch.cuda.synchronize()
+        g0, g1 = ev(), ev()
+        g0.record()
+        for _ in range(10):
+            L.lpfa_mx_gemm(A8, qa.sf_mma, B8, qb.sf_mma, dmat)
+        g1.record()
+        torch.cuda.synchronize()
+        mma["lpfa_mx_gemm_tflops"] = 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
+        try:
+            a8 = A8.view(torch.float8_e4m3fn); b8 = B8.view(torch.float8_e4m3fn)
+            sa = qa.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
+            sb = qb.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
+            for _ in range(3):
+                torch._scaled_mm(a8, b8.t(), sa, sb, out_dtype=torch.bfloat16)
+            torch.cuda.synchronize()
+            g0.record()
+            for _ in range(10):
+                torch._scaled_mm(a8, b8.t(), sa, sb, out_dtype=torch.bfloat16)
+            g1.record()
+            torch.cuda.synchronize()
+            mma["cublas_mxfp8_tflops"] = 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
+        except Exception as exc:  # library path not available in this torch
+            mma["cublas_mxfp8_tflops"] = None
+            mma["cublas_note"] = repr(exc)[:160]
+        del a, b, qa, qb, dmat
+    except Exception as exc:
+        mma["error"] = repr(exc)[:160]
+
+    peaks = _peaks()
+    if peaks and peaks.get("bf16_tflops_sustained"):
+        peak = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
+        peak_src = "measured bf16 sustained x 2 (nominal fp8:bf16), MEASURED_PEAKS.json"
+    else:
+        peak = 1700.0 * FP8_OVER_BF16
+        peak_src = "fallback 1.7 PFLOP/s bf16 sustained x 2"
+    bwd_tflops = bwd_flops / bw / 1e9
+    fwd_tflops = fwd_flops / fw / 1e9
+    total = (fwd_flops + bwd_flops) * world
+    value = total / (ms_max * 1e-3) / 1e15
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as fh:
+                traffic = json.load(fh).get("mx_attn_bwd_kernel_bytes_per_launch")
+        except (OSError, ValueError):
+            traffic = None
+    line = {
+        "metric": METRIC, "value": value, "unit": "PFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 (MXFP8, fp32 accumulate)", "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": "llm: B8 H32 S8192 D128 causal, fwd+bwd incl. MX quantization",
+                   "global_batch": B * world, "seq_len": S, "heads": H, "head_dim": D,
+                   "parallelism": f"replicas x{world} (shard over batch/heads, no collective)",
+                   "l2": "no flush: every input tensor (512 MiB) is larger than L2"},
+        "fwd": {"tflops": fwd_tflops, "ms": fw, "frac_of_peak": fwd_tflops / peak},
+        "bwd": {"tflops": bwd_tflops, "ms": bw, "frac_of_peak": bwd_tflops / peak},
+        "quantize_ms": {"fwd_operands": qf, "bwd_operands": qb},
+        "roofline": {"bound": "tensor", "kernel": "mx_attn_bwd (lpfa_bwd call)",
+                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": bwd_tflops / peak, "traffic": traffic,
+                     "peak_source": peak_src + " (of measured)"},
+        "mma_rate_in_run": mma,
+        "e2e": {"value": total / (e2e_ms * 1e-3) / 1e15, "unit": "PFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+            f, t, text = oracle_sample(1024)
+            cpu = {"value": f / t / 1e15, "unit": "PFLOP/s", "cores": cores,
+                   "kind": "oracle", "sample": text, "seconds": t}
+        line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="lpfa", choices=["lpfa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = _dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_lpfa(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -304,3 +304,60 @@ def mx_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
     if check:
         lpfa_check(ws)
     return o.reshape(shape), lse
+
+
+def quantize_backward_operands(q, k, v, do, seqs: Seqs, stream=None):
+    """MX-quantize Q, K, dO in square 32x32 blocks (both scale layouts) and V
+    in 1x32 blocks along head_dim."""
+    mq = mx_quantize(q, LPFA_BLK_32X32, seqs, compact=False, stream=stream)
+    mk = mx_quantize(k, LPFA_BLK_32X32, seqs, compact=False, stream=stream)
+    mdo = mx_quantize(do, LPFA_BLK_32X32, seqs, compact=False, stream=stream)
+    mv = mx_quantize(v, LPFA_BLK_1X32, seqs, compact=False, stream=stream)
+    return mq, mk, mv, mdo
+
+
+def attention_backward_mx(mq: MXTensor, mk: MXTensor, mv: MXTensor,
+                          mdo: MXTensor, o: torch.Tensor, dout: torch.Tensor,
+                          lse: torch.Tensor, desc: lpfa_attn_desc, dq=None,
+                          dk=None, dv=None, ws=None, stream=None):
+    """lpfa_bwd on already-quantized operands.  o, dout: bf16 [T, Hq, D];
+    lse: fp32 [Hq, T].  Returns (dq fp16, dk bf16, dv bf16, ws)."""
+    T, Hq, D = mq.data.shape
+    Hkv = mk.data.shape[1]
+    dev = mq.data.device
+    if dq is None:
+        dq = torch.empty((T, Hq, D), dtype=torch.float16, device=dev)
+    if dk is None:
+        dk = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    if dv is None:
+        dv = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(bwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    lpfa_bwd(desc, mq.data, mq.sf_mma, mq.sf_mma_t, mk.data, mk.sf_mma,
+             mk.sf_mma_t, mv.data, mv.sf_mma, mdo.data, mdo.sf_mma,
+             mdo.sf_mma_t, o.contiguous(), dout.contiguous(), lse.contiguous(),
+             dq, dk, dv, ws, stream)
+    return dq, dk, dv, ws
+
+
+def mx_attention_backward(q, k, v, o, dout, lse, *, causal: bool,
+                          softmax_scale=None,
+                          cu_seqlens: Optional[torch.Tensor] = None,
+                          dq_static_scale: float = 1.0, check: bool = True):
+    """Quantize and run the MXFP8 backward.  Shapes as mx_attention_forward;
+    o/dout like q, lse [Hq, T].  Returns (dq fp16, dk, dv) shaped like q/k/v."""
+    shape_q, shape_k = q.shape, k.shape
+    qt, B, S = _as_tokens(q)
+    kt, _, _ = _as_tokens(k)
+    vt, _, _ = _as_tokens(v)
+    ot, _, _ = _as_tokens(o)
+    dot, _, _ = _as_tokens(dout)
+    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    T, Hq, D = qt.shape
+    desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
+                     dq_static_scale=dq_static_scale)
+    mq, mk, mv, mdo = quantize_backward_operands(qt, kt, vt, dot, seqs)
+    dq, dk, dv, ws = attention_backward_mx(mq, mk, mv, mdo, ot, dot, lse, desc)
+    if check:
+        lpfa_check(ws)
+    return dq.reshape(shape_q), dk.reshape(shape_k), dv.reshape(shape_k)
