@@ -158,7 +158,7 @@ def oracle_sample(rows: int, seed: int = 2):
     flops = (4.0 + 10.0) * D * visible              # fwd + bwd convention
     text = (f"one head (b0,h0) of B8 H32 S8192 D128 causal: last {rows} query rows "
             f"(fwd, dQ) and last {rows} key rows (dK, dV), fp64 numpy oracle; "
-            f"flops = 14*D*#(query,key) pairs of those rows")
+            f"flops = 14*D*#(visible query,key) pairs of those query rows")
     return flops, dt, text
 
 
@@ -166,7 +166,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    rows = 512
+    rows = 2048
     for _ in range(args.warmup):
         oracle_sample(rows)
     tot_f = tot_t = 0.0
@@ -305,24 +305,24 @@ def run_lpfa(args, world, rank, local):
         M = N = K = 8192
         a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
         b = torch.randn(N, K, device=dev, dtype=torch.bfloat16)
-        qa = L.mx_quantize(a.view(M, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, M), compact=False)
-        qb = L.mx_quantize(b.view(N, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, N), compact=False)
+        ga = L.mx_quantize(a.view(M, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, M), compact=False)
+        gb = L.mx_quantize(b.view(N, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, N), compact=False)
         dmat = torch.empty(M, N, device=dev, dtype=torch.float32)
-        A8, B8 = qa.data.view(M, K), qb.data.view(N, K)
+        A8, B8 = ga.data.view(M, K), gb.data.view(N, K)
         for _ in range(3):
-            L.lpfa_mx_gemm(A8, qa.sf_mma, B8, qb.sf_mma, dmat)
+            L.lpfa_mx_gemm(A8, ga.sf_mma, B8, gb.sf_mma, dmat)
         torch.cuda.synchronize()
         g0, g1 = ev(), ev()
         g0.record()
         for _ in range(10):
-            L.lpfa_mx_gemm(A8, qa.sf_mma, B8, qb.sf_mma, dmat)
+            L.lpfa_mx_gemm(A8, ga.sf_mma, B8, gb.sf_mma, dmat)
         g1.record()
         torch.cuda.synchronize()
         mma["lpfa_mx_gemm_tflops"] = 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
         try:
             a8 = A8.view(torch.float8_e4m3fn); b8 = B8.view(torch.float8_e4m3fn)
-            sa = qa.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
-            sb = qb.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
+            sa = ga.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
+            sb = gb.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)
             for _ in range(3):
                 torch._scaled_mm(a8, b8.t(), sa, sb, out_dtype=torch.bfloat16)
             torch.cuda.synchronize()
@@ -335,7 +335,7 @@ def run_lpfa(args, world, rank, local):
         except Exception as exc:  # library path not available in this torch
             mma["cublas_mxfp8_tflops"] = None
             mma["cublas_note"] = repr(exc)[:160]
-        del a, b, qa, qb, dmat
+        del a, b, ga, gb, dmat
     except Exception as exc:
         mma["error"] = repr(exc)[:160]
 
@@ -385,7 +385,7 @@ def run_lpfa(args, world, rank, local):
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
             cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-            f, t, text = oracle_sample(1024)
+            f, t, text = oracle_sample(8192)
             cpu = {"value": f / t / 1e15, "unit": "PFLOP/s", "cores": cores,
                    "kind": "oracle", "sample": text, "seconds": t}
         line["cpu_baseline"] = cpu

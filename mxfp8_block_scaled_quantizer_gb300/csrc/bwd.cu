@@ -16,12 +16,16 @@
 //
 // CTA = one 128-key tile of one (sequence, kv head); it loops over the query
 // heads of its GQA group and over 64-query steps (causal: from the diagonal).
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// compute (thread = key row for S^T/dP^T, = head_dim channel for dQ^T).
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-9
+// compute in two warpgroups, each owning 32 of the step's 64 queries (thread
+// = key row for S^T/dP^T, = head_dim channel for dQ^T).  dQ partials leave
+// as one tensor reduce-add (FP16) of the 64x128 step tile.
 //
 // TMEM (512 columns):
 //   [  0,128) dK      [128,256) dV      [256,320) S^T -> P^T fp8 (16 cols)
 //   [320,384) dP^T -> dS^T fp8 (16 cols)   [384,448) dQ^T
+//   P^T / dS^T of query block g sit at S^T / dP^T column 32 g, inside the
+//   columns warpgroup g itself read.
 //   [448,512) scale factors (see kCol* below)
 #include <cuda_runtime.h>
 
@@ -36,14 +40,14 @@ constexpr int kD = 128;          // head_dim of this kernel
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320,
                    kColDQ = 384;
 constexpr uint32_t kColSFK = 448, kColSFV = 452, kColSFKt = 456,
                    kColSFQ = 460, kColSFdO = 464, kColSFQt = 468,
-                   kColSFdOt = 472, kColSFP = 476, kColSFdS = 480,
-                   kColSFdSB = 484;
+                   kColSFdOt = 472, kColSFP = 476 /* +4g */,
+                   kColSFdS = 484 /* +4g */, kColSFdSB = 492;
 
 // shared memory layout (bytes from a 1024-aligned base)
 constexpr int kSmK = 0;                          // 128 x 128 B (SW128)
@@ -154,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tma_k,
                        const __grid_constant__ CUtensorMap tma_v,
                        const __grid_constant__ CUtensorMap tma_do,
+                       const __grid_constant__ CUtensorMap tma_dq,
                        const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -178,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_empty[s], 1);
     }
     mbar_init(&bars->st_ready, 1);
-    mbar_init(&bars->ds_ready, 4);
+    mbar_init(&bars->ds_ready, 8);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 4);
+    mbar_init(&bars->dq_free, 8);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
@@ -206,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tma_k);
       tma_prefetch_desc(&tma_v);
       tma_prefetch_desc(&tma_do);
+      tma_prefetch_desc(&tma_dq);
       const int32_t row_k = static_cast<int32_t>(w.start + k0);
       const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
       mbar_arrive_expect_tx(&bars->kv_full, 2 * kBN * kD + 3 * 512);
@@ -300,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < kBQ / 32; ++kb) {
           const uint32_t sfb = kb + 2 * half;
-          mma_mxf8_ts(tmem + kColDV, tmem + kColS + 8 * kb,
+          mma_mxf8_ts(tmem + kColDV, tmem + kColS + 32 * kb,
                       make_sdesc(do_addr + 32 * kD * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_acc, kb, sfb), tmem + kColSFP,
+                      idesc_sf_ids(id_acc, 0, sfb), tmem + kColSFP + 4 * kb,
                       tmem + kColSFdOt, (i > 0) || (kb > 0));
-          mma_mxf8_ts(tmem + kColDK, tmem + kColDP + 8 * kb,
+          mma_mxf8_ts(tmem + kColDK, tmem + kColDP + 32 * kb,
                       make_sdesc(q_addr + 32 * kD * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_acc, kb, sfb), tmem + kColSFdS,
+                      idesc_sf_ids(id_acc, 0, sfb), tmem + kColSFdS + 4 * kb,
                       tmem + kColSFQt, (i > 0) || (kb > 0));
         }
         // dQ^T = K^T dS^T (contraction over the 128 keys)
@@ -332,146 +338,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------- compute
+    const int g = (warp - 2) >> 2;                // query block of the step
     const int quad = warp & 3;
     const int m = quad * 32 + lane;               // key row (and channel for dQ^T)
     const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
     const int key = k0 + m;
-    const int ctid = threadIdx.x - 64;            // 0..127 among compute threads
+    const int ctid = threadIdx.x - 64;            // 0..255 among compute threads
     bool ok = true;
     for (int i = 0; i < nsteps && ok; ++i) {
       const int s = i % kStages;
       const int h = step_head(i), q0 = step_q0(i);
-      const float* lse2 = reinterpret_cast<const float*>(sm + kSmStage0 + s * kStageBytes + kStLse);
-      const float* dlt = reinterpret_cast<const float*>(sm + kSmStage0 + s * kStageBytes + kStDelta);
+      const uint8_t* st = sm + kSmStage0 + s * kStageBytes;
       ok = mbar_wait(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
       tc_fence_after();
-      uint32_t pw[16], dw[16];
-      uint32_t sfp = 0, sfds = 0;
-      uint8_t* ds_row = sm + kSmDS + m * kBQ;      // 64-byte row, 64B swizzle
+      uint32_t rs[32], rd[32];
+      tmem_ld32(tmem + lb + kColS + 32 * g, rs);
+      tmem_ld32(tmem + lb + kColDP + 32 * g, rd);
+      float lse2[32], dlt[32];
+      {
+        const float4* l4 = reinterpret_cast<const float4*>(st + kStLse) + 8 * g;
+        const float4* d4 = reinterpret_cast<const float4*>(st + kStDelta) + 8 * g;
 #pragma unroll
-      for (int jb = 0; jb < kBQ / 32; ++jb) {
-        uint32_t rs[32], rd[32];
-        tmem_ld32(tmem + lb + kColS + 32 * jb, rs);
-        tmem_ld32(tmem + lb + kColDP + 32 * jb, rd);
-        tmem_ld_wait();
-        float pv[32], dsv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int qq = q0 + 32 * jb + j;
-          const bool masked = (key >= w.len) || (qq >= w.len) || (p.causal && key > qq);
-          const float x = fmaf(__uint_as_float(rs[j]), p.scale_log2, -lse2[32 * jb + j]);
-          const float pj = masked ? 0.f : ex2(x);
-          pv[j] = pj;
-          dsv[j] = pj * (__uint_as_float(rd[j]) - dlt[32 * jb + j]);
+        for (int t = 0; t < 8; ++t) {
+          const float4 a4 = l4[t], b4 = d4[t];
+          lse2[4 * t] = a4.x; lse2[4 * t + 1] = a4.y; lse2[4 * t + 2] = a4.z; lse2[4 * t + 3] = a4.w;
+          dlt[4 * t] = b4.x; dlt[4 * t + 1] = b4.y; dlt[4 * t + 2] = b4.z; dlt[4 * t + 3] = b4.w;
         }
-        uint32_t wq[8];
-        const uint32_t cp_ = quant_block32(pv, wq);
+      }
+      tmem_ld_wait();
+      float pv[32], dsv[32];
+      const int qb0 = q0 + 32 * g;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) pw[8 * jb + t] = wq[t];
-        const uint32_t cd = quant_block32(dsv, wq);
-#pragma unroll
-        for (int t = 0; t < 8; ++t) dw[8 * jb + t] = wq[t];
-        sfp |= cp_ << (8 * jb);
-        sfds |= cd << (8 * jb);
-        // dS^T row chunk -> shared memory (two 16-byte chunks of 64)
+      for (int j = 0; j < 32; ++j) {
+        const int qq = qb0 + j;
+        const bool masked = (key >= w.len) || (qq >= w.len) || (p.causal && key > qq);
+        const float x = fmaf(__uint_as_float(rs[j]), p.scale_log2, -lse2[j]);
+        const float pj = masked ? 0.f : ex2(x);
+        pv[j] = pj;
+        dsv[j] = pj * (__uint_as_float(rd[j]) - dlt[j]);
+      }
+      uint32_t wp[8], wd[8];
+      const uint32_t cp_ = quant_block32(pv, wp);
+      const uint32_t cd = quant_block32(dsv, wd);
+      // P^T and dS^T (fp8) into TMEM at column 32 g of the consumed S^T /
+      // dP^T block; their A-operand scales at lane m, column base + 4g + m/32
+      tmem_st8(tmem + lb + kColS + 32 * g, wp);
+      tmem_st8(tmem + lb + kColDP + 32 * g, wd);
+      tmem_st1(tmem + lb + kColSFP + 4 * g + quad, cp_);
+      tmem_st1(tmem + lb + kColSFdS + 4 * g + quad, cd);
+      // dS^T row chunks 2g, 2g+1 -> shared memory (64-byte rows, 64B swizzle)
+      {
+        uint8_t* ds_row = sm + kSmDS + m * kBQ;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const int chunk = 2 * jb + c;
-          const int phys = chunk ^ ((m >> 1) & 3);
+          const int phys = (2 * g + c) ^ ((m >> 1) & 3);
           *reinterpret_cast<uint4*>(ds_row + 16 * phys) =
-              make_uint4(wq[4 * c], wq[4 * c + 1], wq[4 * c + 2], wq[4 * c + 3]);
+              make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
         }
-        // B-operand scale of dQ^T: (query n = 32 jb + lane, key block quad)
-        sm[kSmSFdS + lane * 16 + jb * 4 + quad] = static_cast<uint8_t>(cd);
       }
-      // P^T and dS^T (fp8) into TMEM over the consumed S^T / dP^T columns;
-      // their A-operand scales at lane m, column base + m/32
-      {
-        uint32_t r16[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) r16[t] = pw[t];
-        tmem_st16(tmem + lb + kColS, r16);
-#pragma unroll
-        for (int t = 0; t < 16; ++t) r16[t] = dw[t];
-        tmem_st16(tmem + lb + kColDP, r16);
-      }
-      tmem_st1(tmem + lb + kColSFP + quad, sfp);
-      tmem_st1(tmem + lb + kColSFdS + quad, sfds);
+      // B-operand scale of dQ^T: (query n = 32 g + lane, key block quad)
+      sm[kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_ready);
 
-      // dQ^T readout: thread = channel m, 64 queries
+      // dQ^T readout: thread = channel m, queries 32 g .. 32 g + 31
       ok = mbar_wait(&bars->dq_full, i & 1, p.err, abort, 61);
       if (!ok) break;
       tc_fence_after();
-      uint32_t rq[64];
-      {
-        uint32_t r[32];
-        tmem_ld32(tmem + lb + kColDQ, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) rq[j] = r[j];
-        tmem_ld32(tmem + lb + kColDQ + 32, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) rq[32 + j] = r[j];
-      }
+      uint32_t rq[32];
+      tmem_ld32(tmem + lb + kColDQ + 32 * g, rq);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->dq_free);
-      // stage fp16 rows [q][d] and reduce-add them into global dQ
+      // stage fp16 rows [q][d], then one tensor reduce-add into global dQ
       __half* stg = reinterpret_cast<__half*>(sm + kSmDQ + (i & 1) * kBQ * kD * 2);
       if (ctid == 0) bulk_wait_read_le1();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
 #pragma unroll
-      for (int j = 0; j < kBQ; ++j)
-        stg[j * kD + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
+      for (int j = 0; j < 32; ++j)
+        stg[(32 * g + j) * kD + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
       fence_proxy_async_smem();
-      named_bar_sync(1, 128);
+      named_bar_sync(1, 256);
       if (ctid == 0) {
-        for (int j = 0; j < kBQ; ++j) {
-          const int qq = q0 + j;
-          if (qq >= w.len) break;
-          __half* gdst = p.dq + ((w.start + qq) * p.hq + h) * kD;
-          bulk_reduce_add_f16(gdst, stg + j * kD, kD * 2);
-        }
+        // rows of the step beyond the sequence carry exact zeros
+        tma_reduce_add_3d(&tma_dq, 0, h, static_cast<int32_t>(w.start + q0), stg);
         bulk_commit();
       }
     }
     if (ctid == 0) bulk_wait0();
-    // epilogue: dK (times softmax_scale) and dV -> bf16
+    // epilogue: warpgroup 0 writes dK (times softmax_scale), 1 writes dV
     if (ok) ok = mbar_wait(&bars->acc_done, 0, p.err, abort, 62);
     if (ok) {
       tc_fence_after();
       const bool valid = key < w.len;
       const int64_t tok = w.start + key;
+      const uint32_t col = g == 0 ? kColDK : kColDV;
+      const float mul = g == 0 ? p.softmax_scale : 1.f;
+      __nv_bfloat16* out = (g == 0 ? p.dk : p.dv) + (tok * p.hkv + w.kvh) * kD;
+      uint4* dst = reinterpret_cast<uint4*>(out);
+      uint32_t r[32];
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? kColDK : kColDV;
-        const float mul = which == 0 ? p.softmax_scale : 1.f;
-        __nv_bfloat16* out = (which == 0 ? p.dk : p.dv) + (tok * p.hkv + w.kvh) * kD;
-        uint4* dst = reinterpret_cast<uint4*>(out);
-        uint32_t r[32];
-#pragma unroll 1
-        for (int c = 0; c < kD / 32; ++c) {
-          tmem_ld32(tmem + lb + col + 32 * c, r);
-          tmem_ld_wait();
-          if (valid) {
+      for (int c = 0; c < kD / 32; ++c) {
+        tmem_ld32(tmem + lb + col + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              uint32_t wv[4];
+          for (int t = 0; t < 4; ++t) {
+            uint32_t wv[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * t + 2 * k]) * mul,
-                                                          __uint_as_float(r[8 * t + 2 * k + 1]) * mul);
-                wv[k] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              dst[4 * c + t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            for (int k = 0; k < 4; ++k) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(r[8 * t + 2 * k]) * mul,
+                                                        __uint_as_float(r[8 * t + 2 * k + 1]) * mul);
+              wv[k] = *reinterpret_cast<uint32_t*>(&h2);
             }
+            dst[4 * c + t] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
       }
@@ -616,6 +601,16 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   if ((st = make(&tdo, do8, hq, kBQ)) != LPFA_OK) return st;
   if ((st = make(&tk, k8, hkv, kBN)) != LPFA_OK) return st;
   if ((st = make(&tv, v8, hkv, kBN)) != LPFA_OK) return st;
+  CUtensorMap tdq;
+  {
+    uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(hq),
+                        static_cast<uint64_t>(sv.total_tokens)};
+    uint64_t strides[2] = {static_cast<uint64_t>(D * 2), static_cast<uint64_t>(hq * D * 2)};
+    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, static_cast<uint32_t>(kBQ)};
+    if ((st = encode_tmap(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dq, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_NONE)) != LPFA_OK)
+      return st;
+  }
 
   BwdParams p;
   p.seqs = sv;
@@ -650,7 +645,7 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
                                          static_cast<int>(smem)));
     attr = true;
   }
-  mx_attn_bwd_kernel<<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, tdo, p);
+  mx_attn_bwd_kernel<<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, tdo, tdq, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   if (desc->dq_static_scale != 1.0f) {
     const int64_t n2 = sv.total_tokens * hq * D / 2;

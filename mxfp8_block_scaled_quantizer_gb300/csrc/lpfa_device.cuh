@@ -146,6 +146,18 @@ __device__ __forceinline__ void bulk_reduce_add_f16(void* gdst,
       : "memory");
 }
 
+// Element-wise reduce-add of a shared-memory box into a tensor (the box and
+// element type come from the tensor map; rows outside the tensor are skipped).
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, int32_t x,
+                                                  int32_t y, int32_t z,
+                                                  const void* smem_src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group "
+      "[%0, {%1, %2, %3}], [%4];" ::"l"(tmap),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
