@@ -224,6 +224,43 @@ lpfa_status lpfa_bwd(const lpfa_attn_desc* desc,
                      void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * lpfa_bwd_noalloc — the backward for callers that cannot allocate device
+ * memory.  (The pages have no counterpart; this is a library convenience.)
+ *
+ * Some callers cannot hand lpfa_bwd a workspace: code embedded in a runtime
+ * that owns every device buffer and gives plugins no allocator, or
+ * latency-critical code that must not call cudaMalloc because it can
+ * synchronise the whole device.  This entry point takes the same inputs and
+ * outputs as lpfa_bwd but keeps its scratch (the error word, and the
+ * per-row log2-LSE and D_i arrays) in one static device array of
+ * LPFA_BWD_NOALLOC_SCRATCH_BYTES bytes that the library holds on every GPU
+ * that loads it, until the process exits.  It allocates nothing itself.
+ *  - Size limit: needs lpfa_bwd_workspace_size(desc) <= the array size
+ *    (256 + 8 * heads_q * total_sf_rows bytes); larger problems return
+ *    LPFA_ERR_INVALID_ARG before any device work.
+ *  - The first call on a device looks up the array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture begins.
+ *  - All calls share the array.  Each call clears the part it uses before
+ *    its kernels run, but two calls whose work overlaps on the GPU (on
+ *    different streams, or on different host threads without ordering)
+ *    race on it: serialise them.
+ *  - Expired kernel waits are recorded in the shared array, which callers
+ *    cannot pass to lpfa_check; use lpfa_bwd with a workspace of your own
+ *    when that report is needed.
+ * Arguments, layouts and the returned gradients are those of lpfa_bwd. */
+#define LPFA_BWD_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+lpfa_status lpfa_bwd_noalloc(const lpfa_attn_desc* desc,
+                             const void* q8, const void* sfq_mma,
+                             const void* sfq_mma_t, const void* k8,
+                             const void* sfk_mma, const void* sfk_mma_t,
+                             const void* v8, const void* sfv_mma,
+                             const void* do8, const void* sfdo_mma,
+                             const void* sfdo_mma_t, const void* o,
+                             const void* dout, const float* lse, void* dq,
+                             void* dk, void* dv, void* stream);
+
 /* Synchronises `stream`, reads the error word of a workspace used by
  * lpfa_fwd / lpfa_bwd and returns LPFA_ERR_TIMEOUT if a kernel recorded an
  * expired wait, LPFA_ERR_CUDA if the stream holds an error, else LPFA_OK. */

@@ -29,6 +29,9 @@
 //   [448,512) scale factors (see kCol* below)
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <mutex>
+
 #include "lpfa_device.cuh"
 #include "lpfa_internal.h"
 #include "lpfa_seq.cuh"
@@ -654,4 +657,64 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
     LPFA_CHECK_CUDA(cudaGetLastError());
   }
   return LPFA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// lpfa_bwd_noalloc: the backward with its scratch in a static device array,
+// for callers that cannot allocate (see include/lpfa.h).  It forwards to
+// lpfa_bwd with the array as the workspace.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) uint8_t g_bwd_noalloc_scratch[LPFA_BWD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of the array on the current device; looked up once per
+// device, with that device current.
+lpfa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  LPFA_CHECK_CUDA(cudaGetDevice(&dev));
+  LPFA_CHECK_ARG(dev >= 0 && dev < kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    LPFA_CHECK_CUDA(cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch));
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return LPFA_OK;
+}
+
+}  // namespace
+
+extern "C" lpfa_status lpfa_bwd_noalloc(const lpfa_attn_desc* desc,
+                                        const void* q8, const void* sfq_mma,
+                                        const void* sfq_mma_t, const void* k8,
+                                        const void* sfk_mma, const void* sfk_mma_t,
+                                        const void* v8, const void* sfv_mma,
+                                        const void* do8, const void* sfdo_mma,
+                                        const void* sfdo_mma_t, const void* o,
+                                        const void* dout, const float* lse,
+                                        void* dq, void* dk, void* dv,
+                                        void* stream) {
+  LPFA_CHECK_ARG(desc != nullptr);
+  LPFA_CHECK_ARG(desc->heads_q >= 1 && desc->seqs.total_sf_rows >= 0);
+  const size_t need = bwd_ws_bytes(desc);
+  if (need > LPFA_BWD_NOALLOC_SCRATCH_BYTES) {
+    if (debug_enabled())
+      std::fprintf(stderr,
+                   "lpfa_bwd_noalloc: problem needs %zu scratch bytes, the static "
+                   "array holds %u (heads_q * total_sf_rows too large)\n",
+                   need, LPFA_BWD_NOALLOC_SCRATCH_BYTES);
+    return LPFA_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  lpfa_status st = noalloc_scratch(&scratch);
+  if (st != LPFA_OK) return st;
+  return lpfa_bwd(desc, q8, sfq_mma, sfq_mma_t, k8, sfk_mma, sfk_mma_t, v8, sfv_mma,
+                  do8, sfdo_mma, sfdo_mma_t, o, dout, lse, dq, dk, dv, scratch,
+                  LPFA_BWD_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -72,12 +72,16 @@ _bwd = _sig("lpfa_bwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
 _check = _sig("lpfa_check", ctypes.c_int, _vp, _vp)
+_bwd_noalloc = _sig("lpfa_bwd_noalloc", ctypes.c_int,
+                    ctypes.POINTER(lpfa_attn_desc), _vp, _vp, _vp, _vp, _vp,
+                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                    _vp)
 
 #: every symbol include/lpfa.h declares
 EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_mx_gemm",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
-            "lpfa_bwd", "lpfa_check")
+            "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc")
 
 
 class LpfaError(RuntimeError):
@@ -361,3 +365,14 @@ def mx_attention_backward(q, k, v, o, dout, lse, *, causal: bool,
     if check:
         lpfa_check(ws)
     return dq.reshape(shape_q), dk.reshape(shape_k), dv.reshape(shape_k)
+
+
+def lpfa_bwd_noalloc(desc, q8, sfq, sfq_t, k8, sfk, sfk_t, v8, sfv, do8, sfdo,
+                     sfdo_t, o, dout, lse, dq, dk, dv, stream=None):
+    """lpfa_bwd without a workspace argument: the library's static device
+    scratch array stands in for it (for callers that cannot allocate)."""
+    _ok(_bwd_noalloc(ctypes.byref(desc), _ptr(q8), _ptr(sfq), _ptr(sfq_t),
+                     _ptr(k8), _ptr(sfk), _ptr(sfk_t), _ptr(v8), _ptr(sfv),
+                     _ptr(do8), _ptr(sfdo), _ptr(sfdo_t), _ptr(o), _ptr(dout),
+                     _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+        "lpfa_bwd_noalloc")
