@@ -238,6 +238,8 @@ def run_lpfa(args, world, rank, local):
             e[4].record()
             times.append(e)
 
+    clk = ClockSampler(local).__enter__()   # sample from warm-up to end of e2e
+    time.sleep(1.0)                          # let the sampler start
     for _ in range(args.warmup):
         step()
     L.lpfa_check(fws)
@@ -245,16 +247,15 @@ def run_lpfa(args, world, rank, local):
     torch.cuda.synchronize()
 
     parts = []
-    with ClockSampler(local) as clk:
-        _barrier(world)
-        torch.cuda.synchronize()
-        t0, t1 = ev(), ev()
-        t0.record()
-        for _ in range(args.steps):
-            step(parts)
-        t1.record()
-        torch.cuda.synchronize()
-        _barrier(world)
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    t0.record()
+    for _ in range(args.steps):
+        step(parts)
+    t1.record()
+    torch.cuda.synchronize()
+    _barrier(world)
     L.lpfa_check(fws)
     L.lpfa_check(bws)
     ms = t0.elapsed_time(t1) / args.steps
@@ -295,6 +296,7 @@ def run_lpfa(args, world, rank, local):
         e2e_step()
     e1.record()
     torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
     e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())

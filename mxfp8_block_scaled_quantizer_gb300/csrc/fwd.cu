@@ -5,25 +5,37 @@
 // "Key Algorithmic Innovations" 1-2; "FlashAttention-4 Adds Low-Precision
 // Blackwell Support", "Technical Deep Dive"):
 //   S = Q K^T           block-scaled MXFP8 MMA into TMEM (fp32)
-//   online softmax      FP32 running reference max m and sum l per row, the
-//                       softmax scale folded into one FMA in log2 units;
-//                       m moves only when a tile's max exceeds it by more
-//                       than the rescale threshold (selective rescaling)
+//   online softmax      FP32 running reference max m and sum l per row in
+//                       log2 units (softmax scale folded in); m moves only
+//                       when a tile's max exceeds it by more than the
+//                       rescale threshold (selective rescaling)
 //   P -> MXFP8          1x32 blocks along keys; each block's scale comes from
-//                       the block's logit maximum already computed for the
-//                       row max (amax(P) = exp2(max x - m)), so no extra pass
+//                       the block's logit maximum already reduced for the row
+//                       max (amax(P) = 2^(max x - m)), and the block scale is
+//                       folded into the exponent: p * 2^-e = 2^(x - m - e)
 //   O += P V            block-scaled MMA, P read from TMEM as the A operand
 //   epilogue            O / l -> bf16, LSE = (m + log2 l) ln 2
 //
-// CTA = one 128-query tile of one (sequence, head).  Warp roles:
-//   warp 0     TMA producer: Q tile once, then K_j, V_j and their scale tiles
+// CTA = two 128-query tiles of one (sequence, head) sharing every K/V tile.
+// Warp roles:
+//   warp 0     TMA producer: Q tiles once, then K_j, V_j and their scale tiles
 //              through a 3-stage shared-memory ring.
 //   warp 1     TMEM owner and MMA issuer (one thread).
-//   warps 2-5  softmax: thread i owns query row i = TMEM lane i.
-// TMEM columns (512): S double buffer [0,128) [128,256); O [256,256+D);
-// scale factors from column 384: SFQ (4), SFK per stage (4 each), SFV per
-// stage (4 each), SFP per S buffer (4 each).  P (fp8) overwrites the first
-// 32 columns of its S buffer after the row has been read.
+//   warps 2-5  softmax of query tile 0, warps 6-9 of tile 1 (thread = row =
+//              TMEM lane).
+//
+// TMEM budget (all 512 columns; "TMEM allocation strategies that fit scale
+// factors into the fully utilized 512-column TMEM with minimal new
+// barriers", paragraph 2 of the first page):
+//   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D)
+// No column is free, so the scale factors live inside the S buffers:
+//   - P_i (fp8) overwrites S_i[0,32) once the softmax has read the row; the
+//     PV scales sit beside it: SFP_i at S_i[32,36), SFV_j at S_i[36,40).
+//   - The scales of the S_i MMA (SFQ_i, SFK_j) cannot sit in S_i, which that
+//     MMA writes; they are copied into the tail S_{1-i}[120,128) of the other
+//     tile, which is dead once that tile's softmax has read its row tail.
+//     One new barrier per tile ("S tail read") orders this; everything else
+//     reuses the S-full / P-full / PV-done barriers.
 #include <cuda_runtime.h>
 
 #include "lpfa_device.cuh"
@@ -33,16 +45,13 @@
 namespace lpfa {
 namespace {
 
-constexpr int kBlockM = 128;   // queries per CTA
+constexpr int kBlockM = 128;   // queries per tile (two tiles per CTA)
 constexpr int kBlockN = 128;   // keys per tile
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColO = 256, kColSF = 384;
-constexpr uint32_t kColSFQ = kColSF;
-constexpr uint32_t kColSFK = kColSF + 4;                     // + 4*stage
-constexpr uint32_t kColSFV = kColSFK + 4 * kStages;          // + 4*stage
-constexpr uint32_t kColSFP = kColSFV + 4 * kStages;          // + 4*buffer
+constexpr uint32_t kTailSFQ = 120, kTailSFK = 124;   // in the other S buffer
+constexpr uint32_t kColSFP = 32, kColSFV = 36;       // in the own S buffer
 
 struct FwdParams {
   SeqView seqs;
@@ -53,7 +62,7 @@ struct FwdParams {
   float* lse;           // [Hq, T]
   uint32_t* err;
   int32_t hq, hkv, group;
-  int32_t ntile_q;      // dense: q tiles per sequence
+  int32_t npairs;       // dense: query-tile pairs per sequence
   int32_t causal;
   float scale_log2;     // softmax_scale * log2(e)
   float threshold;      // log2 units
@@ -61,12 +70,12 @@ struct FwdParams {
 
 template <int D>
 struct FwdSmem {
-  static constexpr int kTile = kBlockN * D;          // bytes of one fp8 tile
-  static constexpr int kQ = 0;
-  static constexpr int kStage0 = kQ + kBlockM * D;   // stage s: K, V
+  static constexpr int kTile = kBlockN * D;            // bytes of one fp8 tile
+  static constexpr int kQ = 0;                         // Q0, Q1
+  static constexpr int kStage0 = 2 * kBlockM * D;      // stage s: K, V
   static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kSf0 = kStage0 + kStages * kStageBytes;  // SFQ, then per stage SFK, SFV
-  static constexpr int kBar = kSf0 + 512 * (1 + 2 * kStages);
+  static constexpr int kSf0 = kStage0 + kStages * kStageBytes;  // SFQ0, SFQ1, SFK[s], SFV[s]
+  static constexpr int kBar = kSf0 + 512 * (2 + 2 * kStages);
   static constexpr int kTotal = kBar + 256;
 };
 
@@ -75,6 +84,7 @@ struct FwdBars {
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
+  uint64_t s_tail[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t drain;
@@ -86,6 +96,29 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two lanes of fp32 math in one instruction.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -101,35 +134,37 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Work item of this CTA: (sequence, q tile, head); heavy causal tiles first.
+// Work item of this CTA: (sequence, pair of q tiles, head); heavy causal
+// pairs first.  Returns false for CTAs without work (odd padded tiles).
 struct WorkItem {
-  int seq, qtile, head;
-  int64_t start;      // first token of the sequence
+  int seq, qtile, head;   // qtile = first tile of the pair (even)
+  int64_t start;          // first token of the sequence
   int32_t len;
-  int64_t sf_tile;    // padded 128-row tile index of this q tile
+  int64_t sf_tile;        // padded 128-row tile index of qtile
 };
 
-__device__ __forceinline__ WorkItem work_item(const FwdParams& p) {
-  WorkItem w;
+__device__ __forceinline__ bool work_item(const FwdParams& p, WorkItem& w) {
   const int64_t idx = blockIdx.x;
   w.head = static_cast<int>(idx % p.hq);
   const int64_t rest = idx / p.hq;
   if (p.seqs.cu_seqlens == nullptr) {
     const int nseq = p.seqs.nseq;
     w.seq = static_cast<int>(rest % nseq);
-    w.qtile = p.ntile_q - 1 - static_cast<int>(rest / nseq);
+    w.qtile = 2 * (p.npairs - 1 - static_cast<int>(rest / nseq));
   } else {
-    // padded tile space enumerates every (sequence, q tile)
+    // the padded tile space enumerates every (sequence, q tile); even tiles
+    // of a sequence start a pair
     const int64_t t = rest;
     w.seq = seq_of_sf_row(p.seqs, t * 128);
     const SeqInfo si = seq_info(p.seqs, w.seq);
     w.qtile = static_cast<int>((t * 128 - si.sf_start) / 128);
+    if (w.qtile & 1) return false;
   }
   const SeqInfo si = seq_info(p.seqs, w.seq);
   w.start = si.start;
   w.len = si.len;
   w.sf_tile = si.sf_start / 128 + w.qtile;
-  return w;
+  return w.qtile * kBlockM < w.len;
 }
 
 template <int D>
@@ -149,12 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const WorkItem w = work_item(p);
+  WorkItem w;
+  if (!work_item(p, w)) return;                    // uniform for the CTA
   const int kvh = w.head / p.group;
-  const int q0 = w.qtile * kBlockM;                 // first query (in sequence)
-  if (q0 >= w.len) return;                          // uniform for the CTA
-  const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
-  const int ntiles = (kv_len + kBlockN - 1) / kBlockN;
+  const int q0 = w.qtile * kBlockM;                // first query of tile 0
+  // key tiles per query tile (0 when the tile lies beyond the sequence)
+  auto ntiles_of = [&](int i) {
+    const int qi0 = q0 + i * kBlockM;
+    const int kv_len = p.causal ? min(w.len, qi0 + kBlockM) : w.len;
+    return qi0 < w.len ? (kv_len + kBlockN - 1) / kBlockN : 0;
+  };
+  const int nt0 = ntiles_of(0), nt1 = ntiles_of(1);
+  auto nt = [nt0, nt1](int i) { return i == 0 ? nt0 : nt1; };
+  const int nmax = max(nt0, nt1);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -164,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_tail[b], 4);
       mbar_init(&bars->p_full[b], 4);
       mbar_init(&bars->pv_done[b], 1);
     }
@@ -179,6 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // S_i at column 128 i, O_i at column 256 + D i (computed, not indexed, so
+  // that no per-thread array lands in local memory)
+  auto tS = [tmem](int i) { return tmem + 128u * static_cast<uint32_t>(i); };
+  auto tO = [tmem](int i) { return tmem + 256u + static_cast<uint32_t>(D * i); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -187,15 +234,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tma_k);
       tma_prefetch_desc(&tma_v);
       const int32_t row_q = static_cast<int32_t>(w.start + q0);
-      mbar_arrive_expect_tx(&bars->q_full, kBlockM * D + 512);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * kBlockM * D + 1024);
       tma_load_3d(sm + L::kQ, &tma_q, 0, w.head, row_q, &bars->q_full);
-      bulk_load(sm + L::kSf0, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
-                &bars->q_full);
+      tma_load_3d(sm + L::kQ + kBlockM * D, &tma_q, 0, w.head, row_q + kBlockM, &bars->q_full);
+      // the second tile's scale tile exists in the padded space whenever the
+      // first does (a sequence's padded rows cover whole 128-row tiles); for
+      // a missing second tile it is the next sequence's, and unused
+      const int64_t sfq_last = p.seqs.total_sf_rows / 128 - 1;
+      const int64_t sft1 = w.sf_tile + 1 <= sfq_last ? w.sf_tile + 1 : w.sf_tile;
+      bulk_load(sm + L::kSf0, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512, &bars->q_full);
+      bulk_load(sm + L::kSf0 + 512, p.sfq + (sft1 * p.hq + w.head) * 512, 512, &bars->q_full);
       const int64_t kv_sf_tile0 = w.sf_tile - w.qtile;   // first tile of sequence
       bool ok = true;
       int issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = -1;
-      for (int j = 0; j < ntiles; ++j) {
+      for (int j = 0; j < nmax; ++j) {
         const int s = j % kStages;
         const uint32_t ph = (j / kStages) & 1;
         ok = mbar_wait(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
@@ -207,8 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(kbuf, &tma_k, 0, kvh, row_k, bar);
         tma_load_3d(kbuf + L::kTile, &tma_v, 0, kvh, row_k, bar);
         const int64_t sft = (kv_sf_tile0 + j) * p.hkv + kvh;
-        bulk_load(sm + L::kSf0 + 512 * (1 + s), p.sfk + sft * 512, 512, bar);
-        bulk_load(sm + L::kSf0 + 512 * (1 + kStages + s), p.sfv + sft * 512, 512, bar);
+        bulk_load(sm + L::kSf0 + 512 * (2 + s), p.sfk + sft * 512, 512, bar);
+        bulk_load(sm + L::kSf0 + 512 * (2 + kStages + s), p.sfv + sft * 512, 512, bar);
         issued[s] = static_cast<int>(ph);
       }
       if (!ok) {
@@ -223,154 +276,176 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
       const uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
-      const uint32_t q_addr = smem_u32(sm + L::kQ);
       bool ok = mbar_wait(&bars->q_full, 0, p.err, abort, 20);
-      if (ok) {
-        tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + kColSFQ, sf_tile_desc(smem_u32(sm + L::kSf0)));
-      }
-      // issue S_j = Q K_j^T into S buffer j%2
-      auto issue_s = [&](int j) -> bool {
+      if (ok) tc_fence_after();
+      // S_i,j = Q_i K_j^T; its scales go to the tail of the other S buffer
+      auto issue_s = [&](int i, int j) -> bool {
         const int s = j % kStages;
-        if (!mbar_wait(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21)) return false;
-        tc_fence_after();
+        const int o = 1 - i;
+        // the other tile's softmax must have read its row tail (its S MMA of
+        // this key tile for o = 1, of the previous one for o = 0 ... any
+        // earlier S of tile o still being read)
+        const int jo = (o == 0) ? j : j - 1;      // last S of tile o issued
+        if (jo >= 0 && jo < nt(o)) {
+          if (!mbar_wait(&bars->s_tail[o], jo & 1, p.err, abort, 23)) return false;
+          tc_fence_after();
+        }
+        const uint32_t sf_t = tS(o) + kTailSFQ;
+        tc_cp_32x128b_warpx4(sf_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * i)));
+        tc_cp_32x128b_warpx4(tS(o) + kTailSFK,
+                             sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (2 + s))));
+        const uint32_t q_addr = smem_u32(sm + L::kQ + i * kBlockM * D);
         const uint32_t k_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes);
-        const uint32_t sfk_t = tmem + kColSFK + 4 * s;
-        tc_cp_32x128b_warpx4(sfk_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (1 + s))));
-        const uint32_t d_t = tmem + kColS0 + 128 * (j & 1);
 #pragma unroll
         for (int kb = 0; kb < D / 32; ++kb) {
-          mma_mxf8_ss(d_t, make_sdesc(q_addr + 32 * kb, 16, kSbo, kSw),
+          mma_mxf8_ss(tS(i), make_sdesc(q_addr + 32 * kb, 16, kSbo, kSw),
                       make_sdesc(k_addr + 32 * kb, 16, kSbo, kSw),
-                      idesc_sf_ids(idesc_s, kb, kb), tmem + kColSFQ, sfk_t, kb > 0);
+                      idesc_sf_ids(idesc_s, kb, kb), sf_t, tS(o) + kTailSFK, kb > 0);
         }
-        tc_commit(&bars->s_full[j & 1]);
+        tc_commit(&bars->s_full[i]);
         return true;
       };
-      // issue O += P_j V_j
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j % kStages, b = j & 1;
-        if (!mbar_wait(&bars->p_full[b], (j >> 1) & 1, p.err, abort, 22)) return false;
+      // O_i += P_i,j V_j; the last reader of stage j%kStages releases it
+      auto issue_pv = [&](int i, int j, bool release) -> bool {
+        const int s = j % kStages;
+        if (!mbar_wait(&bars->p_full[i], j & 1, p.err, abort, 22)) return false;
         tc_fence_after();
         const uint32_t v_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes + L::kTile);
-        const uint32_t sfv_t = tmem + kColSFV + 4 * s;
-        tc_cp_32x128b_warpx4(sfv_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (1 + kStages + s))));
-        const uint32_t p_t = tmem + kColS0 + 128 * b;
+        tc_cp_32x128b_warpx4(tS(i) + kColSFV,
+                             sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (2 + kStages + s))));
 #pragma unroll
         for (int kb = 0; kb < kBlockN / 32; ++kb) {
-          mma_mxf8_ts(tmem + kColO, p_t + 8 * kb,
-                      make_sdesc(v_addr + 32 * D * kb, 16, kSbo, kSw),
-                      idesc_sf_ids(idesc_o, kb, kb), tmem + kColSFP + 4 * b, sfv_t,
+          mma_mxf8_ts(tO(i), tS(i) + 8 * kb, make_sdesc(v_addr + 32 * D * kb, 16, kSbo, kSw),
+                      idesc_sf_ids(idesc_o, kb, kb), tS(i) + kColSFP, tS(i) + kColSFV,
                       (j > 0) || (kb > 0));
         }
-        tc_commit(&bars->kv_empty[s]);
-        tc_commit(&bars->pv_done[b]);
+        tc_commit(&bars->pv_done[i]);
+        if (release) tc_commit(&bars->kv_empty[s]);
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 1; j < ntiles && ok; ++j) {
-        ok = issue_s(j);
-        if (ok) ok = issue_pv(j - 1);
+      const bool has1 = nt(1) > 0;
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int s = j % kStages;
+        ok = mbar_wait(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21);
+        if (!ok) break;
+        tc_fence_after();
+        if (j < nt(0)) ok = issue_s(0, j);
+        if (ok && j >= 1 && j - 1 < nt(1)) ok = issue_pv(1, j - 1, true);
+        if (ok && j < nt(1)) ok = issue_s(1, j);
+        if (ok && j < nt(0)) ok = issue_pv(0, j, !has1);
       }
-      if (ok) ok = issue_pv(ntiles - 1);
+      if (ok && has1) ok = issue_pv(1, nmax - 1, true);
       if (!ok) *abort = 1;
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, nullptr, nullptr, 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
+    const int ti = (warp - 2) >> 2;               // query tile of this warpgroup
     const int quad = warp & 3;                    // TMEM lane quarter
     const int row = quad * 32 + lane;             // query row within tile
-    const int qi = q0 + row;                      // query index in sequence
+    const int qt0 = q0 + ti * kBlockM;            // first query of the tile
+    const int qi = qt0 + row;                     // query index in sequence
+    const int ntl = nt(ti);
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tSi = tS(ti) + lane_base;
     const float c2 = p.scale_log2;
+    const uint64_t c2x2 = pack2(c2, c2);
     float m_ref = -INFINITY;                      // log2 units
     float l = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int b = j & 1;
-      ok = mbar_wait(&bars->s_full[b], (j >> 1) & 1, p.err, abort, 30);
+    const int lim = p.causal ? min(w.len, qi + 1) : w.len;   // keys < lim visible
+    for (int j = 0; j < ntl && ok; ++j) {
+      ok = mbar_wait(&bars->s_full[ti], j & 1, p.err, abort, 30);
       if (!ok) break;
       tc_fence_after();
-      float s[kBlockN];
-      {
-        uint32_t r[32];
-#pragma unroll
-        for (int c = 0; c < kBlockN / 32; ++c) {
-          tmem_ld32(tmem + lane_base + kColS0 + 128 * b + 32 * c, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(r[i]);
-        }
-      }
-      // masking: keys beyond the sequence, and causal j > i
       const int k0 = j * kBlockN;
-      const bool need_mask = (k0 + kBlockN > w.len) || (p.causal && k0 + kBlockN - 1 > q0);
+      const bool need_mask = (k0 + kBlockN > w.len) || (p.causal && k0 + kBlockN - 1 > qt0);
+      // the whole 128-column row in one round trip; once it is in registers
+      // the other tile's S MMA may park its scale factors in the row tail
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tSi + 32 * c, sv[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_tail[ti]);
       if (need_mask) {
-        const int lim = p.causal ? min(w.len, qi + 1) : w.len;
 #pragma unroll
-        for (int i = 0; i < kBlockN; ++i)
-          if (k0 + i >= lim) s[i] = -INFINITY;
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (k0 + 32 * c + e >= lim) sv[c][e] = __float_as_uint(-INFINITY);
       }
-      // chunk and tile maxima (raw logits; c2 > 0 so the order is kept)
-      float cmax[kBlockN / 32];
+      // chunk maxima of the raw logits (c2 > 0 keeps the order)
+      float cmax[4];
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
-        float mx = s[32 * c];
+      for (int c = 0; c < 4; ++c) {
+        float a = __uint_as_float(sv[c][0]);
 #pragma unroll
-        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[32 * c + i]);
-        cmax[c] = mx;
+        for (int e = 1; e < 31; e += 2)
+          a = max3(a, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+        cmax[c] = fmaxf(a, __uint_as_float(sv[c][31]));
       }
-      float tmax = cmax[0];
-#pragma unroll
-      for (int c = 1; c < kBlockN / 32; ++c) tmax = fmaxf(tmax, cmax[c]);
+      const float tmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
       const float mt = __fmul_rn(tmax, c2);
       float m_new = m_ref;
       if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
       const bool moved = (m_new != m_ref);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
-      // P = exp2(x - m) with x = fl(s*c2) rounded on its own (no fused
-      // multiply-add), so the element that defines m gives exactly 2^0 and
-      // the block holding it gets the scale of amax = 1.  Quantized per
-      // 32-key block; the block amax reuses the chunk maxima of the row max.
-      uint32_t pw[32];
+      // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
+      uint32_t code[4];
       uint32_t sfp = 0;
-      float lsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c) {
+      for (int c = 0; c < 4; ++c) {
         const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
-        const uint32_t code = e8m0_code_from_amax_bits(__float_as_uint(amax));
-        const float inv = inv_scale_from_code(code);
-        sfp |= code << (8 * c);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float p0 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 0], c2), m_use));
-          const float p1 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 1], c2), m_use));
-          const float p2 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 2], c2), m_use));
-          const float p3 = ex2(__fsub_rn(__fmul_rn(s[32 * c + i + 3], c2), m_use));
-          lsum += (p0 + p1) + (p2 + p3);
-          pw[8 * c + i / 4] = cvt_e4m3x4(p0 * inv, p1 * inv, p2 * inv, p3 * inv);
-        }
+        code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
+        sfp |= code[c] << (8 * c);
       }
-      // P and its scales into TMEM (S columns [0,32) of this buffer; the
-      // A-operand scale of row r sits at lane r, column SFP + r/32)
-      tmem_st32(tmem + lane_base + kColS0 + 128 * b, pw);
-      tmem_st1(tmem + lane_base + kColSFP + 4 * b + quad, sfp);
+      // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
+      // the scaled values per block and rescales by 2^e
+      uint32_t pw[32];
+      float lsum = 0.f;
+      auto do_chunk = [&](int c, const uint32_t (&v)[32]) {
+        const int e = static_cast<int>(code[c]) - 127;
+        const float nb = -(m_use + static_cast<float>(e));
+        const uint64_t nb2 = pack2(nb, nb);
+        uint64_t acc = 0;
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          const uint64_t x0 = fma2(pack2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c2x2, nb2);
+          const uint64_t x1 = fma2(pack2(__uint_as_float(v[2 * k + 2]), __uint_as_float(v[2 * k + 3])), c2x2, nb2);
+          const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
+          const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
+          acc = add2(acc, pack2(p0, p1));
+          acc = add2(acc, pack2(p2, p3));
+          pw[8 * c + k / 2] = cvt_e4m3x4(p0, p1, p2, p3);
+        }
+        // 2^e as fp32 (e in [-127, 119]; 2^-127 flushes to 0, harmless: such
+        // blocks hold only zeros)
+        const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+        lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
+      };
+#pragma unroll
+      for (int c = 0; c < 4; ++c) do_chunk(c, sv[c]);
+      // P and its scales into TMEM: P over S_i[0,32), SFP at S_i[32 + r/32]
+      tmem_st32(tSi, pw);
+      tmem_st1(tSi + kColSFP + quad, sfp);
       tmem_st_wait();
-      // selective rescale of O (and l): only warps holding a moved row
+      // selective rescale of O_i (and l): only warps holding a moved row
       if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
-        ok = mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err, abort, 31);
+        ok = mbar_wait(&bars->pv_done[ti], (j - 1) & 1, p.err, abort, 31);
         if (!ok) break;
         tc_fence_after();
         uint32_t r[32];
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
-          const uint32_t ta = tmem + lane_base + kColO + 32 * c;
+          const uint32_t ta = tO(ti) + lane_base + 32 * c;
           tmem_ld32(ta, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
           tmem_st32(ta, r);
         }
         tmem_st_wait();
@@ -379,43 +454,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_ref = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (lane == 0) mbar_arrive(&bars->p_full[ti]);
     }
     // epilogue: O / l -> bf16, LSE
-    if (ok) {
-      const int jl = ntiles - 1;
-      ok = mbar_wait(&bars->pv_done[jl & 1], (jl >> 1) & 1, p.err, abort, 32);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const bool valid = qi < w.len;
-      const int64_t tok = w.start + qi;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D);
-      uint32_t r[32];
+    if (ok && ntl > 0) {
+      ok = mbar_wait(&bars->pv_done[ti], (ntl - 1) & 1, p.err, abort, 32);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const bool valid = qi < w.len;
+        const int64_t tok = w.start + qi;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D);
+        uint32_t r[32];
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + kColO + 32 * c, r);
-        tmem_ld_wait();
-        if (valid) {
+        for (int c = 0; c < D / 32; ++c) {
+          tmem_ld32(tO(ti) + lane_base + 32 * c, r);
+          tmem_ld_wait();
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t wv[4];
+            for (int i = 0; i < 4; ++i) {
+              uint32_t wv[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                  __uint_as_float(r[8 * i + 2 * k]) * inv_l,
-                  __uint_as_float(r[8 * i + 2 * k + 1]) * inv_l);
-              wv[k] = *reinterpret_cast<uint32_t*>(&h2);
+              for (int k = 0; k < 4; ++k) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                    __uint_as_float(r[8 * i + 2 * k]) * inv_l,
+                    __uint_as_float(r[8 * i + 2 * k + 1]) * inv_l);
+                wv[k] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
-            dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
-      }
-      if (valid) {
-        const float lse2 = m_ref + __log2f(l);
-        p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
-            lse2 * 0.69314718055994531f;
+        if (valid) {
+          const float lse2 = m_ref + __log2f(l);
+          p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
+              lse2 * 0.69314718055994531f;
+        }
       }
     }
   }
@@ -461,15 +535,15 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   p.hq = static_cast<int32_t>(desc->heads_q);
   p.hkv = static_cast<int32_t>(desc->heads_kv);
   p.group = p.hq / p.hkv;
-  p.ntile_q = static_cast<int32_t>(ceil_div(sv.seqlen, kBlockM));
+  p.npairs = static_cast<int32_t>(ceil_div(ceil_div(sv.seqlen, kBlockM), 2));
   p.causal = desc->causal ? 1 : 0;
   p.scale_log2 = desc->softmax_scale * 1.4426950408889634f;
   p.threshold = desc->rescale_threshold;
 
-  const int64_t qtiles = sv.cu_seqlens == nullptr
-                             ? static_cast<int64_t>(sv.nseq) * p.ntile_q
-                             : sv.total_sf_rows / 128;
-  const int64_t nblocks = qtiles * p.hq;
+  const int64_t units = sv.cu_seqlens == nullptr
+                            ? static_cast<int64_t>(sv.nseq) * p.npairs
+                            : sv.total_sf_rows / 128;
+  const int64_t nblocks = units * p.hq;
   LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
   const size_t smem = FwdSmem<D>::kTotal + 1024;
   static bool attr = false;
