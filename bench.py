@@ -395,6 +395,30 @@ def run_lpfa(args, world, rank, local):
     return 0
 
 
+def run_profile_case(iters: int):
+    """One small pass of the hot path for ncu captures: B4 H16 S8192 D128
+    causal (128 MiB per bf16 tensor, larger than L2), fwd + bwd ``iters``
+    times, no timing."""
+    from mxfp8_block_scaled_quantizer_gb300 import build
+    build()
+    from mxfp8_block_scaled_quantizer_gb300 import lpfa as L
+    B, S, H, D = 4, 8192, 16, 128
+    g = torch.Generator(device="cuda").manual_seed(0)
+    mk = lambda: torch.randn(B * S, H, D, device="cuda", dtype=torch.bfloat16, generator=g)
+    q, k, v, do = mk(), mk(), mk(), mk()
+    seqs = L.dense_seqs(B, S)
+    desc = L.attn_desc(seqs, H, H, D, True, D ** -0.5)
+    for _ in range(iters):
+        mq, mk_, mv = L.quantize_forward_operands(q, k, v, seqs)
+        o, lse, ws = L.attention_forward_mx(mq, mk_, mv, desc)
+        bq, bk, bv, bdo = L.quantize_backward_operands(q, k, v, do, seqs)
+        dq, dk, dv, bws = L.attention_backward_mx(bq, bk, bv, bdo, o, do, lse, desc)
+    torch.cuda.synchronize()
+    L.lpfa_check(ws)
+    L.lpfa_check(bws)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -402,7 +426,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="lpfa", choices=["lpfa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", type=int, default=0, metavar="ITERS",
+                    help="run the small ncu capture case ITERS times and exit")
     args = ap.parse_args()
+    if args.profile_case:
+        return run_profile_case(args.profile_case)
     world, rank, local = _dist()
     try:
         if args.impl == "reference":

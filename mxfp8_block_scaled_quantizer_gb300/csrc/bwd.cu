@@ -39,35 +39,48 @@
 namespace lpfa {
 namespace {
 
-constexpr int kD = 128;          // head_dim of this kernel
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
 constexpr int kStages = 2;
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kColDK = 0, kColDV = 128, kColS = 256, kColDP = 320,
-                   kColDQ = 384;
-constexpr uint32_t kColSFK = 448, kColSFV = 452, kColSFKt = 456,
-                   kColSFQ = 460, kColSFdO = 464, kColSFQt = 468,
-                   kColSFdOt = 472, kColSFP = 476 /* +4g */,
-                   kColSFdS = 484 /* +4g */, kColSFdSB = 492;
 
-// shared memory layout (bytes from a 1024-aligned base)
-constexpr int kSmK = 0;                          // 128 x 128 B (SW128)
-constexpr int kSmV = kSmK + kBN * kD;            // 128 x 128 B
-constexpr int kSmStage0 = kSmV + kBN * kD;       // per stage: Q, dO, SFs, LSE2, Delta
-constexpr int kStQ = 0;
-constexpr int kStdO = kStQ + kBQ * kD;           // 8 KB each
-constexpr int kStSF = kStdO + kBQ * kD;          // SFQ, SFQt, SFdO, SFdOt (4 x 512)
-constexpr int kStLse = kStSF + 4 * 512;          // 64 floats
-constexpr int kStDelta = kStLse + kBQ * 4;       // 64 floats
-constexpr int kStageBytes = ((kStDelta + kBQ * 4) + 1023) / 1024 * 1024;
-constexpr int kSmDS = kSmStage0 + kStages * kStageBytes;   // 128 x 64 B (SW64)
-constexpr int kSmSFdS = kSmDS + kBN * kBQ;                 // 512 B
-constexpr int kSmSFkv = kSmSFdS + 512;                     // SFK, SFKt, SFV
-constexpr int kSmDQ = kSmSFkv + 3 * 512;                   // 2 x [64][128] fp16
-constexpr int kSmBar = kSmDQ + 2 * kBQ * kD * 2;
-constexpr int kSmTotal = kSmBar + 256;
+// Layout for head_dim D (64 or 128).
+template <int D>
+struct BwdCfg {
+  static constexpr uint32_t kSw = D == 128 ? 2u : 4u;   // 128B / 64B swizzle
+  static constexpr uint32_t kSbo = 8 * D;                // 8 rows of D bytes
+  // TMEM columns
+  static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D,
+                            kColDP = 2 * D + 64, kColDQ = 2 * D + 128;
+  static constexpr uint32_t kColSF = 2 * D + 192;
+  static constexpr uint32_t kColSFK = kColSF, kColSFV = kColSF + 4,
+                            kColSFKt = kColSF + 8, kColSFQ = kColSF + 12,
+                            kColSFdO = kColSF + 16, kColSFQt = kColSF + 20,
+                            kColSFdOt = kColSF + 24, kColSFP = kColSF + 28 /* +4g */,
+                            kColSFdS = kColSF + 36 /* +4g */, kColSFdSB = kColSF + 44;
+  // shared memory (bytes from a 1024-aligned base)
+  static constexpr int kSmK = 0;                                  // 128 x D (SW D)
+  static constexpr int kSmV = (kBN * D + 1023) / 1024 * 1024;     // 128 x D
+  // A operand of dQ^T = K^T dS^T needs 128-byte rows: for D = 64 a copy of
+  // the K tile zero-padded to 128 channels (64..127 give rows of zeros that
+  // are never read back); for D = 128 the K tile itself
+  static constexpr int kSmKT = kSmV + kBN * D;
+  static constexpr int kKTBytes = D == 128 ? 0 : kBN * 128;
+  static constexpr int kSmStage0 = kSmKT + kKTBytes;              // Q, dO, SFs, LSE2, Delta
+  static constexpr int kStQ = 0;
+  static constexpr int kStdO = kBQ * D;
+  static constexpr int kStSF = 2 * kBQ * D;                       // SFQ, SFQt, SFdO, SFdOt
+  static constexpr int kStLse = kStSF + 4 * 512;                  // 64 floats
+  static constexpr int kStDelta = kStLse + kBQ * 4;               // 64 floats
+  static constexpr int kStageBytes = ((kStDelta + kBQ * 4) + 1023) / 1024 * 1024;
+  static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes; // 128 x 64 B (SW64)
+  static constexpr int kSmSFdS = kSmDS + kBN * kBQ;               // 512 B
+  static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
+  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;  // 2 x [64][D] fp16
+  static constexpr int kSmBar = kSmDQ + 2 * kBQ * D * 2;
+  static constexpr int kSmTotal = kSmBar + 256;
+};
 
 struct BwdParams {
   SeqView seqs;
@@ -100,6 +113,7 @@ struct BwdBars {
   uint64_t dq_full;
   uint64_t dq_free;
   uint64_t acc_done;
+  uint64_t kt_ready;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -156,6 +170,7 @@ __device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t
   return code;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_attn_bwd_kernel(const __grid_constant__ CUtensorMap tma_q,
                        const __grid_constant__ CUtensorMap tma_k,
@@ -163,10 +178,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tma_do,
                        const __grid_constant__ CUtensorMap tma_dq,
                        const BwdParams p) {
+  using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  BwdBars* bars = reinterpret_cast<BwdBars*>(sm + kSmBar);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sm + C::kSmBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -190,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 8);
     mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->kt_ready, 4);
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_barrier_init();
@@ -217,12 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tma_dq);
       const int32_t row_k = static_cast<int32_t>(w.start + k0);
       const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * kBN * kD + 3 * 512);
-      tma_load_3d(sm + kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
-      tma_load_3d(sm + kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
-      bulk_load(sm + kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
-      bulk_load(sm + kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
-      bulk_load(sm + kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+      mbar_arrive_expect_tx(&bars->kv_full, 2 * kBN * D + 3 * 512);
+      tma_load_3d(sm + C::kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
+      tma_load_3d(sm + C::kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
+      bulk_load(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
+      bulk_load(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
+      bulk_load(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
       bool ok = true;
       int issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = -1;
@@ -232,21 +249,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
         if (!ok) break;
         const int h = step_head(i), q0 = step_q0(i);
-        uint8_t* st = sm + kSmStage0 + s * kStageBytes;
+        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
         uint64_t* bar = &bars->q_full[s];
-        mbar_arrive_expect_tx(bar, 2 * kBQ * kD + 4 * 512 + 2 * kBQ * 4);
+        mbar_arrive_expect_tx(bar, 2 * kBQ * D + 4 * 512 + 2 * kBQ * 4);
         const int32_t row_q = static_cast<int32_t>(w.start + q0);
-        tma_load_3d(st + kStQ, &tma_q, 0, h, row_q, bar);
-        tma_load_3d(st + kStdO, &tma_do, 0, h, row_q, bar);
+        tma_load_3d(st + C::kStQ, &tma_q, 0, h, row_q, bar);
+        tma_load_3d(st + C::kStdO, &tma_do, 0, h, row_q, bar);
         const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
         const int64_t qsf = (pr / 128) * p.hq + h;
-        bulk_load(st + kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
-        bulk_load(st + kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
-        bulk_load(st + kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
-        bulk_load(st + kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+        bulk_load(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
+        bulk_load(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
+        bulk_load(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
+        bulk_load(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
         const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
-        bulk_load(st + kStLse, p.lse2 + rowoff, kBQ * 4, bar);
-        bulk_load(st + kStDelta, p.delta + rowoff, kBQ * 4, bar);
+        bulk_load(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, bar);
+        bulk_load(st + C::kStDelta, p.delta + rowoff, kBQ * 4, bar);
         issued[s] = static_cast<int>(ph);
       }
       if (!ok) {
@@ -260,65 +277,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_st = idesc_mxf8(128, kBQ, 0, 0);     // S^T, dP^T
-      const uint32_t id_acc = idesc_mxf8(128, kD, 0, 1);     // dV, dK (B MN-major)
+      const uint32_t id_acc = idesc_mxf8(128, D, 0, 1);     // dV, dK (B MN-major)
       const uint32_t id_dq = idesc_mxf8(128, kBQ, 1, 1);     // dQ^T (A, B MN-major)
-      const uint32_t k_addr = smem_u32(sm + kSmK);
-      const uint32_t v_addr = smem_u32(sm + kSmV);
-      const uint32_t ds_addr = smem_u32(sm + kSmDS);
+      const uint32_t k_addr = smem_u32(sm + C::kSmK);
+      const uint32_t v_addr = smem_u32(sm + C::kSmV);
+      const uint32_t ds_addr = smem_u32(sm + C::kSmDS);
+      const uint32_t kt_addr = D == 128 ? k_addr : smem_u32(sm + C::kSmKT);
       bool ok = mbar_wait(&bars->kv_full, 0, p.err, abort, 50);
       if (ok) {
         tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + kColSFK, sf_tile_desc(smem_u32(sm + kSmSFkv)));
-        tc_cp_32x128b_warpx4(tmem + kColSFKt, sf_tile_desc(smem_u32(sm + kSmSFkv + 512)));
-        tc_cp_32x128b_warpx4(tmem + kColSFV, sf_tile_desc(smem_u32(sm + kSmSFkv + 1024)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFK, sf_tile_desc(smem_u32(sm + C::kSmSFkv)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
       }
       for (int i = 0; i < nsteps && ok; ++i) {
         const int s = i % kStages;
         ok = mbar_wait(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51);
         if (!ok) break;
         tc_fence_after();
-        uint8_t* st = sm + kSmStage0 + s * kStageBytes;
-        const uint32_t q_addr = smem_u32(st + kStQ);
-        const uint32_t do_addr = smem_u32(st + kStdO);
+        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
+        const uint32_t q_addr = smem_u32(st + C::kStQ);
+        const uint32_t do_addr = smem_u32(st + C::kStdO);
         const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
-        tc_cp_32x128b_warpx4(tmem + kColSFQ, sf_tile_desc(smem_u32(st + kStSF)));
-        tc_cp_32x128b_warpx4(tmem + kColSFdO, sf_tile_desc(smem_u32(st + kStSF + 1024)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFQ, sf_tile_desc(smem_u32(st + C::kStSF)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFdO, sf_tile_desc(smem_u32(st + C::kStSF + 1024)));
         // S^T = K Q^T and dP^T = V dO^T (contraction over head_dim)
 #pragma unroll
-        for (int kb = 0; kb < kD / 32; ++kb) {
-          mma_mxf8_ss(tmem + kColS, make_sdesc(k_addr + 32 * kb, 16, 1024, 2),
-                      make_sdesc(q_addr + 32 * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_st, kb, kb), tmem + kColSFK,
-                      tmem + kColSFQ + 2 * half, kb > 0);
+        for (int kb = 0; kb < D / 32; ++kb) {
+          mma_mxf8_ss(tmem + C::kColS, make_sdesc(k_addr + 32 * kb, 16, C::kSbo, C::kSw),
+                      make_sdesc(q_addr + 32 * kb, 16, C::kSbo, C::kSw),
+                      idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
+                      tmem + C::kColSFQ + 2 * half, kb > 0);
         }
 #pragma unroll
-        for (int kb = 0; kb < kD / 32; ++kb) {
-          mma_mxf8_ss(tmem + kColDP, make_sdesc(v_addr + 32 * kb, 16, 1024, 2),
-                      make_sdesc(do_addr + 32 * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_st, kb, kb), tmem + kColSFV,
-                      tmem + kColSFdO + 2 * half, kb > 0);
+        for (int kb = 0; kb < D / 32; ++kb) {
+          mma_mxf8_ss(tmem + C::kColDP, make_sdesc(v_addr + 32 * kb, 16, C::kSbo, C::kSw),
+                      make_sdesc(do_addr + 32 * kb, 16, C::kSbo, C::kSw),
+                      idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
+                      tmem + C::kColSFdO + 2 * half, kb > 0);
         }
         tc_commit(&bars->st_ready);
         ok = mbar_wait(&bars->ds_ready, i & 1, p.err, abort, 52);
         if (!ok) break;
         tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + kColSFQt, sf_tile_desc(smem_u32(st + kStSF + 512)));
-        tc_cp_32x128b_warpx4(tmem + kColSFdOt, sf_tile_desc(smem_u32(st + kStSF + 1536)));
-        tc_cp_32x128b_warpx4(tmem + kColSFdSB, sf_tile_desc(smem_u32(sm + kSmSFdS)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFQt, sf_tile_desc(smem_u32(st + C::kStSF + 512)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFdOt, sf_tile_desc(smem_u32(st + C::kStSF + 1536)));
+        tc_cp_32x128b_warpx4(tmem + C::kColSFdSB, sf_tile_desc(smem_u32(sm + C::kSmSFdS)));
         // dV += P^T dO, dK += dS^T Q (contraction over the 64 queries)
 #pragma unroll
         for (int kb = 0; kb < kBQ / 32; ++kb) {
           const uint32_t sfb = kb + 2 * half;
-          mma_mxf8_ts(tmem + kColDV, tmem + kColS + 32 * kb,
-                      make_sdesc(do_addr + 32 * kD * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_acc, 0, sfb), tmem + kColSFP + 4 * kb,
-                      tmem + kColSFdOt, (i > 0) || (kb > 0));
-          mma_mxf8_ts(tmem + kColDK, tmem + kColDP + 32 * kb,
-                      make_sdesc(q_addr + 32 * kD * kb, 16, 1024, 2),
-                      idesc_sf_ids(id_acc, 0, sfb), tmem + kColSFdS + 4 * kb,
-                      tmem + kColSFQt, (i > 0) || (kb > 0));
+          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColS + 32 * kb,
+                      make_sdesc(do_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
+                      idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFP + 4 * kb,
+                      tmem + C::kColSFdOt, (i > 0) || (kb > 0));
+          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDP + 32 * kb,
+                      make_sdesc(q_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
+                      idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFdS + 4 * kb,
+                      tmem + C::kColSFQt, (i > 0) || (kb > 0));
         }
         // dQ^T = K^T dS^T (contraction over the 128 keys)
+        if (D != 128 && i == 0) {
+          ok = mbar_wait(&bars->kt_ready, 0, p.err, abort, 54);
+          if (!ok) break;
+        }
         if (i > 0) {
           ok = mbar_wait(&bars->dq_free, (i - 1) & 1, p.err, abort, 53);
           if (!ok) break;
@@ -326,10 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int kb = 0; kb < kBN / 32; ++kb) {
-          mma_mxf8_ss(tmem + kColDQ, make_sdesc(k_addr + 32 * kD * kb, 16, 1024, 2),
+          mma_mxf8_ss(tmem + C::kColDQ, make_sdesc(kt_addr + 32 * 128 * kb, 16, 1024, 2),
                       make_sdesc(ds_addr + 32 * kBQ * kb, 16, 8 * kBQ, 4),
-                      idesc_sf_ids(id_dq, kb, kb), tmem + kColSFKt,
-                      tmem + kColSFdSB, kb > 0);
+                      idesc_sf_ids(id_dq, kb, kb), tmem + C::kColSFKt,
+                      tmem + C::kColSFdSB, kb > 0);
         }
         tc_commit(&bars->q_empty[s]);
         tc_commit(&bars->dq_full);
@@ -348,20 +370,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + m;
     const int ctid = threadIdx.x - 64;            // 0..255 among compute threads
     bool ok = true;
+    if (D != 128 && g == 0) {
+      // zero-padded 128-byte-row copy of the K tile (64B swizzle -> 128B)
+      ok = mbar_wait(&bars->kv_full, 0, p.err, abort, 59);
+      if (ok) {
+        const uint8_t* src = sm + C::kSmK + m * D;
+        uint8_t* dst = sm + C::kSmKT + m * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (c < D / 16) v = *reinterpret_cast<const uint4*>(src + 16 * (c ^ ((m >> 1) & 3)));
+          *reinterpret_cast<uint4*>(dst + 16 * (c ^ (m & 7))) = v;
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->kt_ready);
+    }
     for (int i = 0; i < nsteps && ok; ++i) {
       const int s = i % kStages;
       const int h = step_head(i), q0 = step_q0(i);
-      const uint8_t* st = sm + kSmStage0 + s * kStageBytes;
+      const uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
       ok = mbar_wait(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
       tc_fence_after();
       uint32_t rs[32], rd[32];
-      tmem_ld32(tmem + lb + kColS + 32 * g, rs);
-      tmem_ld32(tmem + lb + kColDP + 32 * g, rd);
+      tmem_ld32(tmem + lb + C::kColS + 32 * g, rs);
+      tmem_ld32(tmem + lb + C::kColDP + 32 * g, rd);
       float lse2[32], dlt[32];
       {
-        const float4* l4 = reinterpret_cast<const float4*>(st + kStLse) + 8 * g;
-        const float4* d4 = reinterpret_cast<const float4*>(st + kStDelta) + 8 * g;
+        const float4* l4 = reinterpret_cast<const float4*>(st + C::kStLse) + 8 * g;
+        const float4* d4 = reinterpret_cast<const float4*>(st + C::kStDelta) + 8 * g;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const float4 a4 = l4[t], b4 = d4[t];
@@ -386,13 +425,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t cd = quant_block32(dsv, wd);
       // P^T and dS^T (fp8) into TMEM at column 32 g of the consumed S^T /
       // dP^T block; their A-operand scales at lane m, column base + 4g + m/32
-      tmem_st8(tmem + lb + kColS + 32 * g, wp);
-      tmem_st8(tmem + lb + kColDP + 32 * g, wd);
-      tmem_st1(tmem + lb + kColSFP + 4 * g + quad, cp_);
-      tmem_st1(tmem + lb + kColSFdS + 4 * g + quad, cd);
+      tmem_st8(tmem + lb + C::kColS + 32 * g, wp);
+      tmem_st8(tmem + lb + C::kColDP + 32 * g, wd);
+      tmem_st1(tmem + lb + C::kColSFP + 4 * g + quad, cp_);
+      tmem_st1(tmem + lb + C::kColSFdS + 4 * g + quad, cd);
       // dS^T row chunks 2g, 2g+1 -> shared memory (64-byte rows, 64B swizzle)
       {
-        uint8_t* ds_row = sm + kSmDS + m * kBQ;
+        uint8_t* ds_row = sm + C::kSmDS + m * kBQ;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int phys = (2 * g + c) ^ ((m >> 1) & 3);
@@ -401,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // B-operand scale of dQ^T: (query n = 32 g + lane, key block quad)
-      sm[kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
+      sm[C::kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -413,18 +452,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t rq[32];
-      tmem_ld32(tmem + lb + kColDQ + 32 * g, rq);
+      tmem_ld32(tmem + lb + C::kColDQ + 32 * g, rq);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->dq_free);
       // stage fp16 rows [q][d], then one tensor reduce-add into global dQ
-      __half* stg = reinterpret_cast<__half*>(sm + kSmDQ + (i & 1) * kBQ * kD * 2);
+      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (i & 1) * kBQ * D * 2);
       if (ctid == 0) bulk_wait_read_le1();
       named_bar_sync(1, 256);
+      if (m < D) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        stg[(32 * g + j) * kD + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
+        for (int j = 0; j < 32; ++j)
+          stg[(32 * g + j) * D + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
+      }
       fence_proxy_async_smem();
       named_bar_sync(1, 256);
       if (ctid == 0) {
@@ -440,13 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool valid = key < w.len;
       const int64_t tok = w.start + key;
-      const uint32_t col = g == 0 ? kColDK : kColDV;
+      const uint32_t col = g == 0 ? C::kColDK : C::kColDV;
       const float mul = g == 0 ? p.softmax_scale : 1.f;
-      __nv_bfloat16* out = (g == 0 ? p.dk : p.dv) + (tok * p.hkv + w.kvh) * kD;
+      __nv_bfloat16* out = (g == 0 ? p.dk : p.dv) + (tok * p.hkv + w.kvh) * D;
       uint4* dst = reinterpret_cast<uint4*>(out);
       uint32_t r[32];
 #pragma unroll 1
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         tmem_ld32(tmem + lb + col + 32 * c, r);
         tmem_ld_wait();
         if (valid) {
@@ -570,7 +611,6 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   LPFA_CHECK_ARG(workspace != nullptr &&
                  (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0);
   LPFA_CHECK_ARG(workspace_bytes >= bwd_ws_bytes(desc));
-  if (desc->head_dim != 128) return LPFA_ERR_UNSUPPORTED;
   LPFA_CHECK_ARG(desc->dq_static_scale > 0.f);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (sv.total_tokens == 0) return LPFA_OK;
@@ -592,13 +632,13 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   }
 
   CUtensorMap tq, tk, tv, tdo;
+  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   auto make = [&](CUtensorMap* m, const void* base, int64_t heads, uint32_t rows) {
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
                         static_cast<uint64_t>(sv.total_tokens)};
     uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads * D)};
     uint32_t box[3] = {static_cast<uint32_t>(D), 1u, rows};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, sw);
   };
   if ((st = make(&tq, q8, hq, kBQ)) != LPFA_OK) return st;
   if ((st = make(&tdo, do8, hq, kBQ)) != LPFA_OK) return st;
@@ -640,15 +680,29 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
 
   const int64_t nblocks = (sv.total_sf_rows / 128) * hkv;
   LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
-  const size_t smem = kSmTotal + 1024;
-  static bool attr = false;
-  if (!attr) {
-    LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem)));
-    attr = true;
+  if (D == 128) {
+    const size_t smem = BwdCfg<128>::kSmTotal + 1024;
+    static bool attr = false;
+    if (!attr) {
+      LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel<128>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem)));
+      attr = true;
+    }
+    mx_attn_bwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
+        tq, tk, tv, tdo, tdq, p);
+  } else {
+    const size_t smem = BwdCfg<64>::kSmTotal + 1024;
+    static bool attr = false;
+    if (!attr) {
+      LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel<64>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem)));
+      attr = true;
+    }
+    mx_attn_bwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
+        tq, tk, tv, tdo, tdq, p);
   }
-  mx_attn_bwd_kernel<<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, tdo, tdq, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   if (desc->dq_static_scale != 1.0f) {
     const int64_t n2 = sv.total_tokens * hq * D / 2;

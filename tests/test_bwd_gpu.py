@@ -95,8 +95,19 @@ def test_bwd_isolated_with_oracle_forward(L):
             assert relfro(_tok(g)[rows], _tok(r)[rows]) < 1e-2, name
 
 
+def test_bwd_tiny_full(L):
+    """Tiny workload (head_dim 64, non-causal), every output compared."""
+    w = workloads.get_config("tiny")
+    x = workloads.make_inputs(w)
+    got = _gpu_fwd_bwd(L, x, w)
+    ref, _, _ = _oracle(x, w)
+    allr = (slice(None),)
+    _check(got, ref, allr, allr, "tiny")
+
+
 @pytest.mark.parametrize("case", [
     dict(batch=2, seqlen=200, heads_q=4, heads_kv=1, head_dim=128, causal=True),
+    dict(batch=2, seqlen=333, heads_q=4, heads_kv=2, head_dim=64, causal=True),
     dict(batch=1, seqlen=320, heads_q=2, heads_kv=2, head_dim=128, causal=False),
     dict(batch=1, seqlen=1, heads_q=1, heads_kv=1, head_dim=128, causal=True),
     dict(batch=3, seqlen=96, heads_q=2, heads_kv=2, head_dim=128, causal=True),
