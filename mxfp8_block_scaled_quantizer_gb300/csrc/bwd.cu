@@ -22,10 +22,14 @@
 // as one tensor reduce-add (FP16) of the 64x128 step tile.
 //
 // TMEM (512 columns):
-//   [  0,128) dK      [128,256) dV      [256,320) S^T -> P^T fp8 (16 cols)
-//   [320,384) dP^T -> dS^T fp8 (16 cols)   [384,448) dQ^T
-//   P^T / dS^T of query block g sit at S^T / dP^T column 32 g, inside the
-//   columns warpgroup g itself read.
+//   [  0,128) dK      [128,256) dV      [256,320) S^T      [320,384) dP^T
+//   [384,448) dQ^T, which between steps also holds the fp8 P^T / dS^T of
+//             query block g at columns 32g / 32g + 8 (inside the slice that
+//             warpgroup g alone reads back)
+// The steps are software-pipelined: S^T / dP^T of step i+1 are issued as
+// soon as step i's rows are in registers, and a warpgroup reads back dQ^T of
+// step i-1 after computing step i, so the MMAs of one step overlap the
+// elementwise work of the next.
 //   [448,512) scale factors (see kCol* below)
 #include <cuda_runtime.h>
 
@@ -111,7 +115,7 @@ struct BwdBars {
   uint64_t st_ready;
   uint64_t ds_ready;
   uint64_t dq_full;
-  uint64_t dq_free;
+  uint64_t st_loaded;
   uint64_t acc_done;
   uint64_t kt_ready;
   uint64_t drain;
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->st_ready, 1);
     mbar_init(&bars->ds_ready, 8);
     mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 8);
+    mbar_init(&bars->st_loaded, 8);
     mbar_init(&bars->acc_done, 1);
     mbar_init(&bars->kt_ready, 4);
     mbar_init(&bars->drain, 1);
@@ -290,10 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_cp_32x128b_warpx4(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
         tc_cp_32x128b_warpx4(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
       }
-      for (int i = 0; i < nsteps && ok; ++i) {
+      // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T (contraction over head_dim)
+      auto issue_st = [&](int i) -> bool {
         const int s = i % kStages;
-        ok = mbar_wait(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51);
-        if (!ok) break;
+        if (!mbar_wait(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51)) return false;
         tc_fence_after();
         uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
         const uint32_t q_addr = smem_u32(st + C::kStQ);
@@ -301,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
         tc_cp_32x128b_warpx4(tmem + C::kColSFQ, sf_tile_desc(smem_u32(st + C::kStSF)));
         tc_cp_32x128b_warpx4(tmem + C::kColSFdO, sf_tile_desc(smem_u32(st + C::kStSF + 1024)));
-        // S^T = K Q^T and dP^T = V dO^T (contraction over head_dim)
 #pragma unroll
         for (int kb = 0; kb < D / 32; ++kb) {
           mma_mxf8_ss(tmem + C::kColS, make_sdesc(k_addr + 32 * kb, 16, C::kSbo, C::kSw),
@@ -317,34 +320,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                       tmem + C::kColSFdO + 2 * half, kb > 0);
         }
         tc_commit(&bars->st_ready);
-        ok = mbar_wait(&bars->ds_ready, i & 1, p.err, abort, 52);
-        if (!ok) break;
+        return true;
+      };
+      // dV += P^T dO_i, dK += dS^T Q_i, then dQ^T(i) = K^T dS^T over the
+      // same columns the fp8 P^T / dS^T came from (MMAs execute in order)
+      auto issue_acc = [&](int i) -> bool {
+        const int s = i % kStages;
+        if (!mbar_wait(&bars->ds_ready, i & 1, p.err, abort, 52)) return false;
         tc_fence_after();
+        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
+        const uint32_t q_addr = smem_u32(st + C::kStQ);
+        const uint32_t do_addr = smem_u32(st + C::kStdO);
+        const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
         tc_cp_32x128b_warpx4(tmem + C::kColSFQt, sf_tile_desc(smem_u32(st + C::kStSF + 512)));
         tc_cp_32x128b_warpx4(tmem + C::kColSFdOt, sf_tile_desc(smem_u32(st + C::kStSF + 1536)));
         tc_cp_32x128b_warpx4(tmem + C::kColSFdSB, sf_tile_desc(smem_u32(sm + C::kSmSFdS)));
-        // dV += P^T dO, dK += dS^T Q (contraction over the 64 queries)
 #pragma unroll
         for (int kb = 0; kb < kBQ / 32; ++kb) {
           const uint32_t sfb = kb + 2 * half;
-          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColS + 32 * kb,
+          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColDQ + 32 * kb,
                       make_sdesc(do_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
                       idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFP + 4 * kb,
                       tmem + C::kColSFdOt, (i > 0) || (kb > 0));
-          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDP + 32 * kb,
+          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDQ + 32 * kb + 8,
                       make_sdesc(q_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
                       idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFdS + 4 * kb,
                       tmem + C::kColSFQt, (i > 0) || (kb > 0));
         }
-        // dQ^T = K^T dS^T (contraction over the 128 keys)
         if (D != 128 && i == 0) {
-          ok = mbar_wait(&bars->kt_ready, 0, p.err, abort, 54);
-          if (!ok) break;
-        }
-        if (i > 0) {
-          ok = mbar_wait(&bars->dq_free, (i - 1) & 1, p.err, abort, 53);
-          if (!ok) break;
-          tc_fence_after();
+          if (!mbar_wait(&bars->kt_ready, 0, p.err, abort, 54)) return false;
         }
 #pragma unroll
         for (int kb = 0; kb < kBN / 32; ++kb) {
@@ -355,6 +359,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(&bars->q_empty[s]);
         tc_commit(&bars->dq_full);
+        return true;
+      };
+      if (ok) ok = issue_st(0);
+      for (int i = 0; i < nsteps && ok; ++i) {
+        // the next step's S^T / dP^T run while step i is in the compute warps
+        if (i + 1 < nsteps) {
+          ok = mbar_wait(&bars->st_loaded, i & 1, p.err, abort, 53);
+          if (ok) ok = issue_st(i + 1);
+          if (!ok) break;
+        }
+        ok = issue_acc(i);
       }
       if (ok) tc_commit(&bars->acc_done);
       if (!ok) *abort = 1;
@@ -387,9 +402,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kt_ready);
     }
+    // dQ^T(j) (fp32, this warpgroup's 32 queries) -> fp16 rows [q][d] in
+    // shared memory -> one tensor reduce-add into global dQ
+    auto stage_dq = [&](int j, const uint32_t (&rq)[32]) {
+      const int hj = step_head(j), q0j = step_q0(j);
+      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (j & 1) * kBQ * D * 2);
+      if (ctid == 0) bulk_wait_read_le1();
+      named_bar_sync(1, 256);
+      if (m < D) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          stg[(32 * g + e) * D + m] = __float2half_rn(__uint_as_float(rq[e]) * p.dq_mult);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (ctid == 0) {
+        // rows of the step beyond the sequence carry exact zeros
+        tma_reduce_add_3d(&tma_dq, 0, hj, static_cast<int32_t>(w.start + q0j), stg);
+        bulk_commit();
+      }
+    };
+    auto read_dq = [&](int j, uint32_t (&rq)[32]) -> bool {
+      if (!mbar_wait(&bars->dq_full, j & 1, p.err, abort, 61)) return false;
+      tc_fence_after();
+      tmem_ld32(tmem + lb + C::kColDQ + 32 * g, rq);
+      tmem_ld_wait();
+      return true;
+    };
     for (int i = 0; i < nsteps && ok; ++i) {
       const int s = i % kStages;
-      const int h = step_head(i), q0 = step_q0(i);
+      const int q0 = step_q0(i);
       const uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
       ok = mbar_wait(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
@@ -409,6 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tmem_ld_wait();
+      // S^T / dP^T of this step are in registers: the next step's MMAs may go
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->st_loaded);
       float pv[32], dsv[32];
       const int qb0 = q0 + 32 * g;
 #pragma unroll
@@ -423,10 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t wp[8], wd[8];
       const uint32_t cp_ = quant_block32(pv, wp);
       const uint32_t cd = quant_block32(dsv, wd);
-      // P^T and dS^T (fp8) into TMEM at column 32 g of the consumed S^T /
-      // dP^T block; their A-operand scales at lane m, column base + 4g + m/32
-      tmem_st8(tmem + lb + C::kColS + 32 * g, wp);
-      tmem_st8(tmem + lb + C::kColDP + 32 * g, wd);
+      // the previous step's dQ^T leaves TMEM before this step's fp8 P^T /
+      // dS^T take its columns (and its MMA, the last reader of the dS^T
+      // shared-memory tile, has completed)
+      uint32_t rq[32];
+      if (i > 0) {
+        ok = read_dq(i - 1, rq);
+        if (!ok) break;
+      }
+      // P^T, dS^T (fp8) at dQ^T columns 32g and 32g + 8; their A-operand
+      // scales at lane m, column base + 4g + m/32
+      tmem_st8(tmem + lb + C::kColDQ + 32 * g, wp);
+      tmem_st8(tmem + lb + C::kColDQ + 32 * g + 8, wd);
       tmem_st1(tmem + lb + C::kColSFP + 4 * g + quad, cp_);
       tmem_st1(tmem + lb + C::kColSFdS + 4 * g + quad, cd);
       // dS^T row chunks 2g, 2g+1 -> shared memory (64-byte rows, 64B swizzle)
@@ -446,33 +500,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_ready);
-
-      // dQ^T readout: thread = channel m, queries 32 g .. 32 g + 31
-      ok = mbar_wait(&bars->dq_full, i & 1, p.err, abort, 61);
-      if (!ok) break;
-      tc_fence_after();
+      if (i > 0) stage_dq(i - 1, rq);
+    }
+    if (ok && nsteps > 0) {
       uint32_t rq[32];
-      tmem_ld32(tmem + lb + C::kColDQ + 32 * g, rq);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->dq_free);
-      // stage fp16 rows [q][d], then one tensor reduce-add into global dQ
-      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (i & 1) * kBQ * D * 2);
-      if (ctid == 0) bulk_wait_read_le1();
-      named_bar_sync(1, 256);
-      if (m < D) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          stg[(32 * g + j) * D + m] = __float2half_rn(__uint_as_float(rq[j]) * p.dq_mult);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (ctid == 0) {
-        // rows of the step beyond the sequence carry exact zeros
-        tma_reduce_add_3d(&tma_dq, 0, h, static_cast<int32_t>(w.start + q0), stg);
-        bulk_commit();
-      }
+      ok = read_dq(nsteps - 1, rq);
+      if (ok) stage_dq(nsteps - 1, rq);
     }
     if (ctid == 0) bulk_wait0();
     // epilogue: warpgroup 0 writes dK (times softmax_scale), 1 writes dV
