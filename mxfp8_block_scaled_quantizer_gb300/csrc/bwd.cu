@@ -457,15 +457,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->st_loaded);
       float pv[32], dsv[32];
       const int qb0 = q0 + 32 * g;
+      // visible queries of this key row within the block: [lo, hi)
+      const int lo = p.causal ? max(0, key - qb0) : 0;
+      const int hi = key < w.len ? min(32, w.len - qb0) : 0;
+      const bool all_visible = __all_sync(0xFFFFFFFFu, lo == 0 && hi == 32);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int qq = qb0 + j;
-        const bool masked = (key >= w.len) || (qq >= w.len) || (p.causal && key > qq);
         const float x = fmaf(__uint_as_float(rs[j]), p.scale_log2, -lse2[j]);
-        const float pj = masked ? 0.f : ex2(x);
-        pv[j] = pj;
-        dsv[j] = pj * (__uint_as_float(rd[j]) - dlt[j]);
+        pv[j] = ex2(x);
       }
+      if (!all_visible) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < lo || j >= hi) pv[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) dsv[j] = pv[j] * (__uint_as_float(rd[j]) - dlt[j]);
       uint32_t wp[8], wd[8];
       const uint32_t cp_ = quant_block32(pv, wp);
       const uint32_t cd = quant_block32(dsv, wd);
