@@ -16,26 +16,31 @@
 //   O += P V            block-scaled MMA, P read from TMEM as the A operand
 //   epilogue            O / l -> bf16, LSE = (m + log2 l) ln 2
 //
-// CTA = two 128-query tiles of one (sequence, head) sharing every K/V tile.
+// CTA = one 128-query tile of one (sequence, head); key/value tiles of 256.
 // Warp roles:
-//   warp 0     TMA producer: Q tiles once, then K_j, V_j and their scale tiles
-//              through a 3-stage shared-memory ring.
+//   warp 0     TMA producer: Q once, then K_j, V_j and their scale tiles
+//              through a shared-memory ring.
 //   warp 1     TMEM owner and MMA issuer (one thread).
-//   warps 2-5  softmax of query tile 0, warps 6-9 of tile 1 (thread = row =
-//              TMEM lane).
+//   warps 2-9  softmax: warps 2-5 take keys [0,128) of every tile, warps 6-9
+//              keys [128,256); thread = query row = TMEM lane.  The two
+//              threads of a row exchange their partial maxima (and, at the
+//              end, their partial sums) through shared memory.
+//
+// Pipeline.  S has its own 256 columns and P its own 64, so S_{j+1} = Q
+// K_{j+1}^T is issued as soon as the softmax has the row of S_j in
+// registers; while the softmax works on tile j the tensor pipe runs PV_{j-1}
+// and S_{j+1}.  The only waits on the softmax side are "S_j landed" and,
+// before P_j overwrites P_{j-1}, "PV_{j-1} done".
 //
 // TMEM budget (all 512 columns; "TMEM allocation strategies that fit scale
 // factors into the fully utilized 512-column TMEM with minimal new
 // barriers", paragraph 2 of the first page):
-//   S0 [0,128)  S1 [128,256)  O0 [256,256+D)  O1 [256+D,256+2D)
-// No column is free, so the scale factors live inside the S buffers:
-//   - P_i (fp8) overwrites S_i[0,32) once the softmax has read the row; the
-//     PV scales sit beside it: SFP_i at S_i[32,36), SFV_j at S_i[36,40).
-//   - The scales of the S_i MMA (SFQ_i, SFK_j) cannot sit in S_i, which that
-//     MMA writes; they are copied into the tail S_{1-i}[120,128) of the other
-//     tile, which is dead once that tile's softmax has read its row tail.
-//     One new barrier per tile ("S tail read") orders this; everything else
-//     reuses the S-full / P-full / PV-done barriers.
+//   S [0,256)   O [256,256+D)   P [384,448)   scale factors [448,476):
+//   SFQ 4 columns, SFK 8 (two 128-key scale tiles), SFP 8 (one 4-column
+//   group per softmax warpgroup), SFV 8.  The scale columns are rewritten by
+//   tcgen05.cp (SFK, SFV) or tcgen05.st (SFP) every tile; the MMAs that read
+//   them are ordered behind the copies by the issue order of the tensor pipe
+//   and behind the stores by the P-full barrier that the PV MMA waits on.
 #include <cuda_runtime.h>
 
 #include "lpfa_device.cuh"
@@ -45,13 +50,13 @@
 namespace lpfa {
 namespace {
 
-constexpr int kBlockM = 128;   // queries per tile (two tiles per CTA)
-constexpr int kBlockN = 128;   // keys per tile
-constexpr int kStages = 3;
-constexpr int kThreads = 320;
+constexpr int kBlockM = 128;   // queries per CTA
+constexpr int kBlockN = 256;   // keys per key/value tile
+constexpr int kHalfN = 128;    // keys per softmax warpgroup
+constexpr int kThreads = 352;
 constexpr int kTmemCols = 512;
-constexpr uint32_t kTailSFQ = 120, kTailSFK = 124;   // in the other S buffer
-constexpr uint32_t kColSFP = 32, kColSFV = 36;       // in the own S buffer
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColSFQ = 448, kColSFK = 452, kColSFP = 460, kColSFV = 468;
 
 struct FwdParams {
   SeqView seqs;
@@ -62,32 +67,39 @@ struct FwdParams {
   float* lse;           // [Hq, T]
   uint32_t* err;
   int32_t hq, hkv, group;
-  int32_t npairs;       // dense: query-tile pairs per sequence
+  int32_t nq;           // dense: query tiles per sequence
   int32_t causal;
   float scale_log2;     // softmax_scale * log2(e)
   float threshold;      // log2 units
 };
 
 template <int D>
-struct FwdSmem {
-  static constexpr int kTile = kBlockN * D;            // bytes of one fp8 tile
-  static constexpr int kQ = 0;                         // Q0, Q1
-  static constexpr int kStage0 = 2 * kBlockM * D;      // stage s: K, V
-  static constexpr int kStageBytes = 2 * kTile;
-  static constexpr int kSf0 = kStage0 + kStages * kStageBytes;  // SFQ0, SFQ1, SFK[s], SFV[s]
-  static constexpr int kBar = kSf0 + 512 * (2 + 2 * kStages);
+struct FwdCfg {
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kQBytes = kBlockM * D;
+  static constexpr int kKVBytes = kBlockN * D;            // one of K, V
+  static constexpr int kQ = 0;
+  static constexpr int kStage0 = kQBytes;                 // stage s: K, V
+  static constexpr int kStageBytes = 2 * kKVBytes;
+  static constexpr int kSfQ = kStage0 + kStages * kStageBytes;
+  static constexpr int kSfStage0 = kSfQ + 512;            // SFK[2], SFV[2]
+  static constexpr int kXMax = kSfStage0 + kStages * 2048;  // float [2][2][128]
+  static constexpr int kXSum = kXMax + 2 * 2 * 128 * 4;     // float [2][128]
+  static constexpr int kBar = kXSum + 2 * 128 * 4;
   static constexpr int kTotal = kBar + 256;
 };
 
+template <int S>
 struct FwdBars {
   uint64_t q_full;
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t s_tail[2];
-  uint64_t p_full[2];
-  uint64_t pv_done[2];
-  uint64_t drain;
+  uint64_t kv_full[S];
+  uint64_t kv_empty[S];
+  uint64_t s_full;     // S_j in TMEM (MMA commit)
+  uint64_t s_free;     // every softmax warp holds its row of S_j (8 arrivals)
+  uint64_t p_full;     // P_j, SFP_j in TMEM, O rescaled (8 arrivals)
+  uint64_t pv_done;    // PV_j complete (MMA commit)
+  uint64_t xchg[4];    // row-pair exchange, one per TMEM lane quarter (2)
+  uint64_t drain[2];   // per MMA-issuing warp
   uint32_t tmem_base;
   int abort;
 };
@@ -134,31 +146,39 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Work item of this CTA: (sequence, pair of q tiles, head); heavy causal
-// pairs first.  Returns false for CTAs without work (odd padded tiles).
+// Work item of this CTA: (sequence, q tile, head).  Items that share a key
+// head are consecutive (their K/V tiles stay in L2 while the CTAs that read
+// them run) and, for dense causal inputs, the heavy (late) q tiles of a
+// group come first.
 struct WorkItem {
-  int seq, qtile, head;   // qtile = first tile of the pair (even)
+  int seq, qtile, head;
   int64_t start;          // first token of the sequence
   int32_t len;
-  int64_t sf_tile;        // padded 128-row tile index of qtile
+  int64_t sf_tile;        // padded 128-row tile index of the q tile
 };
 
 __device__ __forceinline__ bool work_item(const FwdParams& p, WorkItem& w) {
   const int64_t idx = blockIdx.x;
-  w.head = static_cast<int>(idx % p.hq);
-  const int64_t rest = idx / p.hq;
+  const int grp = p.group;
+  int kvh;
   if (p.seqs.cu_seqlens == nullptr) {
-    const int nseq = p.seqs.nseq;
-    w.seq = static_cast<int>(rest % nseq);
-    w.qtile = 2 * (p.npairs - 1 - static_cast<int>(rest / nseq));
+    const int64_t per = static_cast<int64_t>(grp) * p.nq;
+    const int64_t g = idx / per;
+    const int r = static_cast<int>(idx % per);
+    kvh = static_cast<int>(g % p.hkv);
+    w.seq = static_cast<int>(g / p.hkv);
+    w.qtile = p.nq - 1 - r / grp;
+    w.head = kvh * grp + r % grp;
   } else {
-    // the padded tile space enumerates every (sequence, q tile); even tiles
-    // of a sequence start a pair
-    const int64_t t = rest;
+    const int64_t ntiles = p.seqs.total_sf_rows / 128;
+    const int64_t per = ntiles * grp;
+    kvh = static_cast<int>(idx / per);
+    const int64_t r = idx % per;
+    const int64_t t = r / grp;
+    w.head = kvh * grp + static_cast<int>(r % grp);
     w.seq = seq_of_sf_row(p.seqs, t * 128);
-    const SeqInfo si = seq_info(p.seqs, w.seq);
-    w.qtile = static_cast<int>((t * 128 - si.sf_start) / 128);
-    if (w.qtile & 1) return false;
+    const SeqInfo s0 = seq_info(p.seqs, w.seq);
+    w.qtile = static_cast<int>((t * 128 - s0.sf_start) / 128);
   }
   const SeqInfo si = seq_info(p.seqs, w.seq);
   w.start = si.start;
@@ -173,13 +193,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tma_k,
                        const __grid_constant__ CUtensorMap tma_v,
                        const FwdParams p) {
-  using L = FwdSmem<D>;
+  using C = FwdCfg<D>;
+  constexpr int kStages = C::kStages;
   constexpr uint32_t kSw = (D == 128) ? 2u : 4u;     // 128B / 64B swizzle
   constexpr uint32_t kSbo = 8 * D;                    // 8 rows of D bytes
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  FwdBars* bars = reinterpret_cast<FwdBars*>(sm + L::kBar);
+  FwdBars<kStages>* bars = reinterpret_cast<FwdBars<kStages>*>(sm + C::kBar);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -187,16 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   WorkItem w;
   if (!work_item(p, w)) return;                    // uniform for the CTA
   const int kvh = w.head / p.group;
-  const int q0 = w.qtile * kBlockM;                // first query of tile 0
-  // key tiles per query tile (0 when the tile lies beyond the sequence)
-  auto ntiles_of = [&](int i) {
-    const int qi0 = q0 + i * kBlockM;
-    const int kv_len = p.causal ? min(w.len, qi0 + kBlockM) : w.len;
-    return qi0 < w.len ? (kv_len + kBlockN - 1) / kBlockN : 0;
-  };
-  const int nt0 = ntiles_of(0), nt1 = ntiles_of(1);
-  auto nt = [nt0, nt1](int i) { return i == 0 ? nt0 : nt1; };
-  const int nmax = max(nt0, nt1);
+  const int q0 = w.qtile * kBlockM;                // first query of the tile
+  const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
+  const int ntiles = (kv_len + kBlockN - 1) / kBlockN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
@@ -204,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_tail[b], 4);
-      mbar_init(&bars->p_full[b], 4);
-      mbar_init(&bars->pv_done[b], 1);
-    }
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 8);
+    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->pv_done, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->xchg[q], 2);
+    mbar_init(&bars->drain[0], 1);
+    mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
     fence_barrier_init();
   }
@@ -222,154 +236,171 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // S_i at column 128 i, O_i at column 256 + D i (computed, not indexed, so
-  // that no per-thread array lands in local memory)
-  auto tS = [tmem](int i) { return tmem + 128u * static_cast<uint32_t>(i); };
-  auto tO = [tmem](int i) { return tmem + 256u + static_cast<uint32_t>(D * i); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop (converged); an elected lane issues the
+    // copies.
     if (lane == 0) {
       tma_prefetch_desc(&tma_q);
       tma_prefetch_desc(&tma_k);
       tma_prefetch_desc(&tma_v);
-      const int32_t row_q = static_cast<int32_t>(w.start + q0);
-      mbar_arrive_expect_tx(&bars->q_full, 2 * kBlockM * D + 1024);
-      tma_load_3d(sm + L::kQ, &tma_q, 0, w.head, row_q, &bars->q_full);
-      tma_load_3d(sm + L::kQ + kBlockM * D, &tma_q, 0, w.head, row_q + kBlockM, &bars->q_full);
-      // the second tile's scale tile exists in the padded space whenever the
-      // first does (a sequence's padded rows cover whole 128-row tiles); for
-      // a missing second tile it is the next sequence's, and unused
-      const int64_t sfq_last = p.seqs.total_sf_rows / 128 - 1;
-      const int64_t sft1 = w.sf_tile + 1 <= sfq_last ? w.sf_tile + 1 : w.sf_tile;
-      bulk_load(sm + L::kSf0, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512, &bars->q_full);
-      bulk_load(sm + L::kSf0 + 512, p.sfq + (sft1 * p.hq + w.head) * 512, 512, &bars->q_full);
-      const int64_t kv_sf_tile0 = w.sf_tile - w.qtile;   // first tile of sequence
-      bool ok = true;
-      int issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = -1;
-      for (int j = 0; j < nmax; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        ok = mbar_wait(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
-        if (!ok) break;
-        uint8_t* kbuf = sm + L::kStage0 + s * L::kStageBytes;
-        uint64_t* bar = &bars->kv_full[s];
-        mbar_arrive_expect_tx(bar, 2 * L::kTile + 1024);
-        const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
-        tma_load_3d(kbuf, &tma_k, 0, kvh, row_k, bar);
-        tma_load_3d(kbuf + L::kTile, &tma_v, 0, kvh, row_k, bar);
-        const int64_t sft = (kv_sf_tile0 + j) * p.hkv + kvh;
-        bulk_load(sm + L::kSf0 + 512 * (2 + s), p.sfk + sft * 512, 512, bar);
-        bulk_load(sm + L::kSf0 + 512 * (2 + kStages + s), p.sfv + sft * 512, 512, bar);
-        issued[s] = static_cast<int>(ph);
-      }
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s] >= 0)
-            mbar_wait(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
-        mbar_wait(&bars->q_full, 0, nullptr, nullptr, 0);
-      }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
-      const uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
-      bool ok = mbar_wait(&bars->q_full, 0, p.err, abort, 20);
-      if (ok) tc_fence_after();
-      // S_i,j = Q_i K_j^T; its scales go to the tail of the other S buffer
-      auto issue_s = [&](int i, int j) -> bool {
-        const int s = j % kStages;
-        const int o = 1 - i;
-        // the other tile's softmax must have read its row tail (its S MMA of
-        // this key tile for o = 1, of the previous one for o = 0 ... any
-        // earlier S of tile o still being read)
-        const int jo = (o == 0) ? j : j - 1;      // last S of tile o issued
-        if (jo >= 0 && jo < nt(o)) {
-          if (!mbar_wait(&bars->s_tail[o], jo & 1, p.err, abort, 23)) return false;
-          tc_fence_after();
-        }
-        const uint32_t sf_t = tS(o) + kTailSFQ;
-        tc_cp_32x128b_warpx4(sf_t, sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * i)));
-        tc_cp_32x128b_warpx4(tS(o) + kTailSFK,
-                             sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (2 + s))));
-        const uint32_t q_addr = smem_u32(sm + L::kQ + i * kBlockM * D);
-        const uint32_t k_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes);
+    mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
+    tma_load_3d_elect(sm + C::kQ, &tma_q, 0, w.head, static_cast<int32_t>(w.start + q0),
+                   &bars->q_full);
+    bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
+                 &bars->q_full);
+    // scale tiles of keys past the sequence's padded rows belong to the
+    // next sequence (finite, and their keys are masked); past the tensor
+    // the last tile stands in
+    const int64_t kv_sf0 = w.sf_tile - w.qtile;
+    const int64_t sf_last = p.seqs.total_sf_rows / 128 - 1;
+    bool ok = true;
+    int issued[kStages];
+    for (int s = 0; s < kStages; ++s) issued[s] = -1;
+    for (int j = 0; j < ntiles; ++j) {
+      const int s = j % kStages;
+      const uint32_t ph = (j / kStages) & 1;
+      ok = mbar_wait_sleep(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
+      if (!ok) break;
+      uint8_t* kbuf = sm + C::kStage0 + s * C::kStageBytes;
+      uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
+      uint64_t* bar = &bars->kv_full[s];
+      mbar_arrive_expect_tx_elect(bar, 2 * C::kKVBytes + 2048);
+      const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
+      tma_load_3d_elect(kbuf, &tma_k, 0, kvh, row_k, bar);
+      tma_load_3d_elect(kbuf + C::kKVBytes, &tma_v, 0, kvh, row_k, bar);
 #pragma unroll
-        for (int kb = 0; kb < D / 32; ++kb) {
-          mma_mxf8_ss(tS(i), make_sdesc(q_addr + 32 * kb, 16, kSbo, kSw),
-                      make_sdesc(k_addr + 32 * kb, 16, kSbo, kSw),
-                      idesc_sf_ids(idesc_s, kb, kb), sf_t, tS(o) + kTailSFK, kb > 0);
-        }
-        tc_commit(&bars->s_full[i]);
+      for (int h = 0; h < 2; ++h) {
+        const int64_t t = min(kv_sf0 + 2 * j + h, sf_last);
+        const int64_t off = (t * p.hkv + kvh) * 512;
+        bulk_load_elect(sfb + 512 * h, p.sfk + off, 512, bar);
+        bulk_load_elect(sfb + 1024 + 512 * h, p.sfv + off, 512, bar);
+      }
+      issued[s] = static_cast<int>(ph);
+    }
+    if (!ok) {
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] >= 0)
+          mbar_wait_sleep(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+      mbar_wait_sleep(&bars->q_full, 0, nullptr, nullptr, 0);
+    }
+  } else if (warp == 1 || warp == 10) {
+    // --------------------------------------------------------- MMA issuers
+    // A warp issues at most one tcgen05 instruction every ~60-90 cycles, and
+    // one tile needs 12 MMAs, 4 scale copies and 2 commits: more than a
+    // single warp can issue in the ~1000 cycles the tensor pipe takes to run
+    // them.  Warp 1 issues S = Q K^T, warp 10 (another scheduler) issues
+    // O += P V; the two write disjoint TMEM columns (S | O, SFQ SFK | SFP
+    // SFV), so their instructions need no mutual order.  Each warp runs its
+    // loop converged and an elected lane issues.  Descriptors of stage 0 are built
+    // once; a stage adds its byte offset / 16 and a K-step 32 bytes (S
+    // operands) or 32 rows of V to the 14-bit address field, which never
+    // carries (shared memory addresses stay below 256 KB).  The key loop is
+    // unrolled by the ring depth so that stage indices are constants.
+    const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSfStage0));
+    bool ok = true;
+    if (warp == 1) {
+      constexpr uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
+      const uint64_t dq = make_sdesc(smem_u32(sm + C::kQ), 16, kSbo, kSw);
+      const uint64_t dk = make_sdesc(smem_u32(sm + C::kStage0), 16, kSbo, kSw);
+      const uint32_t tS = tmem + kColS, tSFQ = tmem + kColSFQ, tSFK = tmem + kColSFK;
+      ok = mbar_wait_sleep(&bars->q_full, 0, p.err, abort, 20);
+      if (ok) {
+        tc_fence_after();
+        tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
+      }
+      // S = Q K_j^T (N = 256: two 128-key scale tiles side by side); S_j
+      // may be overwritten once every softmax warp holds its row of S_{j-1}
+      auto issue_s = [&](int j, int s) -> bool {
+        if (j > 0 && !mbar_wait_sleep(&bars->s_free, (j - 1) & 1, p.err, abort, 23)) return false;
+        if (!mbar_wait_sleep(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21)) return false;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+        const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
+        tc_cp_32x128b_warpx4_elect(tSFK, dsf + fo);
+        tc_cp_32x128b_warpx4_elect(tSFK + 4, dsf + fo + (512 >> 4));
+#pragma unroll
+        for (int kb = 0; kb < D / 32; ++kb)
+          mma_mxf8_ss_elect(tS, dq + 2 * kb, dk + so + 2 * kb,
+                         idesc_sf_ids(idesc_s, kb, kb), tSFQ, tSFK, kb > 0);
+        tc_commit_elect(&bars->s_full);
         return true;
       };
-      // O_i += P_i,j V_j; the last reader of stage j%kStages releases it
-      auto issue_pv = [&](int i, int j, bool release) -> bool {
-        const int s = j % kStages;
-        if (!mbar_wait(&bars->p_full[i], j & 1, p.err, abort, 22)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sm + L::kStage0 + s * L::kStageBytes + L::kTile);
-        tc_cp_32x128b_warpx4(tS(i) + kColSFV,
-                             sf_tile_desc(smem_u32(sm + L::kSf0 + 512 * (2 + kStages + s))));
+      for (int j0 = 0; j0 < ntiles && ok; j0 += kStages) {
 #pragma unroll
-        for (int kb = 0; kb < kBlockN / 32; ++kb) {
-          mma_mxf8_ts(tO(i), tS(i) + 8 * kb, make_sdesc(v_addr + 32 * D * kb, 16, kSbo, kSw),
-                      idesc_sf_ids(idesc_o, kb, kb), tS(i) + kColSFP, tS(i) + kColSFV,
-                      (j > 0) || (kb > 0));
+        for (int ss = 0; ss < kStages; ++ss) {
+          const int j = j0 + ss;                   // j % kStages == ss
+          if (ok && j < ntiles) ok = issue_s(j, ss);
         }
-        tc_commit(&bars->pv_done[i]);
-        if (release) tc_commit(&bars->kv_empty[s]);
+      }
+    } else {
+      constexpr uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
+      const uint64_t dv = make_sdesc(smem_u32(sm + C::kStage0 + C::kKVBytes), 16, kSbo, kSw);
+      const uint32_t tO = tmem + kColO, tP = tmem + kColP;
+      const uint32_t tSFP = tmem + kColSFP, tSFV = tmem + kColSFV;
+      // O += P_j V_j over 256 keys (8 K-steps; scale group = K-step / 4);
+      // V_j landed before S_j could be computed, and P_j is written after
+      // the softmax saw S_j, so P-full orders both
+      auto issue_pv = [&](int j, int s) -> bool {
+        if (!mbar_wait_sleep(&bars->p_full, j & 1, p.err, abort, 22)) return false;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+        const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
+        tc_cp_32x128b_warpx4_elect(tSFV, dsf + fo + (1024 >> 4));
+        tc_cp_32x128b_warpx4_elect(tSFV + 4, dsf + fo + (1536 >> 4));
+#pragma unroll
+        for (int kb = 0; kb < kBlockN / 32; ++kb)
+          mma_mxf8_ts_elect(tO, tP + 8 * kb, dv + so + kb * ((32 * D) >> 4),
+                         idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
+                         tSFV + 4 * (kb >> 2), (j > 0) || (kb > 0));
+        tc_commit_elect(&bars->pv_done);
         return true;
       };
-      const bool has1 = nt(1) > 0;
-      for (int j = 0; j < nmax && ok; ++j) {
-        const int s = j % kStages;
-        ok = mbar_wait(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21);
-        if (!ok) break;
-        tc_fence_after();
-        if (j < nt(0)) ok = issue_s(0, j);
-        if (ok && j >= 1 && j - 1 < nt(1)) ok = issue_pv(1, j - 1, true);
-        if (ok && j < nt(1)) ok = issue_s(1, j);
-        if (ok && j < nt(0)) ok = issue_pv(0, j, !has1);
+      for (int j0 = 0; j0 < ntiles && ok; j0 += kStages) {
+#pragma unroll
+        for (int ss = 0; ss < kStages; ++ss) {
+          const int j = j0 + ss;
+          if (ok && j < ntiles) ok = issue_pv(j, ss);
+        }
       }
-      if (ok && has1) ok = issue_pv(1, nmax - 1, true);
-      if (!ok) *abort = 1;
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, nullptr, nullptr, 0);
     }
+    if (!ok) *abort = 1;
+    uint64_t* dr = &bars->drain[warp == 1 ? 0 : 1];
+    tc_commit_elect(dr);
+    mbar_wait_sleep(dr, 0, nullptr, nullptr, 0);
   } else {
     // ------------------------------------------------------------- softmax
-    const int ti = (warp - 2) >> 2;               // query tile of this warpgroup
+    const int wg = (warp - 2) >> 2;               // key half of every tile
     const int quad = warp & 3;                    // TMEM lane quarter
     const int row = quad * 32 + lane;             // query row within tile
-    const int qt0 = q0 + ti * kBlockM;            // first query of the tile
-    const int qi = qt0 + row;                     // query index in sequence
-    const int ntl = nt(ti);
+    const int qi = q0 + row;                      // query index in sequence
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tSi = tS(ti) + lane_base;
+    const uint32_t tSrow = tmem + kColS + kHalfN * wg + lane_base;
+    float* xmax = reinterpret_cast<float*>(sm + C::kXMax);   // [2][2][128]
+    float* xsum = reinterpret_cast<float*>(sm + C::kXSum);   // [2][128]
+    uint64_t* xbar = &bars->xchg[quad];
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = pack2(c2, c2);
     float m_ref = -INFINITY;                      // log2 units
-    float l = 0.f;
+    float l = 0.f;                                // this half's partial sum
     bool ok = true;
     const int lim = p.causal ? min(w.len, qi + 1) : w.len;   // keys < lim visible
-    for (int j = 0; j < ntl && ok; ++j) {
-      ok = mbar_wait(&bars->s_full[ti], j & 1, p.err, abort, 30);
+    int j = 0;
+    for (; j < ntiles && ok; ++j) {
+      ok = mbar_wait_sleep(&bars->s_full, j & 1, p.err, abort, 30);
       if (!ok) break;
       tc_fence_after();
-      const int k0 = j * kBlockN;
-      const bool need_mask = (k0 + kBlockN > w.len) || (p.causal && k0 + kBlockN - 1 > qt0);
-      // the whole 128-column row in one round trip; once it is in registers
-      // the other tile's S MMA may park its scale factors in the row tail
       uint32_t sv[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tSi + 32 * c, sv[c]);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tSrow + 32 * c, sv[c]);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_tail[ti]);
+      if (lane == 0) mbar_arrive(&bars->s_free);
+      const int k0 = j * kBlockN + wg * kHalfN;
+      const bool need_mask = (k0 + kHalfN > w.len) || (p.causal && k0 + kHalfN - 1 > q0);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -387,7 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           a = max3(a, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
         cmax[c] = fmaxf(a, __uint_as_float(sv[c][31]));
       }
-      const float tmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+      // row maximum over both halves
+      const float hmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+      float* xm = xmax + (j & 1) * 256;
+      xm[wg * 128 + row] = hmax;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      ok = mbar_wait_sleep(xbar, j & 1, p.err, abort, 33);
+      if (!ok) break;
+      const float tmax = fmaxf(hmax, xm[(1 - wg) * 128 + row]);
       const float mt = __fmul_rn(tmax, c2);
       float m_new = m_ref;
       if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
@@ -407,15 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the scaled values per block and rescales by 2^e
       uint32_t pw[32];
       float lsum = 0.f;
-      auto do_chunk = [&](int c, const uint32_t (&v)[32]) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
         const int e = static_cast<int>(code[c]) - 127;
         const float nb = -(m_use + static_cast<float>(e));
         const uint64_t nb2 = pack2(nb, nb);
         uint64_t acc = 0;
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
-          const uint64_t x0 = fma2(pack2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c2x2, nb2);
-          const uint64_t x1 = fma2(pack2(__uint_as_float(v[2 * k + 2]), __uint_as_float(v[2 * k + 3])), c2x2, nb2);
+          const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][2 * k]), __uint_as_float(sv[c][2 * k + 1])), c2x2, nb2);
+          const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][2 * k + 2]), __uint_as_float(sv[c][2 * k + 3])), c2x2, nb2);
           const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
           const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
           acc = add2(acc, pack2(p0, p1));
@@ -426,49 +466,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         // blocks hold only zeros)
         const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
         lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
-      };
-#pragma unroll
-      for (int c = 0; c < 4; ++c) do_chunk(c, sv[c]);
-      // P and its scales into TMEM: P over S_i[0,32), SFP at S_i[32 + r/32]
-      tmem_st32(tSi, pw);
-      tmem_st1(tSi + kColSFP + quad, sfp);
-      tmem_st_wait();
-      // selective rescale of O_i (and l): only warps holding a moved row
-      if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
-        ok = mbar_wait(&bars->pv_done[ti], (j - 1) & 1, p.err, abort, 31);
+      }
+      // P_{j-1} must be consumed before P_j overwrites it (and O is stable
+      // only between PV_{j-1} and PV_j)
+      if (j > 0) {
+        ok = mbar_wait_sleep(&bars->pv_done, (j - 1) & 1, p.err, abort, 31);
         if (!ok) break;
         tc_fence_after();
+        // S_{j-1} and PV_{j-1} are done: their K/V stage may be refilled
+        if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(j - 1) % kStages]);
+      }
+      tmem_st32(tmem + kColP + 32 * wg + lane_base, pw);
+      tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
+      // selective rescale of O (and l): only warps holding a moved row; each
+      // half rescales half of the columns
+      if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
         uint32_t r[32];
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          const uint32_t ta = tO(ti) + lane_base + 32 * c;
+        for (int c = 0; c < D / 64; ++c) {
+          const uint32_t ta = tmem + kColO + (D / 2) * wg + 32 * c + lane_base;
           tmem_ld32(ta, r);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
           tmem_st32(ta, r);
         }
-        tmem_st_wait();
       }
+      tmem_st_wait();
       l = l * alpha + lsum;
       m_ref = m_new;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[ti]);
+      if (lane == 0) mbar_arrive(&bars->p_full);
     }
-    // epilogue: O / l -> bf16, LSE
-    if (ok && ntl > 0) {
-      ok = mbar_wait(&bars->pv_done[ti], (ntl - 1) & 1, p.err, abort, 32);
+    // epilogue: O / l -> bf16 (each half writes half of the columns), LSE
+    if (ok && ntiles > 0) {
+      xsum[wg * 128 + row] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      ok = mbar_wait_sleep(xbar, ntiles & 1, p.err, abort, 34);
+      if (ok) ok = mbar_wait_sleep(&bars->pv_done, (ntiles - 1) & 1, p.err, abort, 32);
       if (ok) {
         tc_fence_after();
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const float lt = l + xsum[(1 - wg) * 128 + row];
+        const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
         const bool valid = qi < w.len;
         const int64_t tok = w.start + qi;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D);
+        uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D + (D / 2) * wg);
         uint32_t r[32];
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          tmem_ld32(tO(ti) + lane_base + 32 * c, r);
+        for (int c = 0; c < D / 64; ++c) {
+          tmem_ld32(tmem + kColO + (D / 2) * wg + 32 * c + lane_base, r);
           tmem_ld_wait();
           if (valid) {
 #pragma unroll
@@ -485,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (valid) {
-          const float lse2 = m_ref + __log2f(l);
+        if (valid && wg == 0) {
+          const float lse2 = m_ref + __log2f(lt);
           p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
               lse2 * 0.69314718055994531f;
         }
@@ -510,19 +558,19 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   const CUtensorMapSwizzle sw =
       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk, tv;
-  auto make = [&](CUtensorMap* m, const void* base, int64_t heads) {
+  auto make = [&](CUtensorMap* m, const void* base, int64_t heads, uint32_t rows) {
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
                         static_cast<uint64_t>(sv.total_tokens)};
     uint64_t strides[2] = {static_cast<uint64_t>(D),
                            static_cast<uint64_t>(heads * D)};
-    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, 128u};
+    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, rows};
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides,
                        box, sw);
   };
   lpfa_status st;
-  if ((st = make(&tq, q8, desc->heads_q)) != LPFA_OK) return st;
-  if ((st = make(&tk, k8, desc->heads_kv)) != LPFA_OK) return st;
-  if ((st = make(&tv, v8, desc->heads_kv)) != LPFA_OK) return st;
+  if ((st = make(&tq, q8, desc->heads_q, kBlockM)) != LPFA_OK) return st;
+  if ((st = make(&tk, k8, desc->heads_kv, kBlockN)) != LPFA_OK) return st;
+  if ((st = make(&tv, v8, desc->heads_kv, kBlockN)) != LPFA_OK) return st;
 
   FwdParams p;
   p.seqs = sv;
@@ -535,17 +583,17 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   p.hq = static_cast<int32_t>(desc->heads_q);
   p.hkv = static_cast<int32_t>(desc->heads_kv);
   p.group = p.hq / p.hkv;
-  p.npairs = static_cast<int32_t>(ceil_div(ceil_div(sv.seqlen, kBlockM), 2));
+  p.nq = static_cast<int32_t>(ceil_div(sv.seqlen, kBlockM));
   p.causal = desc->causal ? 1 : 0;
   p.scale_log2 = desc->softmax_scale * 1.4426950408889634f;
   p.threshold = desc->rescale_threshold;
 
   const int64_t units = sv.cu_seqlens == nullptr
-                            ? static_cast<int64_t>(sv.nseq) * p.npairs
+                            ? static_cast<int64_t>(sv.nseq) * p.nq
                             : sv.total_sf_rows / 128;
   const int64_t nblocks = units * p.hq;
   LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
-  const size_t smem = FwdSmem<D>::kTotal + 1024;
+  const size_t smem = FwdCfg<D>::kTotal + 1024;
   static bool attr = false;
   if (!attr) {
     LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_fwd_kernel<D>,

@@ -74,6 +74,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// (up to `hint_ns`, or until the phase completes) instead of returning at
+// once, so that a waiting warp does not take issue slots from the warps that
+// share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wall-clock bound of every wait.  A correct pipeline never waits longer
 // than microseconds; the bound only turns a logic error into a reported
 // error instead of a hung GPU.
@@ -95,6 +112,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         report_error(err, ERR_WAIT_TIMEOUT, site);
         return false;
       }
+    }
+  }
+}
+
+
+// mbar_wait for roles that wait long and share a scheduler with compute
+// warps (producers, MMA issuers, waiting consumers): the same contract, with
+// the polling thread suspended between tests.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                uint32_t* err, volatile int* abort,
+                                                uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (abort != nullptr) *abort = 1;
+      report_error(err, ERR_WAIT_TIMEOUT, site);
+      return false;
     }
   }
 }
@@ -216,6 +253,86 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- single-thread instructions issued from a converged warp: every lane
+// of the warp makes the call and the lane that elect.sync picks issues the
+// instruction.  The elected-lane predicate costs far fewer issue cycles per
+// tcgen05 instruction than a branch on the lane index or a predicate derived
+// from one (measured on sm_103a: ~39 cycles per MMA against ~62 and ~86),
+// and keeps the warp converged.
+#define LPFA_ELECT "elect.sync _|e, 0xffffffff;\n\t"
+
+__device__ __forceinline__ void tc_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::
+          "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_32x128b_warpx4_elect(uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t" LPFA_ELECT
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t" LPFA_ELECT
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_elect(void* smem_dst, const void* tmap, int32_t x,
+                                                  int32_t y, int32_t z, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_elect(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                                uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 

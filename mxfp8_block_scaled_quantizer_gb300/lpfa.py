@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 LPFA_OK, LPFA_ERR_INVALID_ARG, LPFA_ERR_UNSUPPORTED, LPFA_ERR_CUDA, \
     LPFA_ERR_TIMEOUT = range(5)
 LPFA_BLK_1X32, LPFA_BLK_32X1, LPFA_BLK_32X32 = range(3)
+from . import FWD_KV_TILE  # noqa: E402  (key tile of the forward softmax)
 
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64
