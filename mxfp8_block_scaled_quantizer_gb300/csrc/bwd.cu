@@ -19,7 +19,7 @@
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-9
 // compute in two warpgroups, each owning 32 of the step's 64 queries (thread
 // = key row for S^T/dP^T, = head_dim channel for dQ^T).  dQ partials leave
-// as one tensor reduce-add (FP16) of the 64x128 step tile.
+// as FP16 tensor reduce-adds, one per warp (32 queries x 32 channels).
 //
 // TMEM (512 columns):
 //   [  0,128) dK      [128,256) dV      [256,320) S^T      [320,384) dP^T
@@ -81,8 +81,9 @@ struct BwdCfg {
   static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes; // 128 x 64 B (SW64)
   static constexpr int kSmSFdS = kSmDS + kBN * kBQ;               // 512 B
   static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
-  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;  // 2 x [64][D] fp16
-  static constexpr int kSmBar = kSmDQ + 2 * kBQ * D * 2;
+  // dQ staging: per compute warp two [32 queries][32 channels] fp16 tiles
+  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
+  static constexpr int kSmBar = kSmDQ + 8 * 2 * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
 };
 
@@ -230,152 +231,156 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop (converged); an elected lane issues the
+    // copies.
     if (lane == 0) {
       tma_prefetch_desc(&tma_q);
       tma_prefetch_desc(&tma_k);
       tma_prefetch_desc(&tma_v);
       tma_prefetch_desc(&tma_do);
       tma_prefetch_desc(&tma_dq);
-      const int32_t row_k = static_cast<int32_t>(w.start + k0);
-      const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
-      mbar_arrive_expect_tx(&bars->kv_full, 2 * kBN * D + 3 * 512);
-      tma_load_3d(sm + C::kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
-      tma_load_3d(sm + C::kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
-      bulk_load(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
-      bulk_load(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
-      bulk_load(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
-      bool ok = true;
-      int issued[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = -1;
-      for (int i = 0; i < nsteps; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (i / kStages) & 1;
-        ok = mbar_wait(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
-        if (!ok) break;
-        const int h = step_head(i), q0 = step_q0(i);
-        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-        uint64_t* bar = &bars->q_full[s];
-        mbar_arrive_expect_tx(bar, 2 * kBQ * D + 4 * 512 + 2 * kBQ * 4);
-        const int32_t row_q = static_cast<int32_t>(w.start + q0);
-        tma_load_3d(st + C::kStQ, &tma_q, 0, h, row_q, bar);
-        tma_load_3d(st + C::kStdO, &tma_do, 0, h, row_q, bar);
-        const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
-        const int64_t qsf = (pr / 128) * p.hq + h;
-        bulk_load(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
-        bulk_load(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
-        bulk_load(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
-        bulk_load(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
-        const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
-        bulk_load(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, bar);
-        bulk_load(st + C::kStDelta, p.delta + rowoff, kBQ * 4, bar);
-        issued[s] = static_cast<int>(ph);
-      }
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s] >= 0)
-            mbar_wait(&bars->q_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
-        mbar_wait(&bars->kv_full, 0, nullptr, nullptr, 0);
-      }
+    }
+    const int32_t row_k = static_cast<int32_t>(w.start + k0);
+    const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
+    mbar_arrive_expect_tx_elect(&bars->kv_full, 2 * kBN * D + 3 * 512);
+    tma_load_3d_elect(sm + C::kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
+    tma_load_3d_elect(sm + C::kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
+    bulk_load_elect(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
+    bulk_load_elect(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
+    bulk_load_elect(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+    bool ok = true;
+    int issued[kStages];
+    for (int s = 0; s < kStages; ++s) issued[s] = -1;
+    for (int i = 0; i < nsteps; ++i) {
+      const int s = i % kStages;
+      const uint32_t ph = (i / kStages) & 1;
+      ok = mbar_wait_sleep(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
+      if (!ok) break;
+      const int h = step_head(i), q0 = step_q0(i);
+      uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
+      uint64_t* bar = &bars->q_full[s];
+      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * D + 4 * 512 + 2 * kBQ * 4);
+      const int32_t row_q = static_cast<int32_t>(w.start + q0);
+      tma_load_3d_elect(st + C::kStQ, &tma_q, 0, h, row_q, bar);
+      tma_load_3d_elect(st + C::kStdO, &tma_do, 0, h, row_q, bar);
+      const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
+      const int64_t qsf = (pr / 128) * p.hq + h;
+      bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
+      bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
+      bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
+      bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+      const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
+      bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, bar);
+      bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, bar);
+      issued[s] = static_cast<int>(ph);
+    }
+    if (!ok) {
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s] >= 0)
+          mbar_wait_sleep(&bars->q_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+      mbar_wait_sleep(&bars->kv_full, 0, nullptr, nullptr, 0);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t id_st = idesc_mxf8(128, kBQ, 0, 0);     // S^T, dP^T
-      const uint32_t id_acc = idesc_mxf8(128, D, 0, 1);     // dV, dK (B MN-major)
-      const uint32_t id_dq = idesc_mxf8(128, kBQ, 1, 1);     // dQ^T (A, B MN-major)
-      const uint32_t k_addr = smem_u32(sm + C::kSmK);
-      const uint32_t v_addr = smem_u32(sm + C::kSmV);
-      const uint32_t ds_addr = smem_u32(sm + C::kSmDS);
-      const uint32_t kt_addr = D == 128 ? k_addr : smem_u32(sm + C::kSmKT);
-      bool ok = mbar_wait(&bars->kv_full, 0, p.err, abort, 50);
-      if (ok) {
-        tc_fence_after();
-        tc_cp_32x128b_warpx4(tmem + C::kColSFK, sf_tile_desc(smem_u32(sm + C::kSmSFkv)));
-        tc_cp_32x128b_warpx4(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
-        tc_cp_32x128b_warpx4(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
-      }
-      // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T (contraction over head_dim)
-      auto issue_st = [&](int i) -> bool {
-        const int s = i % kStages;
-        if (!mbar_wait(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51)) return false;
-        tc_fence_after();
-        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-        const uint32_t q_addr = smem_u32(st + C::kStQ);
-        const uint32_t do_addr = smem_u32(st + C::kStdO);
-        const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
-        tc_cp_32x128b_warpx4(tmem + C::kColSFQ, sf_tile_desc(smem_u32(st + C::kStSF)));
-        tc_cp_32x128b_warpx4(tmem + C::kColSFdO, sf_tile_desc(smem_u32(st + C::kStSF + 1024)));
-#pragma unroll
-        for (int kb = 0; kb < D / 32; ++kb) {
-          mma_mxf8_ss(tmem + C::kColS, make_sdesc(k_addr + 32 * kb, 16, C::kSbo, C::kSw),
-                      make_sdesc(q_addr + 32 * kb, 16, C::kSbo, C::kSw),
-                      idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
-                      tmem + C::kColSFQ + 2 * half, kb > 0);
-        }
-#pragma unroll
-        for (int kb = 0; kb < D / 32; ++kb) {
-          mma_mxf8_ss(tmem + C::kColDP, make_sdesc(v_addr + 32 * kb, 16, C::kSbo, C::kSw),
-                      make_sdesc(do_addr + 32 * kb, 16, C::kSbo, C::kSw),
-                      idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
-                      tmem + C::kColSFdO + 2 * half, kb > 0);
-        }
-        tc_commit(&bars->st_ready);
-        return true;
-      };
-      // dV += P^T dO_i, dK += dS^T Q_i, then dQ^T(i) = K^T dS^T over the
-      // same columns the fp8 P^T / dS^T came from (MMAs execute in order)
-      auto issue_acc = [&](int i) -> bool {
-        const int s = i % kStages;
-        if (!mbar_wait(&bars->ds_ready, i & 1, p.err, abort, 52)) return false;
-        tc_fence_after();
-        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-        const uint32_t q_addr = smem_u32(st + C::kStQ);
-        const uint32_t do_addr = smem_u32(st + C::kStdO);
-        const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
-        tc_cp_32x128b_warpx4(tmem + C::kColSFQt, sf_tile_desc(smem_u32(st + C::kStSF + 512)));
-        tc_cp_32x128b_warpx4(tmem + C::kColSFdOt, sf_tile_desc(smem_u32(st + C::kStSF + 1536)));
-        tc_cp_32x128b_warpx4(tmem + C::kColSFdSB, sf_tile_desc(smem_u32(sm + C::kSmSFdS)));
-#pragma unroll
-        for (int kb = 0; kb < kBQ / 32; ++kb) {
-          const uint32_t sfb = kb + 2 * half;
-          mma_mxf8_ts(tmem + C::kColDV, tmem + C::kColDQ + 32 * kb,
-                      make_sdesc(do_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
-                      idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFP + 4 * kb,
-                      tmem + C::kColSFdOt, (i > 0) || (kb > 0));
-          mma_mxf8_ts(tmem + C::kColDK, tmem + C::kColDQ + 32 * kb + 8,
-                      make_sdesc(q_addr + 32 * D * kb, 16, C::kSbo, C::kSw),
-                      idesc_sf_ids(id_acc, 0, sfb), tmem + C::kColSFdS + 4 * kb,
-                      tmem + C::kColSFQt, (i > 0) || (kb > 0));
-        }
-        if (D != 128 && i == 0) {
-          if (!mbar_wait(&bars->kt_ready, 0, p.err, abort, 54)) return false;
-        }
-#pragma unroll
-        for (int kb = 0; kb < kBN / 32; ++kb) {
-          mma_mxf8_ss(tmem + C::kColDQ, make_sdesc(kt_addr + 32 * 128 * kb, 16, 1024, 2),
-                      make_sdesc(ds_addr + 32 * kBQ * kb, 16, 8 * kBQ, 4),
-                      idesc_sf_ids(id_dq, kb, kb), tmem + C::kColSFKt,
-                      tmem + C::kColSFdSB, kb > 0);
-        }
-        tc_commit(&bars->q_empty[s]);
-        tc_commit(&bars->dq_full);
-        return true;
-      };
-      if (ok) ok = issue_st(0);
-      for (int i = 0; i < nsteps && ok; ++i) {
-        // the next step's S^T / dP^T run while step i is in the compute warps
-        if (i + 1 < nsteps) {
-          ok = mbar_wait(&bars->st_loaded, i & 1, p.err, abort, 53);
-          if (ok) ok = issue_st(i + 1);
-          if (!ok) break;
-        }
-        ok = issue_acc(i);
-      }
-      if (ok) tc_commit(&bars->acc_done);
-      if (!ok) *abort = 1;
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, nullptr, nullptr, 0);
+    // The whole warp runs the loop (converged); the lane elect.sync picks
+    // issues each tcgen05 instruction (the cheapest issue form).  Shared
+    // memory descriptors are built once and offset by constants: a stage
+    // adds its byte offset / 16, a K-step 32 bytes (K-major operands) or 32
+    // rows (MN-major operands) to the 14-bit address field, which never
+    // carries (shared memory addresses stay below 256 KB).  The step loop is
+    // unrolled by the ring depth so that stage indices are constants.
+    constexpr uint32_t id_st = idesc_mxf8(128, kBQ, 0, 0);     // S^T, dP^T
+    constexpr uint32_t id_acc = idesc_mxf8(128, D, 0, 1);     // dV, dK (B MN-major)
+    constexpr uint32_t id_dq = idesc_mxf8(128, kBQ, 1, 1);     // dQ^T (A, B MN-major)
+    const uint64_t dk_ = make_sdesc(smem_u32(sm + C::kSmK), 16, C::kSbo, C::kSw);
+    const uint64_t dv_ = make_sdesc(smem_u32(sm + C::kSmV), 16, C::kSbo, C::kSw);
+    const uint64_t dkt = make_sdesc(D == 128 ? smem_u32(sm + C::kSmK) : smem_u32(sm + C::kSmKT),
+                                    16, 1024, 2);
+    const uint64_t dds = make_sdesc(smem_u32(sm + C::kSmDS), 16, 8 * kBQ, 4);
+    const uint64_t dq_ = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStQ), 16, C::kSbo, C::kSw);
+    const uint64_t ddo = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStdO), 16, C::kSbo, C::kSw);
+    const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSmStage0 + C::kStSF));
+    const uint64_t dsfds = sf_tile_desc(smem_u32(sm + C::kSmSFdS));
+    bool ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 50);
+    if (ok) {
+      tc_fence_after();
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFK, sf_tile_desc(smem_u32(sm + C::kSmSFkv)));
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
     }
+    // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T (contraction over head_dim)
+    auto issue_st = [&](int i, int s) -> bool {
+      if (!mbar_wait_sleep(&bars->q_full[s], (i / kStages) & 1, p.err, abort, 51)) return false;
+      tc_fence_after();
+      const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+      const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
+#pragma unroll
+      for (int kb = 0; kb < D / 32; ++kb)
+        mma_mxf8_ss_elect(tmem + C::kColS, dk_ + 2 * kb, dq_ + so + 2 * kb,
+                          idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
+                          tmem + C::kColSFQ + 2 * half, kb > 0);
+#pragma unroll
+      for (int kb = 0; kb < D / 32; ++kb)
+        mma_mxf8_ss_elect(tmem + C::kColDP, dv_ + 2 * kb, ddo + so + 2 * kb,
+                          idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
+                          tmem + C::kColSFdO + 2 * half, kb > 0);
+      tc_commit_elect(&bars->st_ready);
+      return true;
+    };
+    // dV += P^T dO_i, dK += dS^T Q_i, then dQ^T(i) = K^T dS^T over the same
+    // columns the fp8 P^T / dS^T came from (MMAs execute in order)
+    auto issue_acc = [&](int i, int s) -> bool {
+      if (!mbar_wait_sleep(&bars->ds_ready, i & 1, p.err, abort, 52)) return false;
+      tc_fence_after();
+      const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
+      const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQt, dsf + so + (512 >> 4));
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdOt, dsf + so + (1536 >> 4));
+      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdSB, dsfds);
+#pragma unroll
+      for (int kb = 0; kb < kBQ / 32; ++kb) {
+        const uint32_t sfb = kb + 2 * half;
+        mma_mxf8_ts_elect(tmem + C::kColDV, tmem + C::kColDQ + 32 * kb,
+                          ddo + so + kb * ((32 * D) >> 4), idesc_sf_ids(id_acc, 0, sfb),
+                          tmem + C::kColSFP + 4 * kb, tmem + C::kColSFdOt, (i > 0) || (kb > 0));
+        mma_mxf8_ts_elect(tmem + C::kColDK, tmem + C::kColDQ + 32 * kb + 8,
+                          dq_ + so + kb * ((32 * D) >> 4), idesc_sf_ids(id_acc, 0, sfb),
+                          tmem + C::kColSFdS + 4 * kb, tmem + C::kColSFQt, (i > 0) || (kb > 0));
+      }
+      if (D != 128 && i == 0) {
+        if (!mbar_wait_sleep(&bars->kt_ready, 0, p.err, abort, 54)) return false;
+      }
+#pragma unroll
+      for (int kb = 0; kb < kBN / 32; ++kb)
+        mma_mxf8_ss_elect(tmem + C::kColDQ, dkt + kb * ((32 * 128) >> 4),
+                          dds + kb * ((32 * kBQ) >> 4), idesc_sf_ids(id_dq, kb, kb),
+                          tmem + C::kColSFKt, tmem + C::kColSFdSB, kb > 0);
+      // the compute warps release the Q / dO stage once they see dQ^T(i)
+      tc_commit_elect(&bars->dq_full);
+      return true;
+    };
+    if (ok) ok = issue_st(0, 0);
+    for (int i0 = 0; i0 < nsteps && ok; i0 += kStages) {
+#pragma unroll
+      for (int ss = 0; ss < kStages; ++ss) {
+        const int i = i0 + ss;                     // i % kStages == ss
+        if (ok && i < nsteps) {
+          // the next step's S^T / dP^T run while step i is in the compute
+          // warps
+          if (i + 1 < nsteps) {
+            ok = mbar_wait_sleep(&bars->st_loaded, i & 1, p.err, abort, 53);
+            if (ok) ok = issue_st(i + 1, (ss + 1) % kStages);
+          }
+          if (ok) ok = issue_acc(i, ss);
+        }
+      }
+    }
+    if (ok) tc_commit_elect(&bars->acc_done);
+    if (!ok) *abort = 1;
+    tc_commit_elect(&bars->drain);
+    mbar_wait_sleep(&bars->drain, 0, nullptr, nullptr, 0);
   } else {
     // ------------------------------------------------------------- compute
     const int g = (warp - 2) >> 2;                // query block of the step
@@ -387,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (D != 128 && g == 0) {
       // zero-padded 128-byte-row copy of the K tile (64B swizzle -> 128B)
-      ok = mbar_wait(&bars->kv_full, 0, p.err, abort, 59);
+      ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 59);
       if (ok) {
         const uint8_t* src = sm + C::kSmK + m * D;
         uint8_t* dst = sm + C::kSmKT + m * 128;
@@ -402,29 +407,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->kt_ready);
     }
-    // dQ^T(j) (fp32, this warpgroup's 32 queries) -> fp16 rows [q][d] in
-    // shared memory -> one tensor reduce-add into global dQ
+    // dQ^T(j) of this warp (32 channels x this warpgroup's 32 queries, fp32)
+    // -> fp16 [query][channel] tile in the warp's own shared-memory buffer
+    // -> one tensor reduce-add into global dQ, issued by lane 0 (bulk async
+    // groups belong to the issuing thread).  No other warp takes part.
     auto stage_dq = [&](int j, const uint32_t (&rq)[32]) {
+      if (quad * 32 >= D) return;                  // no channels here (D = 64)
       const int hj = step_head(j), q0j = step_q0(j);
-      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (j & 1) * kBQ * D * 2);
-      if (ctid == 0) bulk_wait_read_le1();
-      named_bar_sync(1, 256);
-      if (m < D) {
+      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (warp - 2) * 4096 + (j & 1) * 2048);
+      if (lane == 0) bulk_wait_read_le1();        // step j-2's reduce has read it
+      __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          stg[(32 * g + e) * D + m] = __float2half_rn(__uint_as_float(rq[e]) * p.dq_mult);
-      }
+      for (int e = 0; e < 32; ++e)
+        stg[e * 32 + lane] = __float2half_rn(__uint_as_float(rq[e]) * p.dq_mult);
       fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (ctid == 0) {
+      __syncwarp();
+      if (lane == 0) {
         // rows of the step beyond the sequence carry exact zeros
-        tma_reduce_add_3d(&tma_dq, 0, hj, static_cast<int32_t>(w.start + q0j), stg);
+        tma_reduce_add_3d(&tma_dq, 32 * quad, hj, static_cast<int32_t>(w.start + q0j + 32 * g),
+                          stg);
         bulk_commit();
       }
     };
     auto read_dq = [&](int j, uint32_t (&rq)[32]) -> bool {
-      if (!mbar_wait(&bars->dq_full, j & 1, p.err, abort, 61)) return false;
+      if (!mbar_wait_sleep(&bars->dq_full, j & 1, p.err, abort, 61)) return false;
       tc_fence_after();
+      // every MMA of step j has completed: its Q / dO stage may be refilled
+      if (ctid == 0) mbar_arrive(&bars->q_empty[j % kStages]);
       tmem_ld32(tmem + lb + C::kColDQ + 32 * g, rq);
       tmem_ld_wait();
       return true;
@@ -433,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % kStages;
       const int q0 = step_q0(i);
       const uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-      ok = mbar_wait(&bars->st_ready, i & 1, p.err, abort, 60);
+      ok = mbar_wait_sleep(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
       tc_fence_after();
       uint32_t rs[32], rd[32];
@@ -514,9 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = read_dq(nsteps - 1, rq);
       if (ok) stage_dq(nsteps - 1, rq);
     }
-    if (ctid == 0) bulk_wait0();
+    if (lane == 0) bulk_wait0();
     // epilogue: warpgroup 0 writes dK (times softmax_scale), 1 writes dV
-    if (ok) ok = mbar_wait(&bars->acc_done, 0, p.err, abort, 62);
+    if (ok) ok = mbar_wait_sleep(&bars->acc_done, 0, p.err, abort, 62);
     if (ok) {
       tc_fence_after();
       const bool valid = key < w.len;
@@ -689,7 +698,7 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(hq),
                         static_cast<uint64_t>(sv.total_tokens)};
     uint64_t strides[2] = {static_cast<uint64_t>(D * 2), static_cast<uint64_t>(hq * D * 2)};
-    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, static_cast<uint32_t>(kBQ)};
+    uint32_t box[3] = {32u, 1u, 32u};   // one warp's [32 queries][32 channels]
     if ((st = encode_tmap(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dq, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_NONE)) != LPFA_OK)
       return st;
