@@ -6,7 +6,7 @@
 // the scale arrangement differs); V in 1x32 blocks along head_dim.  Per key
 // tile the kernel recomputes P from the forward LSE, forms
 // dS = P o (dP - D) with D_i = rowsum(dO o O), quantizes P and dS online in
-// 32x32 blocks (per-lane max, then the warp-wide redux.sync.max.abs.f32), and
+// 32x32 blocks (per-lane max, then a warp-wide redux.sync max), and
 // accumulates
 //   dV += P^T dO,  dK += dS^T Q   (TMEM-resident over the query loop)
 //   dQ^T = K^T dS^T               (per query step; scaled by softmax_scale *
@@ -45,7 +45,7 @@ namespace {
 
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
-constexpr int kStages = 2;
+constexpr int kStages = 5;   // Q / dO ring: loads run several steps ahead
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 
@@ -96,8 +96,8 @@ struct BwdParams {
   const uint8_t* sfv;
   const uint8_t* sfdo;
   const uint8_t* sfdo_t;
-  const float* lse2;     // [Hq, Tp]  LSE * log2(e), padded rows
-  const float* delta;    // [Hq, Tp]
+  const float* lse2;     // [Hq, Tp]  -LSE * log2(e), padded rows
+  const float* delta;    // [Hq, Tp]  -D
   __half* dq;            // [T, Hq, D] fp16, accumulated
   __nv_bfloat16* dk;     // [T, Hkv, D]
   __nv_bfloat16* dv;
@@ -155,24 +155,39 @@ __device__ __forceinline__ KvItem kv_item(const BwdParams& p) {
   return w;
 }
 
-// Quantize 32 values (one thread's row of a 32x32 block) with the block's
-// warp-wide amax.  Returns the E8M0 code; writes 8 packed words.
-__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t (&w)[8]) {
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-  const float amax = warp_max_abs(m);
-  const uint32_t code = e8m0_code_from_amax_bits(__float_as_uint(amax));
+// Scale 32 values (one thread's row of a 32x32 block) by 2^-e for the E8M0
+// code of the block's amax (given as fp32 bits) and convert to E4M3; a block
+// holding Inf or NaN gets code 0xFF and payloads 0x7F.  Writes 8 packed
+// words, returns the code.
+__device__ __forceinline__ uint32_t quant_block32(const float (&v)[32], uint32_t amax_bits,
+                                                  uint32_t (&w)[8]) {
+  const uint32_t code = e8m0_code_from_amax_bits(amax_bits);
   const float inv = inv_scale_from_code(code);
+  const uint64_t inv2 = pack2(inv, inv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    w[i] = cvt_e4m3x4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv,
-                      v[4 * i + 3] * inv);
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t a = mul2(pack2(v[4 * i], v[4 * i + 1]), inv2);
+    const uint64_t b = mul2(pack2(v[4 * i + 2], v[4 * i + 3]), inv2);
+    w[i] = cvt_e4m3x4(lo2(a), hi2(a), lo2(b), hi2(b));
+  }
   if (code == 0xFFu) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = 0x7F7F7F7Fu;
   }
   return code;
+}
+
+// max(|a|, |b|, |c|), NaN-propagating.
+__device__ __forceinline__ float max3_abs_nan(float a, float b, float c) {
+  float d;
+  asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Warp-wide maximum of non-negative fp32 values (NaN above +Inf), as bits:
+// for such values the unsigned order of the bits is the numeric order.
+__device__ __forceinline__ uint32_t warp_max_nonneg_bits(float x) {
+  return __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(x));
 }
 
 template <int D>
@@ -414,12 +429,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_dq = [&](int j, const uint32_t (&rq)[32]) {
       if (quad * 32 >= D) return;                  // no channels here (D = 64)
       const int hj = step_head(j), q0j = step_q0(j);
-      __half* stg = reinterpret_cast<__half*>(sm + C::kSmDQ + (warp - 2) * 4096 + (j & 1) * 2048);
+      uint32_t* stg = reinterpret_cast<uint32_t*>(sm + C::kSmDQ + (warp - 2) * 4096 + (j & 1) * 2048);
       if (lane == 0) bulk_wait_read_le1();        // step j-2's reduce has read it
       __syncwarp();
+      // lanes 2k and 2k+1 hold channels 2k, 2k+1: the even lane packs the
+      // pair for queries 0-15, the odd lane for queries 16-31, after one
+      // exchange of the other half
+      const bool odd = lane & 1;
+      const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        stg[e * 32 + lane] = __float2half_rn(__uint_as_float(rq[e]) * p.dq_mult);
+      for (int e = 0; e < 16; e += 2) {
+        const uint64_t a = mul2(pack2(__uint_as_float(rq[e]), __uint_as_float(rq[e + 1])), mul);
+        const uint64_t b = mul2(pack2(__uint_as_float(rq[e + 16]), __uint_as_float(rq[e + 17])), mul);
+        const uint64_t keep = odd ? b : a, send = odd ? a : b;
+        const float o0 = __shfl_xor_sync(0xFFFFFFFFu, lo2(send), 1);
+        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, hi2(send), 1);
+        // low half = even channel
+        const float l0 = odd ? o0 : lo2(keep), h0 = odd ? lo2(keep) : o0;
+        const float l1 = odd ? o1 : hi2(keep), h1 = odd ? hi2(keep) : o1;
+        uint32_t w0, w1;
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w0) : "f"(h0), "f"(l0));
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w1) : "f"(h1), "f"(l1));
+        const int qrow = e + (odd ? 16 : 0);
+        stg[qrow * 16 + (lane >> 1)] = w0;
+        stg[(qrow + 1) * 16 + (lane >> 1)] = w1;
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
@@ -448,15 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rs[32], rd[32];
       tmem_ld32(tmem + lb + C::kColS + 32 * g, rs);
       tmem_ld32(tmem + lb + C::kColDP + 32 * g, rd);
-      float lse2[32], dlt[32];
+      float nlse2[32], ndlt[32];
       {
         const float4* l4 = reinterpret_cast<const float4*>(st + C::kStLse) + 8 * g;
         const float4* d4 = reinterpret_cast<const float4*>(st + C::kStDelta) + 8 * g;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const float4 a4 = l4[t], b4 = d4[t];
-          lse2[4 * t] = a4.x; lse2[4 * t + 1] = a4.y; lse2[4 * t + 2] = a4.z; lse2[4 * t + 3] = a4.w;
-          dlt[4 * t] = b4.x; dlt[4 * t + 1] = b4.y; dlt[4 * t + 2] = b4.z; dlt[4 * t + 3] = b4.w;
+          nlse2[4 * t] = a4.x; nlse2[4 * t + 1] = a4.y; nlse2[4 * t + 2] = a4.z; nlse2[4 * t + 3] = a4.w;
+          ndlt[4 * t] = b4.x; ndlt[4 * t + 1] = b4.y; ndlt[4 * t + 2] = b4.z; ndlt[4 * t + 3] = b4.w;
         }
       }
       tmem_ld_wait();
@@ -470,21 +504,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo = p.causal ? max(0, key - qb0) : 0;
       const int hi = key < w.len ? min(32, w.len - qb0) : 0;
       const bool all_visible = __all_sync(0xFFFFFFFFu, lo == 0 && hi == 32);
+      // x = s * c2 - LSE2, two elements per instruction (the workspace holds
+      // -LSE2 and -D); invisible entries get x = -inf, so P = 2^x = 0
+      const uint64_t c2x2 = pack2(p.scale_log2, p.scale_log2);
+      float xv[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float x = fmaf(__uint_as_float(rs[j]), p.scale_log2, -lse2[j]);
-        pv[j] = ex2(x);
+      for (int j = 0; j < 32; j += 2) {
+        const uint64_t x = fma2(pack2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])), c2x2,
+                                pack2(nlse2[j], nlse2[j + 1]));
+        xv[j] = lo2(x);
+        xv[j + 1] = hi2(x);
       }
       if (!all_visible) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (j < lo || j >= hi) pv[j] = 0.f;
+          if (j < lo || j >= hi) xv[j] = -INFINITY;
       }
+      // P's block amax is 2^(max x) (2^x is monotonic); its warp reduction
+      // is under way while the exponentials run
+      float mx = fmaxf(xv[0], xv[1]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) dsv[j] = pv[j] * (__uint_as_float(rd[j]) - dlt[j]);
+      for (int j = 2; j < 32; j += 2) mx = max3(mx, xv[j], xv[j + 1]);
+      const uint32_t ap_bits = warp_max_nonneg_bits(ex2(mx));
+#pragma unroll
+      for (int j = 0; j < 32; ++j) pv[j] = ex2(xv[j]);
+      // dS = P (dP - D)
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const uint64_t d = add2(pack2(__uint_as_float(rd[j]), __uint_as_float(rd[j + 1])),
+                                pack2(ndlt[j], ndlt[j + 1]));
+        const uint64_t ds = mul2(pack2(pv[j], pv[j + 1]), d);
+        dsv[j] = lo2(ds);
+        dsv[j + 1] = hi2(ds);
+      }
+      float md = max3_abs_nan(dsv[0], dsv[1], dsv[2]);
+#pragma unroll
+      for (int j = 3; j < 31; j += 2) md = max3_abs_nan(md, dsv[j], dsv[j + 1]);
+      md = max3_abs_nan(md, dsv[31], 0.f);
+      const uint32_t ad_bits = warp_max_nonneg_bits(md);
       uint32_t wp[8], wd[8];
-      const uint32_t cp_ = quant_block32(pv, wp);
-      const uint32_t cd = quant_block32(dsv, wd);
+      const uint32_t cp_ = quant_block32(pv, ap_bits, wp);
+      const uint32_t cd = quant_block32(dsv, ad_bits, wd);
       // the previous step's dQ^T leaves TMEM before this step's fp8 P^T /
       // dS^T take its columns (and its MMA, the last reader of the dS^T
       // shared-memory tile, has completed)
@@ -564,7 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = sum_d dO_id * O_id and LSE in log2 units, in the padded row layout.
+// -D_i = -sum_d dO_id * O_id and -LSE in log2 units, in the padded row layout
+// (negated so that the backward adds them in packed fp32x2 instructions).
 // One warp per (token, head).
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const SeqView sv, const __nv_bfloat16* __restrict__ o,
@@ -608,8 +669,8 @@ __global__ void __launch_bounds__(256)
     const SeqInfo si = seq_info(sv, s);
     const int64_t pr = si.sf_start + (tok - si.start);
     const int64_t idx = static_cast<int64_t>(h) * sv.total_sf_rows + pr;
-    delta[idx] = acc;
-    lse2[idx] = lse[static_cast<int64_t>(h) * sv.total_tokens + tok] * 1.4426950408889634f;
+    delta[idx] = -acc;
+    lse2[idx] = -(lse[static_cast<int64_t>(h) * sv.total_tokens + tok] * 1.4426950408889634f);
   }
 }
 
