@@ -7,10 +7,10 @@
 // floor(log2 amax) - 8 + 127 clamped at 0 (taken from amax's exponent bits),
 // payload = RNE-satfinite E4M3 of x * 2^-e.
 //
-// One warp owns a 32-token x 32-channel tile of one head; lane i holds token
-// row i (64 contiguous bytes).  The block shape only changes how amax is
-// grouped: per lane (1x32), per column across lanes (32x1), or the whole
-// tile (32x32).  The kernel is a single pass over HBM: 2 bytes read and
+// One warp owns a 32-token x head_dim block of one head; head_dim/32 lanes
+// share each token row.  The block shape only changes how amax is grouped:
+// per lane row (1x32), per channel across the block's tokens (32x1), or the
+// whole 32x32 tile (32x32).  The kernel is a single pass over HBM: 2 bytes read and
 // 1 + 1/32 (+1/32 per extra scale layout) bytes written per element.
 #include <cuda_runtime.h>
 
@@ -56,98 +56,165 @@ __device__ __forceinline__ void quant_row(const float (&f)[32],
   }
 }
 
-template <int kMode>  // 0: 1x32, 1: 32x1, 2: 32x32
+// bf16 pair -> two floats
+__device__ __forceinline__ void unpack_row(const uint4 (&v)[4], float (&f)[32]) {
+  const uint32_t* u = reinterpret_cast<const uint32_t*>(v);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    f[2 * i + 0] = __uint_as_float(u[i] << 16);
+    f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+
+// One warp per (32-row padded block rb, head h).  kNcb = head_dim / 32
+// consecutive lanes share a token row (lane = t * kNcb + cb: channel block
+// cb of token t), so one load instruction of the warp reads whole 2*head_dim
+// byte head rows of 32 / kNcb tokens; kNcb loads cover the 32 tokens.
+// (Token-per-lane loads, 64 bytes at the token stride, reach ~2/3 of the
+// bandwidth of these.)  Block maxima over tokens reduce across the lanes
+// that share cb.
+template <int kMode, int kNcb>  // mode 0: 1x32, 1: 32x1, 2: 32x32
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     mx_quantize_kernel(const QuantArgs a) {
+  constexpr int kTpl = 32 / kNcb;                  // tokens per load
   const int lane = threadIdx.x & 31;
-  const int64_t tile =
-      static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (tile >= a.ntiles) return;
-  const int ncb = a.D >> 5;
-  const int cb = static_cast<int>(tile % ncb);
-  const int64_t t2 = tile / ncb;
-  const int h = static_cast<int>(t2 % a.H);
-  const int64_t rb = t2 / a.H;
-  const int64_t pr0 = rb * 32;  // first padded scale row of the block
-
-  const int s = seq_of_sf_row(a.seqs, pr0);
-  const SeqInfo si = seq_info(a.seqs, s);
+  const int cb = lane % kNcb, t = lane / kNcb;
+  const int64_t task = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t ntasks = (a.seqs.total_sf_rows / 32) * a.H;
+  if (task >= ntasks) return;
+  const int h = static_cast<int>(task % a.H);
+  const int64_t rb = task / a.H;
+  const int64_t pr0 = rb * 32;                     // first padded row of the block
+  const int sq = seq_of_sf_row(a.seqs, pr0);
+  const SeqInfo si = seq_info(a.seqs, sq);
   const int64_t off = pr0 - si.sf_start;           // token offset in sequence
   const int64_t nvalid64 = static_cast<int64_t>(si.len) - off;
   const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : static_cast<int>(nvalid64));
-  const bool valid = lane < nvalid;
-  const int64_t tok = si.start + off + lane;
-  const int64_t elem0 = (tok * a.H + h) * a.D + 32 * cb;
+  const int64_t tile_base = ((rb >> 2) * a.H + h) * 512;   // 512-byte scale tile
+  const int kb_row = static_cast<int>(rb & 3);     // token block within the tile
 
-  float f[32];
-  {
-    uint4 v[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                  make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  // ---- all rows of this lane in flight at once
+  uint4 v[kNcb][4];
+#pragma unroll
+  for (int r = 0; r < kNcb; ++r) {
+    const int row = r * kTpl + t;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[r][i] = make_uint4(0, 0, 0, 0);
+    if (row < nvalid) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.x + ((si.start + off + row) * a.H + h) * a.D + 32 * cb);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[r][i] = __ldcs(src + i);
+    }
+  }
+
+  uint32_t bcode = 0;                              // 32x32: the block's code
+  uint32_t ccode[32];                              // 32x1: per channel of cb
+  if (kMode != 0) {
+    // maxima over this lane's rows, then over the lanes sharing cb
+    uint32_t m = 0;
+    uint32_t mc[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mc[j] = 0;
+#pragma unroll
+    for (int r = 0; r < kNcb; ++r) {
+      float f[32];
+      unpack_row(v[r], f);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (kMode == 2) m = max(m, abs_bits(f[j]));
+        else mc[j] = max(mc[j], abs_bits(f[j]));
+      }
+    }
+    if (kMode == 2) {
+#pragma unroll
+      for (int x = kNcb; x < 32; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
+      bcode = e8m0_code_from_amax_bits(m);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        uint32_t q = mc[j];
+#pragma unroll
+        for (int x = kNcb; x < 32; x <<= 1) q = max(q, __shfl_xor_sync(0xFFFFFFFFu, q, x));
+        ccode[j] = e8m0_code_from_amax_bits(q);
+      }
+    }
+  }
+
+  // ---- payload and per-row scales
+#pragma unroll
+  for (int r = 0; r < kNcb; ++r) {
+    const int row = r * kTpl + t;                  // token row within the block
+    const bool valid = row < nvalid;
+    const int64_t tok = si.start + off + row;
+    float f[32];
+    unpack_row(v[r], f);
+    uint32_t code[32];
+    if (kMode == 0) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
+      const uint32_t c = e8m0_code_from_amax_bits(m);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) code[j] = c;
+    } else if (kMode == 1) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) code[j] = ccode[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) code[j] = bcode;
+    }
     if (valid) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.x + elem0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = __ldcs(src + i);
+      uint32_t w[8];
+      quant_row(f, code, w);
+      uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.H + h) * a.D + 32 * cb);
+      __stcs(dst + 0, make_uint4(w[0], w[1], w[2], w[3]));
+      __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
     }
-    const uint32_t* u = reinterpret_cast<const uint32_t*>(v);
+    if (kMode != 1) {
+      // this row's kNcb codes gathered into one word by the cb = 0 lane:
+      // compact [tok][h][cb] bytes and tensor-core bytes
+      // row * 16 + kb_row * 4 + cb are both contiguous in cb
+      const uint32_t c = (kMode == 0 && !valid) ? 0u : code[0];
+      uint32_t word = c;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      f[2 * i + 0] = __uint_as_float(u[i] << 16);
-      f[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+      for (int k = 1; k < kNcb; ++k)
+        word |= __shfl_down_sync(0xFFFFFFFFu, c, k) << (8 * k);
+      if (cb == 0) {
+        if (a.sf_mma != nullptr) {
+          const uint32_t wm = (kMode == 2 && !valid) ? 0u : word;
+          uint8_t* d = a.sf_mma + tile_base + row * 16 + kb_row * 4;
+          if (kNcb == 4) *reinterpret_cast<uint32_t*>(d) = wm;
+          else *reinterpret_cast<uint16_t*>(d) = static_cast<uint16_t>(wm);
+        }
+        if (kMode == 0 && a.sf != nullptr && valid) {
+          uint8_t* d = a.sf + (tok * a.H + h) * kNcb;
+          if (kNcb == 4) *reinterpret_cast<uint32_t*>(d) = word;
+          else *reinterpret_cast<uint16_t*>(d) = static_cast<uint16_t>(word);
+        }
+      }
+      if (kMode == 2 && a.sf_mma_t != nullptr)
+        a.sf_mma_t[tile_base + row * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(bcode);
     }
   }
 
-  uint32_t code[32];
-  if (kMode == 0) {
-    uint32_t m = 0;
+  // ---- block-level scales
+  if (kMode == 2 && a.sf != nullptr && t == 0)
+    a.sf[(rb * a.H + h) * kNcb + cb] = static_cast<uint8_t>(bcode);
+  if (kMode == 1) {
+    // channel 32 cb + j of the block: the kTpl lanes of cb each write 32 /
+    // kTpl consecutive channels
+    constexpr int kPer = 32 / kTpl;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
-    const uint32_t c = e8m0_code_from_amax_bits(m);
+    for (int k = 0; k < kPer; ++k) {
+      const int j = t * kPer + k;
+      uint32_t cj = 0;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) code[j] = c;
-  } else if (kMode == 1) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      code[j] = e8m0_code_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, abs_bits(f[j])));
-  } else {
-    uint32_t m = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
-    const uint32_t c = e8m0_code_from_amax_bits(__reduce_max_sync(0xFFFFFFFFu, m));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) code[j] = c;
-  }
-
-  if (valid) {
-    uint32_t w[8];
-    quant_row(f, code, w);
-    uint4* dst = reinterpret_cast<uint4*>(a.out + elem0);
-    __stcs(dst + 0, make_uint4(w[0], w[1], w[2], w[3]));
-    __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
-  }
-
-  // ---- scales
-  const int64_t tile128 = (rb >> 2) * a.H + h;   // [Tp/128, H] index
-  const int kb_row = static_cast<int>(rb & 3);   // token block within tile
-  if (kMode == 0) {
-    const uint8_t c = static_cast<uint8_t>(code[0]);
-    if (a.sf != nullptr && valid) a.sf[(tok * a.H + h) * (a.D >> 5) + cb] = c;
-    if (a.sf_mma != nullptr)
-      a.sf_mma[tile128 * 512 + lane * 16 + kb_row * 4 + cb] = valid ? c : 0;
-  } else if (kMode == 1) {
-    // lane j reports channel 32*cb + j
-    uint32_t cj = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) cj = (lane == j) ? code[j] : cj;
-    if (a.sf != nullptr) a.sf[(rb * a.H + h) * a.D + 32 * cb + lane] = static_cast<uint8_t>(cj);
-    if (a.sf_mma != nullptr)
-      a.sf_mma[tile128 * 512 + lane * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(cj);
-  } else {
-    const uint8_t c = static_cast<uint8_t>(code[0]);
-    if (a.sf != nullptr && lane == 0) a.sf[(rb * a.H + h) * (a.D >> 5) + cb] = c;
-    if (a.sf_mma != nullptr)
-      a.sf_mma[tile128 * 512 + lane * 16 + kb_row * 4 + cb] = valid ? c : 0;
-    if (a.sf_mma_t != nullptr)
-      a.sf_mma_t[tile128 * 512 + lane * 16 + cb * 4 + kb_row] = c;
+      for (int q = 0; q < 32; ++q) cj = (q == j) ? ccode[q] : cj;
+      if (a.sf != nullptr) a.sf[(rb * a.H + h) * a.D + 32 * cb + j] = static_cast<uint8_t>(cj);
+      if (a.sf_mma != nullptr)
+        a.sf_mma[tile_base + j * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(cj);
+    }
   }
 }
 
@@ -194,13 +261,24 @@ extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
   a.H = static_cast<int32_t>(heads);
   a.D = static_cast<int32_t>(head_dim);
   a.ntiles = (Tp / 32) * heads * (head_dim / 32);
-  const int64_t blocks = ceil_div(a.ntiles, kWarpsPerBlock);
+  const int64_t ntasks = (Tp / 32) * heads;        // one warp per (32-row block, head)
+  const int64_t blocks = ceil_div(ntasks, kWarpsPerBlock);
   LPFA_CHECK_ARG(blocks < (1ll << 31));
   dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
+  const bool d128 = head_dim == 128;
   switch (blk) {
-    case LPFA_BLK_1X32: mx_quantize_kernel<0><<<grid, block, 0, cs>>>(a); break;
-    case LPFA_BLK_32X1: mx_quantize_kernel<1><<<grid, block, 0, cs>>>(a); break;
-    case LPFA_BLK_32X32: mx_quantize_kernel<2><<<grid, block, 0, cs>>>(a); break;
+    case LPFA_BLK_1X32:
+      if (d128) mx_quantize_kernel<0, 4><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<0, 2><<<grid, block, 0, cs>>>(a);
+      break;
+    case LPFA_BLK_32X1:
+      if (d128) mx_quantize_kernel<1, 4><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<1, 2><<<grid, block, 0, cs>>>(a);
+      break;
+    case LPFA_BLK_32X32:
+      if (d128) mx_quantize_kernel<2, 4><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<2, 2><<<grid, block, 0, cs>>>(a);
+      break;
   }
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
