@@ -432,27 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t* stg = reinterpret_cast<uint32_t*>(sm + C::kSmDQ + (warp - 2) * 4096 + (j & 1) * 2048);
       if (lane == 0) bulk_wait_read_le1();        // step j-2's reduce has read it
       __syncwarp();
-      // lanes 2k and 2k+1 hold channels 2k, 2k+1: the even lane packs the
-      // pair for queries 0-15, the odd lane for queries 16-31, after one
-      // exchange of the other half
-      const bool odd = lane & 1;
+      // lane = channel: each query row of the tile is 32 consecutive halves
+      __half* stg16 = reinterpret_cast<__half*>(stg);
       const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
 #pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        const uint64_t a = mul2(pack2(__uint_as_float(rq[e]), __uint_as_float(rq[e + 1])), mul);
-        const uint64_t b = mul2(pack2(__uint_as_float(rq[e + 16]), __uint_as_float(rq[e + 17])), mul);
-        const uint64_t keep = odd ? b : a, send = odd ? a : b;
-        const float o0 = __shfl_xor_sync(0xFFFFFFFFu, lo2(send), 1);
-        const float o1 = __shfl_xor_sync(0xFFFFFFFFu, hi2(send), 1);
-        // low half = even channel
-        const float l0 = odd ? o0 : lo2(keep), h0 = odd ? lo2(keep) : o0;
-        const float l1 = odd ? o1 : hi2(keep), h1 = odd ? hi2(keep) : o1;
-        uint32_t w0, w1;
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w0) : "f"(h0), "f"(l0));
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w1) : "f"(h1), "f"(l1));
-        const int qrow = e + (odd ? 16 : 0);
-        stg[qrow * 16 + (lane >> 1)] = w0;
-        stg[(qrow + 1) * 16 + (lane >> 1)] = w1;
+      for (int e = 0; e < 32; e += 2) {
+        const uint64_t v = mul2(pack2(__uint_as_float(rq[e]), __uint_as_float(rq[e + 1])), mul);
+        stg16[e * 32 + lane] = __float2half_rn(lo2(v));
+        stg16[(e + 1) * 32 + lane] = __float2half_rn(hi2(v));
       }
       fence_proxy_async_smem();
       __syncwarp();
