@@ -56,6 +56,22 @@ __device__ __forceinline__ void quant_row(const float (&f)[32],
   }
 }
 
+// As quant_row with the codes of the 32 values packed four to a word
+// (element 4i + q takes byte q of cw[i]).
+__device__ __forceinline__ void quant_row_packed(const float (&f)[32], const uint32_t (&cw)[8],
+                                                 uint32_t (&w)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float x[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) x[q] = f[4 * i + q] * inv_scale_from_code((cw[i] >> (8 * q)) & 0xFFu);
+    w[i] = cvt_e4m3x4(x[0], x[1], x[2], x[3]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (((cw[i] >> (8 * q)) & 0xFFu) == 0xFFu) w[i] = (w[i] & ~(0xFFu << (8 * q))) | (0x7Fu << (8 * q));
+  }
+}
+
 // bf16 pair -> two floats
 __device__ __forceinline__ void unpack_row(const uint4 (&v)[4], float (&f)[32]) {
   const uint32_t* u = reinterpret_cast<const uint32_t*>(v);
@@ -74,7 +90,7 @@ __device__ __forceinline__ void unpack_row(const uint4 (&v)[4], float (&f)[32]) 
 // bandwidth of these.)  Block maxima over tokens reduce across the lanes
 // that share cb.
 template <int kMode, int kNcb>  // mode 0: 1x32, 1: 32x1, 2: 32x32
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per SM
     mx_quantize_kernel(const QuantArgs a) {
   constexpr int kTpl = 32 / kNcb;                  // tokens per load
   const int lane = threadIdx.x & 31;
@@ -109,35 +125,44 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 
   uint32_t bcode = 0;                              // 32x32: the block's code
-  uint32_t ccode[32];                              // 32x1: per channel of cb
-  if (kMode != 0) {
-    // maxima over this lane's rows, then over the lanes sharing cb
+  uint32_t cw[8];                                  // 32x1: codes of cb's 32 channels, 4 per word
+  if (kMode == 2) {
+    // maximum over this lane's rows, then over the lanes sharing cb
     uint32_t m = 0;
-    uint32_t mc[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) mc[j] = 0;
 #pragma unroll
     for (int r = 0; r < kNcb; ++r) {
-      float f[32];
-      unpack_row(v[r], f);
+      const uint32_t* u = reinterpret_cast<const uint32_t*>(v[r]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (kMode == 2) m = max(m, abs_bits(f[j]));
-        else mc[j] = max(mc[j], abs_bits(f[j]));
-      }
+      for (int i = 0; i < 16; ++i)
+        m = max(m, max((u[i] << 16) & 0x7FFFFFFFu, u[i] & 0x7FFF0000u));
     }
-    if (kMode == 2) {
 #pragma unroll
-      for (int x = kNcb; x < 32; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
-      bcode = e8m0_code_from_amax_bits(m);
-    } else {
+    for (int x = kNcb; x < 32; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
+    bcode = e8m0_code_from_amax_bits(m);
+  } else if (kMode == 1) {
+    // per channel: maximum over this lane's rows, then over the lanes
+    // sharing cb; four channels at a time keeps the live state small
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        uint32_t q = mc[j];
+    for (int g4 = 0; g4 < 8; ++g4) {
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int x = kNcb; x < 32; x <<= 1) q = max(q, __shfl_xor_sync(0xFFFFFFFFu, q, x));
-        ccode[j] = e8m0_code_from_amax_bits(q);
+      for (int r = 0; r < kNcb; ++r) {
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(v[r]);
+        const uint32_t lo = u[2 * g4], hi = u[2 * g4 + 1];   // channels 4 g4 .. 4 g4 + 3
+        q[0] = max(q[0], (lo << 16) & 0x7FFFFFFFu);
+        q[1] = max(q[1], lo & 0x7FFF0000u);
+        q[2] = max(q[2], (hi << 16) & 0x7FFFFFFFu);
+        q[3] = max(q[3], hi & 0x7FFF0000u);
       }
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t qq = q[k];
+#pragma unroll
+        for (int x = kNcb; x < 32; x <<= 1) qq = max(qq, __shfl_xor_sync(0xFFFFFFFFu, qq, x));
+        word |= e8m0_code_from_amax_bits(qq) << (8 * k);
+      }
+      cw[g4] = word;
     }
   }
 
@@ -157,16 +182,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
       const uint32_t c = e8m0_code_from_amax_bits(m);
 #pragma unroll
       for (int j = 0; j < 32; ++j) code[j] = c;
-    } else if (kMode == 1) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) code[j] = ccode[j];
-    } else {
+    } else if (kMode == 2) {
 #pragma unroll
       for (int j = 0; j < 32; ++j) code[j] = bcode;
     }
     if (valid) {
       uint32_t w[8];
-      quant_row(f, code, w);
+      if (kMode == 1) quant_row_packed(f, cw, w);
+      else quant_row(f, code, w);
       uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.H + h) * a.D + 32 * cb);
       __stcs(dst + 0, make_uint4(w[0], w[1], w[2], w[3]));
       __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
@@ -208,9 +231,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int j = t * kPer + k;
-      uint32_t cj = 0;
+      uint32_t word = 0;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) cj = (q == j) ? ccode[q] : cj;
+      for (int q = 0; q < 8; ++q) word = (q == (j >> 2)) ? cw[q] : word;
+      const uint32_t cj = (word >> (8 * (j & 3))) & 0xFFu;
       if (a.sf != nullptr) a.sf[(rb * a.H + h) * a.D + 32 * cb + j] = static_cast<uint8_t>(cj);
       if (a.sf_mma != nullptr)
         a.sf_mma[tile_base + j * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(cj);
