@@ -611,53 +611,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// -D_i = -sum_d dO_id * O_id and -LSE in log2 units, in the padded row layout
-// (negated so that the backward adds them in packed fp32x2 instructions).
-// One warp per (token, head).
+// -D_i = -sum_d dO_id * O_id and -LSE in log2 units for every padded row
+// (zeros on padding rows), negated so that the backward adds them in packed
+// fp32x2 instructions; the FP16 dQ row of each token is cleared on the way.
+// Rows in (padded row, head) order; head_dim / 8 lanes per row, one 16-byte
+// chunk of O and of dO each.
+template <int D>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const SeqView sv, const __nv_bfloat16* __restrict__ o,
                           const __nv_bfloat16* __restrict__ dout,
                           const float* __restrict__ lse, float* __restrict__ lse2,
-                          float* __restrict__ delta, int32_t hq, int32_t d) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  if (row >= sv.total_tokens * hq) return;
-  const int64_t tok = row / hq;
-  const int h = static_cast<int>(row % hq);
+                          float* __restrict__ delta, __half* __restrict__ dq, int32_t hq) {
+  constexpr int kLanes = D / 8;
+  const int64_t nrows = sv.total_sf_rows * hq;
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gid / kLanes;
+  const int sub = static_cast<int>(gid % kLanes);
+  const bool in = row < nrows;
   float acc = 0.f;
-  for (int c = lane * 4; c < d; c += 128) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + row * d + c);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + row * d + c);
-    const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  bool valid = false;
+  int64_t tok = 0, pr = 0;
+  int h = 0;
+  if (in) {
+    pr = row / hq;
+    h = static_cast<int>(row % hq);
+    const SeqInfo si = seq_info(sv, seq_of_sf_row(sv, pr));
+    const int64_t off = pr - si.sf_start;
+    valid = off < si.len;
+    tok = si.start + off;
+    if (valid) {
+      const int64_t e = (tok * hq + h) * D + 8 * sub;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + e);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + e);
+      const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 fa = __bfloat1622float2(a2[k]);
-      const float2 fb = __bfloat1622float2(b2[k]);
-      acc = fmaf(fa.x, fb.x, acc);
-      acc = fmaf(fa.y, fb.y, acc);
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(a2[k]);
+        const float2 fb = __bfloat1622float2(b2[k]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
+      *reinterpret_cast<uint4*>(dq + e) = make_uint4(0, 0, 0, 0);
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  if (lane == 0) {
-    // padded row of this token
-    int s;
-    if (sv.cu_seqlens == nullptr) {
-      s = static_cast<int>(tok / sv.seqlen);
-    } else {
-      int lo = 0, hi = sv.nseq - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(sv.cu_seqlens + mid) <= tok) lo = mid; else hi = mid - 1;
-      }
-      s = lo;
-    }
-    const SeqInfo si = seq_info(sv, s);
-    const int64_t pr = si.sf_start + (tok - si.start);
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (in && sub == 0) {
     const int64_t idx = static_cast<int64_t>(h) * sv.total_sf_rows + pr;
-    delta[idx] = -acc;
-    lse2[idx] = -(lse[static_cast<int64_t>(h) * sv.total_tokens + tok] * 1.4426950408889634f);
+    delta[idx] = valid ? -acc : 0.f;
+    lse2[idx] = valid ? -(lse[static_cast<int64_t>(h) * sv.total_tokens + tok] * 1.4426950408889634f)
+                      : 0.f;
   }
 }
 
@@ -717,14 +721,20 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);
   float* lse2 = reinterpret_cast<float*>(ws + 256);
   float* delta = lse2 + hq * sv.total_sf_rows;
-  LPFA_CHECK_CUDA(cudaMemsetAsync(ws, 0, bwd_ws_bytes(desc), cs));
-  LPFA_CHECK_CUDA(cudaMemsetAsync(dq, 0, sv.total_tokens * hq * D * 2, cs));
-
+  // error words; the preprocess writes every log2-LSE / D row and clears dQ
+  LPFA_CHECK_CUDA(cudaMemsetAsync(ws, 0, 256, cs));
   {
-    const int64_t rows = sv.total_tokens * hq;
-    bwd_preprocess_kernel<<<static_cast<unsigned>(ceil_div(rows, 8)), 256, 0, cs>>>(
-        sv, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
-        lse, lse2, delta, static_cast<int32_t>(hq), static_cast<int32_t>(D));
+    const int64_t threads = sv.total_sf_rows * hq * (D / 8);
+    LPFA_CHECK_ARG(ceil_div(threads, 256) < (1ll << 31));
+    const unsigned blocks = static_cast<unsigned>(ceil_div(threads, 256));
+    if (D == 128)
+      bwd_preprocess_kernel<128><<<blocks, 256, 0, cs>>>(
+          sv, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+          lse, lse2, delta, static_cast<__half*>(dq), static_cast<int32_t>(hq));
+    else
+      bwd_preprocess_kernel<64><<<blocks, 256, 0, cs>>>(
+          sv, static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout),
+          lse, lse2, delta, static_cast<__half*>(dq), static_cast<int32_t>(hq));
     LPFA_CHECK_CUDA(cudaGetLastError());
   }
 
