@@ -77,12 +77,18 @@ struct BwdCfg {
   static constexpr int kStSF = 2 * kBQ * D;                       // SFQ, SFQt, SFdO, SFdOt
   static constexpr int kStLse = kStSF + 4 * 512;                  // 64 floats
   static constexpr int kStDelta = kStLse + kBQ * 4;               // 64 floats
-  static constexpr int kStageBytes = ((kStDelta + kBQ * 4) + 1023) / 1024 * 1024;
+  // accumulator seeds: [64 queries][16 bf16] K-major, 32-byte swizzle; row q
+  // holds hi, lo of -LSE_q / c (k = 0, 1) and of -D_q (k = 2, 3)
+  static constexpr int kStSeed = ((kStDelta + kBQ * 4) + 255) / 256 * 256;
+  static constexpr int kStageBytes = ((kStSeed + kBQ * 32) + 1023) / 1024 * 1024;
   static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes; // 128 x 64 B (SW64)
   static constexpr int kSmSFdS = kSmDS + kBN * kBQ;               // 512 B
   static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
+  // constant A operands of the seed MMAs: [128 keys][16 bf16], 32-byte
+  // swizzle, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
+  static constexpr int kSmOnes = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
   // dQ staging: per compute warp two [32 queries][32 channels] fp16 tiles
-  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
+  static constexpr int kSmDQ = kSmOnes + 2 * kBN * 32;
   static constexpr int kSmBar = kSmDQ + 8 * 2 * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
 };
@@ -111,8 +117,9 @@ struct BwdParams {
 
 struct BwdBars {
   uint64_t kv_full;
-  uint64_t q_full[kStages];
+  uint64_t q_full[kStages];    // Q, dO, scales landed and the seed tile written
   uint64_t q_empty[kStages];
+  uint64_t lse_full[kStages];  // the stage's -log2 LSE and -D rows landed
   uint64_t st_ready;
   uint64_t ds_ready;
   uint64_t dq_full;
@@ -218,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_full[s], 2);
       mbar_init(&bars->q_empty[s], 1);
+      mbar_init(&bars->lse_full[s], 1);
     }
     mbar_init(&bars->st_ready, 1);
     mbar_init(&bars->ds_ready, 8);
@@ -263,6 +271,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     bulk_load_elect(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
     bulk_load_elect(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
     bulk_load_elect(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+    // Constant "ones" operands and zeroed seed tiles (32-byte swizzle: the
+    // 16-byte half k/8 of row r sits at half (k/8) ^ ((r >> 2) & 1)).  The
+    // first q_full arrival below publishes them to the tensor pipe.
+    {
+      uint32_t* ones = reinterpret_cast<uint32_t*>(sm + C::kSmOnes);
+      for (int i = lane; i < 2 * kBN * 8; i += 32) {
+        const int t = i / (kBN * 8), r = (i / 8) % kBN, wd = i % 8;   // word wd of row r
+        const int lhalf = (wd >> 2) ^ ((r >> 2) & 1);                    // logical half
+        // bf16 pair (1.0, 1.0) in logical word 0 (k = 0, 1) of the LSE tile
+        // and logical word 1 (k = 2, 3) of the D tile
+        const bool one = lhalf == 0 && (wd & 3) == t;
+        ones[i] = one ? 0x3F803F80u : 0u;
+      }
+      for (int st = 0; st < kStages; ++st) {
+        uint32_t* seed = reinterpret_cast<uint32_t*>(sm + C::kSmStage0 + st * C::kStageBytes + C::kStSeed);
+        for (int i = lane; i < kBQ * 8; i += 32) seed[i] = 0u;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+    const float inv_c2 = 1.f / p.scale_log2;
     bool ok = true;
     int issued[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
@@ -274,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = step_head(i), q0 = step_q0(i);
       uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
       uint64_t* bar = &bars->q_full[s];
-      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * D + 4 * 512 + 2 * kBQ * 4);
+      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * D + 4 * 512);
       const int32_t row_q = static_cast<int32_t>(w.start + q0);
       tma_load_3d_elect(st + C::kStQ, &tma_q, 0, h, row_q, bar);
       tma_load_3d_elect(st + C::kStdO, &tma_do, 0, h, row_q, bar);
@@ -285,14 +314,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
       bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
       const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
-      bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, bar);
-      bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, bar);
+      uint64_t* lbar = &bars->lse_full[s];
+      mbar_arrive_expect_tx_elect(lbar, 2 * kBQ * 4);
+      bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, lbar);
+      bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, lbar);
       issued[s] = static_cast<int>(ph);
+      // seed rows: -LSE_q / c = -log2LSE_q / c2 and -D_q, each as a bf16
+      // pair hi + lo (hi = bf16(v), lo = bf16(v - hi): ~16 significant bits)
+      ok = mbar_wait_sleep(lbar, ph, p.err, abort, 41);
+      if (ok) {
+        const float* nl = reinterpret_cast<const float*>(st + C::kStLse);
+        const float* nd = reinterpret_cast<const float*>(st + C::kStDelta);
+        uint8_t* seed = st + C::kStSeed;
+#pragma unroll
+        for (int k = 0; k < kBQ / 32; ++k) {
+          const int r = lane + 32 * k;
+          const float vl = nl[r] * inv_c2, vd = nd[r];
+          const __nv_bfloat16 hl = __float2bfloat16_rn(vl);
+          const __nv_bfloat16 ll = __float2bfloat16_rn(vl - __bfloat162float(hl));
+          const __nv_bfloat16 hd = __float2bfloat16_rn(vd);
+          const __nv_bfloat16 ld = __float2bfloat16_rn(vd - __bfloat162float(hd));
+          const uint32_t w0 = static_cast<uint32_t>(__bfloat16_as_ushort(hl)) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(ll)) << 16);
+          const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(hd)) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(ld)) << 16);
+          *reinterpret_cast<uint2*>(seed + r * 32 + ((r >> 2) & 1) * 16) = make_uint2(w0, w1);
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      // second arrival (also on abort, so that the phase can still complete
+      // once the copies land)
+      if (lane == 0) mbar_arrive(bar);
+      if (!ok) break;
     }
     if (!ok) {
       for (int s = 0; s < kStages; ++s)
-        if (issued[s] >= 0)
+        if (issued[s] >= 0) {
+          mbar_wait_sleep(&bars->lse_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
           mbar_wait_sleep(&bars->q_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+        }
       mbar_wait_sleep(&bars->kv_full, 0, nullptr, nullptr, 0);
     }
   } else if (warp == 1) {
@@ -315,6 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq_ = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStQ), 16, C::kSbo, C::kSw);
     const uint64_t ddo = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStdO), 16, C::kSbo, C::kSw);
     const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSmStage0 + C::kStSF));
+    // seed MMAs (bf16, K = 16): S^T <- -LSE / c, dP^T <- -D, broadcast over keys
+    constexpr uint32_t id_seed = idesc_bf16(128, kBQ, 0, 0);
+    const uint64_t dones_l = make_sdesc(smem_u32(sm + C::kSmOnes), 16, 256, 6);
+    const uint64_t dones_d = make_sdesc(smem_u32(sm + C::kSmOnes + kBN * 32), 16, 256, 6);
+    const uint64_t dseed = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStSeed), 16, 256, 6);
     const uint64_t dsfds = sf_tile_desc(smem_u32(sm + C::kSmSFdS));
     bool ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 50);
     if (ok) {
@@ -331,16 +397,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
       tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
       tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
+      mma_bf16_ss_elect(tmem + C::kColS, dones_l, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < D / 32; ++kb)
         mma_mxf8_ss_elect(tmem + C::kColS, dk_ + 2 * kb, dq_ + so + 2 * kb,
                           idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
-                          tmem + C::kColSFQ + 2 * half, kb > 0);
+                          tmem + C::kColSFQ + 2 * half, 1);
+      mma_bf16_ss_elect(tmem + C::kColDP, dones_d, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < D / 32; ++kb)
         mma_mxf8_ss_elect(tmem + C::kColDP, dv_ + 2 * kb, ddo + so + 2 * kb,
                           idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
-                          tmem + C::kColSFdO + 2 * half, kb > 0);
+                          tmem + C::kColSFdO + 2 * half, 1);
       tc_commit_elect(&bars->st_ready);
       return true;
     };
@@ -460,26 +528,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (int i = 0; i < nsteps && ok; ++i) {
-      const int s = i % kStages;
       const int q0 = step_q0(i);
-      const uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
       ok = mbar_wait_sleep(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
       tc_fence_after();
       uint32_t rs[32], rd[32];
       tmem_ld32(tmem + lb + C::kColS + 32 * g, rs);
       tmem_ld32(tmem + lb + C::kColDP + 32 * g, rd);
-      float nlse2[32], ndlt[32];
-      {
-        const float4* l4 = reinterpret_cast<const float4*>(st + C::kStLse) + 8 * g;
-        const float4* d4 = reinterpret_cast<const float4*>(st + C::kStDelta) + 8 * g;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float4 a4 = l4[t], b4 = d4[t];
-          nlse2[4 * t] = a4.x; nlse2[4 * t + 1] = a4.y; nlse2[4 * t + 2] = a4.z; nlse2[4 * t + 3] = a4.w;
-          ndlt[4 * t] = b4.x; ndlt[4 * t + 1] = b4.y; ndlt[4 * t + 2] = b4.z; ndlt[4 * t + 3] = b4.w;
-        }
-      }
       tmem_ld_wait();
       // S^T / dP^T of this step are in registers: the next step's MMAs may go
       tc_fence_before();
@@ -491,14 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo = p.causal ? max(0, key - qb0) : 0;
       const int hi = key < w.len ? min(32, w.len - qb0) : 0;
       const bool all_visible = __all_sync(0xFFFFFFFFu, lo == 0 && hi == 32);
-      // x = s * c2 - LSE2, two elements per instruction (the workspace holds
-      // -LSE2 and -D); invisible entries get x = -inf, so P = 2^x = 0
+      // TMEM holds S^T - LSE / c (seeded accumulator), so x = s * c2 - LSE2
+      // is one multiply, two elements per instruction; invisible entries get
+      // x = -inf, so P = 2^x = 0
       const uint64_t c2x2 = pack2(p.scale_log2, p.scale_log2);
       float xv[32];
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const uint64_t x = fma2(pack2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])), c2x2,
-                                pack2(nlse2[j], nlse2[j + 1]));
+        const uint64_t x = mul2(pack2(__uint_as_float(rs[j]), __uint_as_float(rs[j + 1])), c2x2);
         xv[j] = lo2(x);
         xv[j + 1] = hi2(x);
       }
@@ -515,12 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ap_bits = warp_max_nonneg_bits(ex2(mx));
 #pragma unroll
       for (int j = 0; j < 32; ++j) pv[j] = ex2(xv[j]);
-      // dS = P (dP - D)
+      // dS = P (dP - D); TMEM holds dP^T - D (seeded accumulator)
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const uint64_t d = add2(pack2(__uint_as_float(rd[j]), __uint_as_float(rd[j + 1])),
-                                pack2(ndlt[j], ndlt[j + 1]));
-        const uint64_t ds = mul2(pack2(pv[j], pv[j + 1]), d);
+        const uint64_t ds = mul2(pack2(pv[j], pv[j + 1]),
+                                 pack2(__uint_as_float(rd[j]), __uint_as_float(rd[j + 1])));
         dsv[j] = lo2(ds);
         dsv[j + 1] = hi2(ds);
       }
