@@ -272,29 +272,70 @@ def run_lpfa(args, world, rank, local):
                 "dk": torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory(),
                 "dv": torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory()}
 
-    def e2e_step():
-        dq_, dk_, dv_ = None, None, None
-        qd, kd, vd, dod = (host[n].to(dev, non_blocking=True) for n in ("q", "k", "v", "do"))
+    # Copies overlap compute: inputs go up on their own stream into
+    # double-buffered device tensors (step i+1's inputs while step i runs), O
+    # comes back while the backward runs, dQ/dK/dV after it.  Every copy of
+    # every timed step is inside the timed region.
+    names = ("q", "k", "v", "do")
+    dev_in = [{n: torch.empty_like(host[n], device=dev) for n in names} for _ in range(2)]
+    cur = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    for e in in_free:
+        e.record(cur)
+
+    def upload(i):
+        b = i % 2
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(in_free[b])
+            for n in names:
+                dev_in[b][n].copy_(host[n], non_blocking=True)
+            in_ready[b].record(h2d_s)
+
+    def e2e_step(i, last):
+        b = i % 2
+        cur.wait_event(in_ready[b])
+        if not last:
+            upload(i + 1)
+        x_ = dev_in[b]
         shp = lambda t, h: t.view(B, S, h, D)
-        o_, lse_ = L.mx_attention_forward(shp(qd, H), shp(kd, Hkv), shp(vd, Hkv),
+        o_, lse_ = L.mx_attention_forward(shp(x_["q"], H), shp(x_["k"], Hkv), shp(x_["v"], Hkv),
                                           causal=w.causal, softmax_scale=w.softmax_scale,
                                           check=False)
-        dq_, dk_, dv_ = L.mx_attention_backward(shp(qd, H), shp(kd, Hkv), shp(vd, Hkv), o_,
-                                                shp(dod, H), lse_, causal=w.causal,
-                                                softmax_scale=w.softmax_scale, check=False)
-        out_host["o"].copy_(o_.view(T, H, D), non_blocking=True)
-        out_host["dq"].copy_(dq_.view(T, H, D), non_blocking=True)
-        out_host["dk"].copy_(dk_.view(T, Hkv, D), non_blocking=True)
-        out_host["dv"].copy_(dv_.view(T, Hkv, D), non_blocking=True)
+        o_done = torch.cuda.Event()
+        o_done.record(cur)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(o_done)
+            o_.record_stream(d2h_s)
+            out_host["o"].copy_(o_.view(T, H, D), non_blocking=True)
+        dq_, dk_, dv_ = L.mx_attention_backward(shp(x_["q"], H), shp(x_["k"], Hkv),
+                                                shp(x_["v"], Hkv), o_, shp(x_["do"], H), lse_,
+                                                causal=w.causal, softmax_scale=w.softmax_scale,
+                                                check=False)
+        in_free[b].record(cur)
+        g_done = torch.cuda.Event()
+        g_done.record(cur)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(g_done)
+            for t_, n in ((dq_, "dq"), (dk_, "dk"), (dv_, "dv")):
+                t_.record_stream(d2h_s)
+                out_host[n].copy_(t_.view(out_host[n].shape), non_blocking=True)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_run(nsteps):
+        upload(0)
+        for i in range(nsteps):
+            e2e_step(i, i == nsteps - 1)
+        done = torch.cuda.Event()
+        done.record(d2h_s)
+        cur.wait_event(done)
+
+    e2e_run(max(1, args.warmup))
     torch.cuda.synchronize()
     _barrier(world)
     e0, e1 = ev(), ev()
     e0.record()
-    for _ in range(args.steps):
-        e2e_step()
+    e2e_run(args.steps)
     e1.record()
     torch.cuda.synchronize()
     clk.__exit__(None, None, None)
