@@ -46,6 +46,7 @@ namespace {
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
 constexpr int kStages = 5;   // Q / dO ring: loads run several steps ahead
+constexpr int kDqBufs = 4;   // dQ staging tiles per compute warp (reduce-adds in flight)
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 
@@ -87,9 +88,10 @@ struct BwdCfg {
   // constant A operands of the seed MMAs: [128 keys][16 bf16], 32-byte
   // swizzle, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
   static constexpr int kSmOnes = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
-  // dQ staging: per compute warp two [32 queries][32 channels] fp16 tiles
+  // dQ staging: per compute warp kDqBufs [32 queries][32 channels] fp16
+  // tiles, 64-byte rows, 64B swizzle (2 KB each, 1024-aligned)
   static constexpr int kSmDQ = kSmOnes + 2 * kBN * 32;
-  static constexpr int kSmBar = kSmDQ + 8 * 2 * 32 * 32 * 2;
+  static constexpr int kSmBar = kSmDQ + 8 * kDqBufs * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
 };
 
@@ -491,23 +493,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->kt_ready);
     }
     // dQ^T(j) of this warp (32 channels x this warpgroup's 32 queries, fp32)
-    // -> fp16 [query][channel] tile in the warp's own shared-memory buffer
-    // -> one tensor reduce-add into global dQ, issued by lane 0 (bulk async
-    // groups belong to the issuing thread).  No other warp takes part.
+    // -> fp16 [query][channel] tile in one of the warp's own shared-memory
+    // buffers -> one tensor reduce-add into global dQ, issued by lane 0
+    // (bulk async groups belong to the issuing thread).  No other warp takes
+    // part.  The values arrive in the accumulator-fragment arrangement
+    // (16x256b loads: rq[16h + 4k + 2s + e] = channel 16h + 8s + lane/4,
+    // query 8k + 2(lane%4) + e), which is what a transposing stmatrix takes:
+    // one instruction writes the four 8-channel blocks of 8 queries.
     auto stage_dq = [&](int j, const uint32_t (&rq)[32]) {
       if (quad * 32 >= D) return;                  // no channels here (D = 64)
       const int hj = step_head(j), q0j = step_q0(j);
-      uint32_t* stg = reinterpret_cast<uint32_t*>(sm + C::kSmDQ + (warp - 2) * 4096 + (j & 1) * 2048);
-      if (lane == 0) bulk_wait_read_le1();        // step j-2's reduce has read it
+      uint8_t* stg = sm + C::kSmDQ + ((warp - 2) * kDqBufs + j % kDqBufs) * 2048;
+      if (lane == 0) bulk_wait_read_le3();        // step j-4's reduce has read it
       __syncwarp();
-      // lane = channel: each query row of the tile is 32 consecutive halves
-      __half* stg16 = reinterpret_cast<__half*>(stg);
       const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
+      const uint32_t sbase = smem_u32(stg);
+      const int cb = lane >> 3;                   // channel block whose row this lane addresses
 #pragma unroll
-      for (int e = 0; e < 32; e += 2) {
-        const uint64_t v = mul2(pack2(__uint_as_float(rq[e]), __uint_as_float(rq[e + 1])), mul);
-        stg16[e * 32 + lane] = __float2half_rn(lo2(v));
-        stg16[(e + 1) * 32 + lane] = __float2half_rn(hi2(v));
+      for (int k = 0; k < 4; ++k) {
+        uint32_t hv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {             // matrix i = channel block 2h + s
+          const int r = 16 * (i >> 1) + 4 * k + 2 * (i & 1);
+          const uint64_t v = mul2(pack2(__uint_as_float(rq[r]), __uint_as_float(rq[r + 1])), mul);
+          const __half2 h2 = __floats2half2_rn(lo2(v), hi2(v));
+          hv[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        const int q = 8 * k + (lane & 7);         // query row addressed by this lane
+        stmatrix_x4_trans(sbase + q * 64 + 16 * (cb ^ ((q >> 1) & 3)), hv[0], hv[1], hv[2], hv[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -523,7 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // every MMA of step j has completed: its Q / dO stage may be refilled
       if (ctid == 0) mbar_arrive(&bars->q_empty[j % kStages]);
-      tmem_ld32(tmem + lb + C::kColDQ + 32 * g, rq);
+      tmem_ld_16x256b_x4(tmem + lb + C::kColDQ + 32 * g, rq);
+      tmem_ld_16x256b_x4(tmem + lb + (16u << 16) + C::kColDQ + 32 * g, rq + 16);
       tmem_ld_wait();
       return true;
     };
@@ -812,7 +826,7 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
     uint64_t strides[2] = {static_cast<uint64_t>(D * 2), static_cast<uint64_t>(hq * D * 2)};
     uint32_t box[3] = {32u, 1u, 32u};   // one warp's [32 queries][32 channels]
     if ((st = encode_tmap(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, dq, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_NONE)) != LPFA_OK)
+                          CU_TENSOR_MAP_SWIZZLE_64B)) != LPFA_OK)
       return st;
   }
 

@@ -205,8 +205,22 @@ __device__ __forceinline__ void bulk_wait_read0() {
 __device__ __forceinline__ void bulk_wait_read_le1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
+// At most three committed bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_le3() {
+  asm volatile("cp.async.bulk.wait_group.read 3;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Four 8x8 16-bit matrices to shared memory, transposed: lanes 8i..8i+7
+// give the addresses of the 8 rows of matrix i; register ri of thread t holds
+// its elements (t/4, 2(t%4)) and (t/4, 2(t%4)+1), which land in rows
+// 2(t%4), 2(t%4)+1 at column t/4.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1,
+                                                  uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};"
+               :: "r"(saddr), "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -485,6 +499,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+
+// 16x256b shape, four repetitions along columns: thread t gets, for
+// repetition k (columns 8k..8k+7 from taddr), r[4k], r[4k+1] = lane
+// base + t/4, columns 8k + 2(t%4) + {0, 1}, and r[4k+2], r[4k+3] = the same
+// columns of lane base + 8 + t/4 (the accumulator-fragment arrangement)
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
         "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
