@@ -139,10 +139,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 struct KvItem {
   int seq, ktile, kvh;
   int64_t start;
@@ -500,14 +496,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (16x256b loads: rq[16h + 4k + 2s + e] = channel 16h + 8s + lane/4,
     // query 8k + 2(lane%4) + e), which is what a transposing stmatrix takes:
     // one instruction writes the four 8-channel blocks of 8 queries.
-    auto stage_dq = [&](int j, const uint32_t (&rq)[32]) {
+    // Staging is split so that one proxy fence covers both this step's dS^T
+    // tile and the previous step's dQ tile: stage_dq_store writes the tile
+    // (slot j % kDqBufs), stage_dq_issue sends it after the fence.
+    auto stage_dq_store = [&](int j, const uint32_t (&rq)[32]) {
       if (quad * 32 >= D) return;                  // no channels here (D = 64)
-      const int hj = step_head(j), q0j = step_q0(j);
-      uint8_t* stg = sm + C::kSmDQ + ((warp - 2) * kDqBufs + j % kDqBufs) * 2048;
+      const uint32_t sbase = smem_u32(sm + C::kSmDQ + ((warp - 2) * kDqBufs + (j & (kDqBufs - 1))) * 2048);
       if (lane == 0) bulk_wait_read_le3();        // step j-4's reduce has read it
       __syncwarp();
       const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
-      const uint32_t sbase = smem_u32(stg);
       const int cb = lane >> 3;                   // channel block whose row this lane addresses
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -522,12 +519,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = 8 * k + (lane & 7);         // query row addressed by this lane
         stmatrix_x4_trans(sbase + q * 64 + 16 * (cb ^ ((q >> 1) & 3)), hv[0], hv[1], hv[2], hv[3]);
       }
-      fence_proxy_async_smem();
-      __syncwarp();
+    };
+    auto stage_dq_issue = [&](int j, int hj, int q0j) {
+      if (quad * 32 >= D) return;
       if (lane == 0) {
         // rows of the step beyond the sequence carry exact zeros
         tma_reduce_add_3d(&tma_dq, 32 * quad, hj, static_cast<int32_t>(w.start + q0j + 32 * g),
-                          stg);
+                          sm + C::kSmDQ + ((warp - 2) * kDqBufs + (j & (kDqBufs - 1))) * 2048);
         bulk_commit();
       }
     };
@@ -541,8 +539,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       return true;
     };
+    // (query head, first query) of step i and of step i-1, advanced without
+    // divisions
+    int cur_h = w.kvh * p.group, cur_qs = qstep0, prev_h = 0, prev_q0 = 0;
     for (int i = 0; i < nsteps && ok; ++i) {
-      const int q0 = step_q0(i);
+      const int q0 = cur_qs * kBQ;
       ok = mbar_wait_sleep(&bars->st_ready, i & 1, p.err, abort, 60);
       if (!ok) break;
       tc_fence_after();
@@ -626,17 +627,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // B-operand scale of dQ^T: (query n = 32 g + lane, key block quad)
       sm[C::kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
+      if (i > 0) stage_dq_store(i - 1, rq);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->ds_ready);
-      if (i > 0) stage_dq(i - 1, rq);
+      if (i > 0) stage_dq_issue(i - 1, prev_h, prev_q0);
+      prev_h = cur_h;
+      prev_q0 = q0;
+      if (++cur_qs == nqsteps) {
+        cur_qs = qstep0;
+        ++cur_h;
+      }
     }
     if (ok && nsteps > 0) {
       uint32_t rq[32];
       ok = read_dq(nsteps - 1, rq);
-      if (ok) stage_dq(nsteps - 1, rq);
+      if (ok) {
+        stage_dq_store(nsteps - 1, rq);
+        fence_proxy_async_smem();
+        __syncwarp();
+        stage_dq_issue(nsteps - 1, prev_h, prev_q0);
+      }
     }
     if (lane == 0) bulk_wait0();
     // epilogue: warpgroup 0 writes dK (times softmax_scale), 1 writes dV
