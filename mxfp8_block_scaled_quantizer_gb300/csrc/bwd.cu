@@ -30,7 +30,7 @@
 // soon as step i's rows are in registers, and a warpgroup reads back dQ^T of
 // step i-1 after computing step i, so the MMAs of one step overlap the
 // elementwise work of the next.
-//   [448,512) scale factors (see kCol* below)
+//   [448,512) scale factors and the seed MMAs' constant A tiles (kCol* below)
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -64,6 +64,9 @@ struct BwdCfg {
                             kColSFdO = kColSF + 16, kColSFQt = kColSF + 20,
                             kColSFdOt = kColSF + 24, kColSFP = kColSF + 28 /* +4g */,
                             kColSFdS = kColSF + 36 /* +4g */, kColSFdSB = kColSF + 44;
+  // constant A operands of the seed MMAs: [128 keys][16 bf16], 8 columns
+  // each, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
+  static constexpr uint32_t kColOnesL = kColSF + 48, kColOnesD = kColSF + 56;
   // shared memory (bytes from a 1024-aligned base)
   static constexpr int kSmK = 0;                                  // 128 x D (SW D)
   static constexpr int kSmV = (kBN * D + 1023) / 1024 * 1024;     // 128 x D
@@ -85,12 +88,9 @@ struct BwdCfg {
   static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes; // 128 x 64 B (SW64)
   static constexpr int kSmSFdS = kSmDS + kBN * kBQ;               // 512 B
   static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
-  // constant A operands of the seed MMAs: [128 keys][16 bf16], 32-byte
-  // swizzle, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
-  static constexpr int kSmOnes = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
   // dQ staging: per compute warp kDqBufs [32 queries][32 channels] fp16
   // tiles, 64-byte rows, 64B swizzle (2 KB each, 1024-aligned)
-  static constexpr int kSmDQ = kSmOnes + 2 * kBN * 32;
+  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
   static constexpr int kSmBar = kSmDQ + 8 * kDqBufs * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
 };
@@ -245,6 +245,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  // the seed MMAs' constant A operands (one warpgroup covers the 128 lanes)
+  if (warp >= 2 && warp < 6) {
+    const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t one2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
+    const uint32_t ol[8] = {one2, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    const uint32_t od[8] = {0u, one2, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st8(tmem + lanes + C::kColOnesL, ol);
+    tmem_st8(tmem + lanes + C::kColOnesD, od);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   // step i -> (query head, first query of the step)
   auto step_head = [&](int i) { return w.kvh * p.group + i / steps_per_head; };
@@ -269,19 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bulk_load_elect(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
     bulk_load_elect(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
     bulk_load_elect(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
-    // Constant "ones" operands and zeroed seed tiles (32-byte swizzle: the
-    // 16-byte half k/8 of row r sits at half (k/8) ^ ((r >> 2) & 1)).  The
-    // first q_full arrival below publishes them to the tensor pipe.
+    // Zeroed seed tiles (32-byte swizzle: the 16-byte half k/8 of row r
+    // sits at half (k/8) ^ ((r >> 2) & 1)).  The first q_full arrival below
+    // publishes them to the tensor pipe.
     {
-      uint32_t* ones = reinterpret_cast<uint32_t*>(sm + C::kSmOnes);
-      for (int i = lane; i < 2 * kBN * 8; i += 32) {
-        const int t = i / (kBN * 8), r = (i / 8) % kBN, wd = i % 8;   // word wd of row r
-        const int lhalf = (wd >> 2) ^ ((r >> 2) & 1);                    // logical half
-        // bf16 pair (1.0, 1.0) in logical word 0 (k = 0, 1) of the LSE tile
-        // and logical word 1 (k = 2, 3) of the D tile
-        const bool one = lhalf == 0 && (wd & 3) == t;
-        ones[i] = one ? 0x3F803F80u : 0u;
-      }
       for (int st = 0; st < kStages; ++st) {
         uint32_t* seed = reinterpret_cast<uint32_t*>(sm + C::kSmStage0 + st * C::kStageBytes + C::kStSeed);
         for (int i = lane; i < kBQ * 8; i += 32) seed[i] = 0u;
@@ -376,8 +380,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSmStage0 + C::kStSF));
     // seed MMAs (bf16, K = 16): S^T <- -LSE / c, dP^T <- -D, broadcast over keys
     constexpr uint32_t id_seed = idesc_bf16(128, kBQ, 0, 0);
-    const uint64_t dones_l = make_sdesc(smem_u32(sm + C::kSmOnes), 16, 256, 6);
-    const uint64_t dones_d = make_sdesc(smem_u32(sm + C::kSmOnes + kBN * 32), 16, 256, 6);
     const uint64_t dseed = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStSeed), 16, 256, 6);
     const uint64_t dsfds = sf_tile_desc(smem_u32(sm + C::kSmSFdS));
     bool ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 50);
@@ -395,13 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
       tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
       tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
-      mma_bf16_ss_elect(tmem + C::kColS, dones_l, dseed + so, id_seed, 0);
+      mma_bf16_ts_elect(tmem + C::kColS, tmem + C::kColOnesL, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < D / 32; ++kb)
         mma_mxf8_ss_elect(tmem + C::kColS, dk_ + 2 * kb, dq_ + so + 2 * kb,
                           idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
                           tmem + C::kColSFQ + 2 * half, 1);
-      mma_bf16_ss_elect(tmem + C::kColDP, dones_d, dseed + so, id_seed, 0);
+      mma_bf16_ts_elect(tmem + C::kColDP, tmem + C::kColOnesD, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < D / 32; ++kb)
         mma_mxf8_ss_elect(tmem + C::kColDP, dv_ + 2 * kb, ddo + so + 2 * kb,
