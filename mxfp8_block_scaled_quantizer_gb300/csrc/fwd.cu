@@ -16,11 +16,17 @@
 //   O += P V            block-scaled MMA, P read from TMEM as the A operand
 //   epilogue            O / l -> bf16, LSE = (m + log2 l) ln 2
 //
-// CTA = one 128-query tile of one (sequence, head); key/value tiles of 256.
+// Persistent: one CTA per SM walks work items (a 128-query tile of one
+// (sequence, head)) in "snake" order (round r takes items r*G .. r*G+G-1,
+// left to right on even rounds and right to left on odd ones), which
+// balances heavy and light causal tiles across CTAs; key/value tiles of 256.
+// Every barrier phase runs on across items, so the next item's Q, K/V loads
+// and first S MMA overlap the current item's last tile and epilogue.
 // Warp roles:
-//   warp 0     TMA producer: Q once, then K_j, V_j and their scale tiles
-//              through a shared-memory ring.
-//   warp 1     TMEM owner and MMA issuer (one thread).
+//   warp 0     TMA producer: per item Q, then K_j, V_j and their scale
+//              tiles through a shared-memory ring.
+//   warp 1     TMEM owner and issuer of the S = Q K^T MMAs.
+//   warp 10    issuer of the O += P V MMAs.
 //   warps 2-9  softmax: warps 2-5 take keys [0,128) of every tile, warps 6-9
 //              keys [128,256); thread = query row = TMEM lane.  The two
 //              threads of a row exchange their partial maxima (and, at the
@@ -68,6 +74,7 @@ struct FwdParams {
   uint32_t* err;
   int32_t hq, hkv, group;
   int32_t nq;           // dense: query tiles per sequence
+  int64_t nitems;       // work items (some may be empty: varlen tails)
   int32_t causal;
   float scale_log2;     // softmax_scale * log2(e)
   float threshold;      // log2 units
@@ -92,6 +99,7 @@ struct FwdCfg {
 template <int S>
 struct FwdBars {
   uint64_t q_full;
+  uint64_t q_empty;    // an item's last S MMA complete (MMA commit)
   uint64_t kv_full[S];
   uint64_t kv_empty[S];
   uint64_t s_full;     // S_j in TMEM (MMA commit)
@@ -123,10 +131,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Work item of this CTA: (sequence, q tile, head).  Items that share a key
-// head are consecutive (their K/V tiles stay in L2 while the CTAs that read
-// them run) and, for dense causal inputs, the heavy (late) q tiles of a
-// group come first.
+// Work item idx: (sequence, q tile, head).  Items that share a key head are
+// consecutive (their K/V tiles stay in L2 while the CTAs that read them run)
+// and, for dense causal inputs, the heavy (late) q tiles of a group come
+// first.
 struct WorkItem {
   int seq, qtile, head;
   int64_t start;          // first token of the sequence
@@ -134,8 +142,7 @@ struct WorkItem {
   int64_t sf_tile;        // padded 128-row tile index of the q tile
 };
 
-__device__ __forceinline__ bool work_item(const FwdParams& p, WorkItem& w) {
-  const int64_t idx = blockIdx.x;
+__device__ __forceinline__ bool work_item(const FwdParams& p, int64_t idx, WorkItem& w) {
   const int grp = p.group;
   int kvh;
   if (p.seqs.cu_seqlens == nullptr) {
@@ -164,6 +171,21 @@ __device__ __forceinline__ bool work_item(const FwdParams& p, WorkItem& w) {
   return w.qtile * kBlockM < w.len;
 }
 
+// Item of round r for this CTA in snake order; -1 once the rounds run out.
+__device__ __forceinline__ int64_t round_item(const FwdParams& p, int r) {
+  const int64_t g = gridDim.x;
+  const int64_t idx = static_cast<int64_t>(r) * g +
+                      ((r & 1) ? (g - 1 - blockIdx.x) : static_cast<int64_t>(blockIdx.x));
+  return idx < p.nitems ? idx : -1;
+}
+
+// Key/value tiles of an item.
+__device__ __forceinline__ int item_tiles(const FwdParams& p, const WorkItem& w) {
+  const int q0 = w.qtile * kBlockM;
+  const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
+  return (kv_len + kBlockN - 1) / kBlockN;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_attn_fwd_kernel(const __grid_constant__ CUtensorMap tma_q,
@@ -182,15 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  WorkItem w;
-  if (!work_item(p, w)) return;                    // uniform for the CTA
-  const int kvh = w.head / p.group;
-  const int q0 = w.qtile * kBlockM;                // first query of the tile
-  const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
-  const int ntiles = (kv_len + kBlockN - 1) / kBlockN;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
@@ -214,6 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Every role walks the same item sequence and counts the same key/value
+  // tiles (gt) and items (k); barrier phases follow those counts.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // The whole warp runs the loop (converged); an elected lane issues the
@@ -223,45 +242,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tma_k);
       tma_prefetch_desc(&tma_v);
     }
-    mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
-    tma_load_3d_elect(sm + C::kQ, &tma_q, 0, w.head, static_cast<int32_t>(w.start + q0),
-                   &bars->q_full);
-    bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
-                 &bars->q_full);
-    // scale tiles of keys past the sequence's padded rows belong to the
-    // next sequence (finite, and their keys are masked); past the tensor
-    // the last tile stands in
-    const int64_t kv_sf0 = w.sf_tile - w.qtile;
     const int64_t sf_last = p.seqs.total_sf_rows / 128 - 1;
     bool ok = true;
+    int gt = 0, k = 0, q_issued = -1;
     int issued[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
-    for (int j = 0; j < ntiles; ++j) {
-      const int s = j % kStages;
-      const uint32_t ph = (j / kStages) & 1;
-      ok = mbar_wait_sleep(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
-      if (!ok) break;
-      uint8_t* kbuf = sm + C::kStage0 + s * C::kStageBytes;
-      uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
-      uint64_t* bar = &bars->kv_full[s];
-      mbar_arrive_expect_tx_elect(bar, 2 * C::kKVBytes + 2048);
-      const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
-      tma_load_3d_elect(kbuf, &tma_k, 0, kvh, row_k, bar);
-      tma_load_3d_elect(kbuf + C::kKVBytes, &tma_v, 0, kvh, row_k, bar);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t t = min(kv_sf0 + 2 * j + h, sf_last);
-        const int64_t off = (t * p.hkv + kvh) * 512;
-        bulk_load_elect(sfb + 512 * h, p.sfk + off, 512, bar);
-        bulk_load_elect(sfb + 1024 + 512 * h, p.sfv + off, 512, bar);
+    for (int r = 0; ok; ++r) {
+      const int64_t idx = round_item(p, r);
+      if (idx < 0) break;
+      WorkItem w;
+      if (!work_item(p, idx, w)) continue;
+      const int kvh = w.head / p.group;
+      const int q0 = w.qtile * kBlockM;
+      const int ntiles = item_tiles(p, w);
+      // the Q tile (and its scale tile) is free once the previous item's
+      // last S MMA has completed
+      if (k > 0) {
+        ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11);
+        if (!ok) break;
       }
-      issued[s] = static_cast<int>(ph);
+      mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
+      tma_load_3d_elect(sm + C::kQ, &tma_q, 0, w.head, static_cast<int32_t>(w.start + q0),
+                        &bars->q_full);
+      bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
+                      &bars->q_full);
+      q_issued = k & 1;
+      ++k;
+      // scale tiles of keys past the sequence's padded rows belong to the
+      // next sequence (finite, and their keys are masked); past the tensor
+      // the last tile stands in
+      const int64_t kv_sf0 = w.sf_tile - w.qtile;
+      for (int j = 0; j < ntiles; ++j, ++gt) {
+        const int s = gt % kStages;
+        const uint32_t ph = (gt / kStages) & 1;
+        ok = mbar_wait_sleep(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
+        if (!ok) break;
+        uint8_t* kbuf = sm + C::kStage0 + s * C::kStageBytes;
+        uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
+        uint64_t* bar = &bars->kv_full[s];
+        mbar_arrive_expect_tx_elect(bar, 2 * C::kKVBytes + 2048);
+        const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
+        tma_load_3d_elect(kbuf, &tma_k, 0, kvh, row_k, bar);
+        tma_load_3d_elect(kbuf + C::kKVBytes, &tma_v, 0, kvh, row_k, bar);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t t = min(kv_sf0 + 2 * j + h, sf_last);
+          const int64_t off = (t * p.hkv + kvh) * 512;
+          bulk_load_elect(sfb + 512 * h, p.sfk + off, 512, bar);
+          bulk_load_elect(sfb + 1024 + 512 * h, p.sfv + off, 512, bar);
+        }
+        issued[s] = static_cast<int>(ph);
+      }
     }
     if (!ok) {
       for (int s = 0; s < kStages; ++s)
         if (issued[s] >= 0)
           mbar_wait_sleep(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
-      mbar_wait_sleep(&bars->q_full, 0, nullptr, nullptr, 0);
+      if (q_issued >= 0)
+        mbar_wait_sleep(&bars->q_full, static_cast<uint32_t>(q_issued), nullptr, nullptr, 0);
     }
   } else if (warp == 1 || warp == 10) {
     // --------------------------------------------------------- MMA issuers
@@ -271,28 +309,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // them.  Warp 1 issues S = Q K^T, warp 10 (another scheduler) issues
     // O += P V; the two write disjoint TMEM columns (S | O, SFQ SFK | SFP
     // SFV), so their instructions need no mutual order.  Each warp runs its
-    // loop converged and an elected lane issues.  Descriptors of stage 0 are built
-    // once; a stage adds its byte offset / 16 and a K-step 32 bytes (S
+    // loop converged and an elected lane issues.  Descriptors of stage 0 are
+    // built once; a stage adds its byte offset / 16 and a K-step 32 bytes (S
     // operands) or 32 rows of V to the 14-bit address field, which never
-    // carries (shared memory addresses stay below 256 KB).  The key loop is
-    // unrolled by the ring depth so that stage indices are constants.
+    // carries (shared memory addresses stay below 256 KB).
     const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSfStage0));
     bool ok = true;
+    int gt = 0, k = 0;
     if (warp == 1) {
       constexpr uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
       const uint64_t dq = make_sdesc(smem_u32(sm + C::kQ), 16, kSbo, kSw);
       const uint64_t dk = make_sdesc(smem_u32(sm + C::kStage0), 16, kSbo, kSw);
       const uint32_t tS = tmem + kColS, tSFQ = tmem + kColSFQ, tSFK = tmem + kColSFK;
-      ok = mbar_wait_sleep(&bars->q_full, 0, p.err, abort, 20);
-      if (ok) {
-        tc_fence_after();
-        tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
-      }
-      // S = Q K_j^T (N = 256: two 128-key scale tiles side by side); S_j
-      // may be overwritten once every softmax warp holds its row of S_{j-1}
-      auto issue_s = [&](int j, int s) -> bool {
-        if (j > 0 && !mbar_wait_sleep(&bars->s_free, (j - 1) & 1, p.err, abort, 23)) return false;
-        if (!mbar_wait_sleep(&bars->kv_full[s], (j / kStages) & 1, p.err, abort, 21)) return false;
+      // S = Q K^T (N = 256: two 128-key scale tiles side by side); S may be
+      // overwritten once every softmax warp holds its row of the previous S
+      auto issue_s = [&](int g) -> bool {
+        const int s = g % kStages;
+        if (g > 0 && !mbar_wait_sleep(&bars->s_free, (g - 1) & 1, p.err, abort, 23)) return false;
+        if (!mbar_wait_sleep(&bars->kv_full[s], (g / kStages) & 1, p.err, abort, 21)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
         const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
@@ -301,27 +335,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < D / 32; ++kb)
           mma_mxf8_ss_elect(tS, dq + 2 * kb, dk + so + 2 * kb,
-                         idesc_sf_ids(idesc_s, kb, kb), tSFQ, tSFK, kb > 0);
+                            idesc_sf_ids(idesc_s, kb, kb), tSFQ, tSFK, kb > 0);
         tc_commit_elect(&bars->s_full);
         return true;
       };
-      for (int j0 = 0; j0 < ntiles && ok; j0 += kStages) {
-#pragma unroll
-        for (int ss = 0; ss < kStages; ++ss) {
-          const int j = j0 + ss;                   // j % kStages == ss
-          if (ok && j < ntiles) ok = issue_s(j, ss);
-        }
+      for (int r = 0; ok; ++r) {
+        const int64_t idx = round_item(p, r);
+        if (idx < 0) break;
+        WorkItem w;
+        if (!work_item(p, idx, w)) continue;
+        const int ntiles = item_tiles(p, w);
+        ok = mbar_wait_sleep(&bars->q_full, k & 1, p.err, abort, 20);
+        if (!ok) break;
+        tc_fence_after();
+        tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) ok = issue_s(gt);
+        // the item's last reader of the Q tile is issued: the tile is free
+        // once it completes
+        if (ok) tc_commit_elect(&bars->q_empty);
+        ++k;
       }
     } else {
       constexpr uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
       const uint64_t dv = make_sdesc(smem_u32(sm + C::kStage0 + C::kKVBytes), 16, kSbo, kSw);
       const uint32_t tO = tmem + kColO, tP = tmem + kColP;
       const uint32_t tSFP = tmem + kColSFP, tSFV = tmem + kColSFV;
-      // O += P_j V_j over 256 keys (8 K-steps; scale group = K-step / 4);
-      // V_j landed before S_j could be computed, and P_j is written after
-      // the softmax saw S_j, so P-full orders both
-      auto issue_pv = [&](int j, int s) -> bool {
-        if (!mbar_wait_sleep(&bars->p_full, j & 1, p.err, abort, 22)) return false;
+      // O (+)= P V over 256 keys (8 K-steps; scale group = K-step / 4); V
+      // landed before its S could be computed, and P is written after the
+      // softmax saw S, so P-full orders both.  An item's first PV overwrites
+      // O: its P-full comes after the softmax read the previous item's O.
+      auto issue_pv = [&](int g, bool first) -> bool {
+        const int s = g % kStages;
+        if (!mbar_wait_sleep(&bars->p_full, g & 1, p.err, abort, 22)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
         const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
@@ -330,17 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < kBlockN / 32; ++kb)
           mma_mxf8_ts_elect(tO, tP + 8 * kb, dv + so + kb * ((32 * D) >> 4),
-                         idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
-                         tSFV + 4 * (kb >> 2), (j > 0) || (kb > 0));
+                            idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
+                            tSFV + 4 * (kb >> 2), (!first) || (kb > 0));
         tc_commit_elect(&bars->pv_done);
         return true;
       };
-      for (int j0 = 0; j0 < ntiles && ok; j0 += kStages) {
-#pragma unroll
-        for (int ss = 0; ss < kStages; ++ss) {
-          const int j = j0 + ss;
-          if (ok && j < ntiles) ok = issue_pv(j, ss);
-        }
+      for (int r = 0; ok; ++r) {
+        const int64_t idx = round_item(p, r);
+        if (idx < 0) break;
+        WorkItem w;
+        if (!work_item(p, idx, w)) continue;
+        const int ntiles = item_tiles(p, w);
+        for (int j = 0; j < ntiles && ok; ++j, ++gt) ok = issue_pv(gt, j == 0);
       }
     }
     if (!ok) *abort = 1;
@@ -352,7 +398,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wg = (warp - 2) >> 2;               // key half of every tile
     const int quad = warp & 3;                    // TMEM lane quarter
     const int row = quad * 32 + lane;             // query row within tile
-    const int qi = q0 + row;                      // query index in sequence
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tSrow = tmem + kColS + kHalfN * wg + lane_base;
     float* xmax = reinterpret_cast<float*>(sm + C::kXMax);   // [2][2][128]
@@ -360,161 +405,175 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* xbar = &bars->xchg[quad];
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = pack2(c2, c2);
-    float m_ref = -INFINITY;                      // log2 units
-    float l = 0.f;                                // this half's partial sum
     bool ok = true;
-    const int lim = p.causal ? min(w.len, qi + 1) : w.len;   // keys < lim visible
-    int j = 0;
-    for (; j < ntiles && ok; ++j) {
-      ok = mbar_wait_sleep(&bars->s_full, j & 1, p.err, abort, 30);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tSrow + 32 * c, sv[c]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free);
-      const int k0 = j * kBlockN + wg * kHalfN;
-      const bool need_mask = (k0 + kHalfN > w.len) || (p.causal && k0 + kHalfN - 1 > q0);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (k0 + 32 * c + e >= lim) sv[c][e] = __float_as_uint(-INFINITY);
-      }
-      // chunk maxima of the raw logits (c2 > 0 keeps the order)
-      float cmax[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float a = __uint_as_float(sv[c][0]);
-#pragma unroll
-        for (int e = 1; e < 31; e += 2)
-          a = max3(a, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
-        cmax[c] = fmaxf(a, __uint_as_float(sv[c][31]));
-      }
-      // row maximum over both halves
-      const float hmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
-      float* xm = xmax + (j & 1) * 256;
-      xm[wg * 128 + row] = hmax;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xbar);
-      ok = mbar_wait_sleep(xbar, j & 1, p.err, abort, 33);
-      if (!ok) break;
-      const float tmax = fmaxf(hmax, xm[(1 - wg) * 128 + row]);
-      const float mt = __fmul_rn(tmax, c2);
-      float m_new = m_ref;
-      if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
-      const bool moved = (m_new != m_ref);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
-      // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
-      uint32_t code[4];
-      uint32_t sfp = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
-        code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
-        sfp |= code[c] << (8 * c);
-      }
-      // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
-      // the scaled values per block and rescales by 2^e
-      uint32_t pw[32];
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e = static_cast<int>(code[c]) - 127;
-        const float nb = -(m_use + static_cast<float>(e));
-        const uint64_t nb2 = pack2(nb, nb);
-        uint64_t acc = 0;
-#pragma unroll
-        for (int k = 0; k < 16; k += 2) {
-          const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][2 * k]), __uint_as_float(sv[c][2 * k + 1])), c2x2, nb2);
-          const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][2 * k + 2]), __uint_as_float(sv[c][2 * k + 3])), c2x2, nb2);
-          const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
-          const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
-          acc = add2(acc, pack2(p0, p1));
-          acc = add2(acc, pack2(p2, p3));
-          pw[8 * c + k / 2] = cvt_e4m3x4(p0, p1, p2, p3);
-        }
-        // 2^e as fp32 (e in [-127, 119]; 2^-127 flushes to 0, harmless: such
-        // blocks hold only zeros)
-        const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
-        lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
-      }
-      // P_{j-1} must be consumed before P_j overwrites it (and O is stable
-      // only between PV_{j-1} and PV_j)
-      if (j > 0) {
-        ok = mbar_wait_sleep(&bars->pv_done, (j - 1) & 1, p.err, abort, 31);
+    int gt = 0;                                   // tiles so far (all items)
+    int gx = 0;                                   // row-pair exchanges so far
+    for (int r = 0; ok; ++r) {
+      const int64_t idx = round_item(p, r);
+      if (idx < 0) break;
+      WorkItem w;
+      if (!work_item(p, idx, w)) continue;
+      const int q0 = w.qtile * kBlockM;
+      const int ntiles = item_tiles(p, w);
+      const int qi = q0 + row;                    // query index in sequence
+      float m_ref = -INFINITY;                    // log2 units
+      float l = 0.f;                              // this half's partial sum
+      const int lim = p.causal ? min(w.len, qi + 1) : w.len;   // keys < lim visible
+      for (int j = 0; j < ntiles && ok; ++j, ++gt) {
+        ok = mbar_wait_sleep(&bars->s_full, gt & 1, p.err, abort, 30);
         if (!ok) break;
         tc_fence_after();
-        // S_{j-1} and PV_{j-1} are done: their K/V stage may be refilled
-        if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(j - 1) % kStages]);
-      }
-      tmem_st32(tmem + kColP + 32 * wg + lane_base, pw);
-      tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
-      // selective rescale of O (and l): only warps holding a moved row; each
-      // half rescales half of the columns
-      if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
-        uint32_t r[32];
-#pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          const uint32_t ta = tmem + kColO + (D / 2) * wg + 32 * c + lane_base;
-          tmem_ld32(ta, r);
-          tmem_ld_wait();
+        uint32_t sv[4][32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tmem_st32(ta, r);
+        for (int c = 0; c < 4; ++c) tmem_ld32(tSrow + 32 * c, sv[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free);
+        const int k0 = j * kBlockN + wg * kHalfN;
+        const bool need_mask = (k0 + kHalfN > w.len) || (p.causal && k0 + kHalfN - 1 > q0);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (k0 + 32 * c + e >= lim) sv[c][e] = __float_as_uint(-INFINITY);
         }
+        // chunk maxima of the raw logits (c2 > 0 keeps the order)
+        float cmax[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float a = __uint_as_float(sv[c][0]);
+#pragma unroll
+          for (int e = 1; e < 31; e += 2)
+            a = max3(a, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+          cmax[c] = fmaxf(a, __uint_as_float(sv[c][31]));
+        }
+        // row maximum over both halves
+        const float hmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+        float* xm = xmax + (gx & 1) * 256;
+        xm[wg * 128 + row] = hmax;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xbar);
+        ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 33);
+        if (!ok) break;
+        ++gx;
+        const float tmax = fmaxf(hmax, xm[(1 - wg) * 128 + row]);
+        const float mt = __fmul_rn(tmax, c2);
+        float m_new = m_ref;
+        if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
+        const bool moved = (m_new != m_ref);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
+        // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
+        uint32_t code[4];
+        uint32_t sfp = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
+          code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
+          sfp |= code[c] << (8 * c);
+        }
+        // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
+        // the scaled values per block and rescales by 2^e
+        uint32_t pw[32];
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int e = static_cast<int>(code[c]) - 127;
+          const float nb = -(m_use + static_cast<float>(e));
+          const uint64_t nb2 = pack2(nb, nb);
+          uint64_t acc = 0;
+#pragma unroll
+          for (int kk = 0; kk < 16; kk += 2) {
+            const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][2 * kk]), __uint_as_float(sv[c][2 * kk + 1])), c2x2, nb2);
+            const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][2 * kk + 2]), __uint_as_float(sv[c][2 * kk + 3])), c2x2, nb2);
+            const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
+            const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
+            acc = add2(acc, pack2(p0, p1));
+            acc = add2(acc, pack2(p2, p3));
+            pw[8 * c + kk / 2] = cvt_e4m3x4(p0, p1, p2, p3);
+          }
+          // 2^e as fp32 (e in [-127, 119]; 2^-127 flushes to 0, harmless: such
+          // blocks hold only zeros)
+          const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+          lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
+        }
+        // the previous P must be consumed before this P overwrites it (and O
+        // is stable only between two PVs); an item's first tile follows the
+        // previous item's epilogue, which waited for its last PV
+        if (j > 0) {
+          ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 31);
+          if (!ok) break;
+          tc_fence_after();
+          // the previous tile's S and PV are done: its K/V stage may be refilled
+          if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
+        }
+        tmem_st32(tmem + kColP + 32 * wg + lane_base, pw);
+        tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
+        // selective rescale of O (and l): only warps holding a moved row; each
+        // half rescales half of the columns
+        if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
+          uint32_t rr[32];
+#pragma unroll 1
+          for (int c = 0; c < D / 64; ++c) {
+            const uint32_t ta = tmem + kColO + (D / 2) * wg + 32 * c + lane_base;
+            tmem_ld32(ta, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st32(ta, rr);
+          }
+        }
+        tmem_st_wait();
+        l = l * alpha + lsum;
+        m_ref = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_full);
       }
-      tmem_st_wait();
-      l = l * alpha + lsum;
-      m_ref = m_new;
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
-    }
-    // epilogue: O / l -> bf16 (each half writes half of the columns), LSE
-    if (ok && ntiles > 0) {
+      if (!ok) break;
+      // epilogue: O / l -> bf16 (each half writes half of the columns), LSE
       xsum[wg * 128 + row] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(xbar);
-      ok = mbar_wait_sleep(xbar, ntiles & 1, p.err, abort, 34);
-      if (ok) ok = mbar_wait_sleep(&bars->pv_done, (ntiles - 1) & 1, p.err, abort, 32);
-      if (ok) {
-        tc_fence_after();
-        const float lt = l + xsum[(1 - wg) * 128 + row];
-        const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
-        const bool valid = qi < w.len;
-        const int64_t tok = w.start + qi;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D + (D / 2) * wg);
-        uint32_t r[32];
+      ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 34);
+      if (!ok) break;
+      ++gx;
+      ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 32);
+      if (!ok) break;
+      tc_fence_after();
+      // the item's last S and PV are done: its K/V stage may be refilled
+      if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
+      const float lt = l + xsum[(1 - wg) * 128 + row];
+      const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
+      const bool valid = qi < w.len;
+      const int64_t tok = w.start + qi;
+      uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D + (D / 2) * wg);
+      uint32_t rr[32];
 #pragma unroll 1
-        for (int c = 0; c < D / 64; ++c) {
-          tmem_ld32(tmem + kColO + (D / 2) * wg + 32 * c + lane_base, r);
-          tmem_ld_wait();
-          if (valid) {
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tmem + kColO + (D / 2) * wg + 32 * c + lane_base, rr);
+        tmem_ld_wait();
+        if (valid) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint32_t wv[4];
+          for (int i = 0; i < 4; ++i) {
+            uint32_t wv[4];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                    __uint_as_float(r[8 * i + 2 * k]) * inv_l,
-                    __uint_as_float(r[8 * i + 2 * k + 1]) * inv_l);
-                wv[k] = *reinterpret_cast<uint32_t*>(&h2);
-              }
-              dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            for (int kk = 0; kk < 4; ++kk) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(
+                  __uint_as_float(rr[8 * i + 2 * kk]) * inv_l,
+                  __uint_as_float(rr[8 * i + 2 * kk + 1]) * inv_l);
+              wv[kk] = *reinterpret_cast<uint32_t*>(&h2);
             }
+            dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
-        if (valid && wg == 0) {
-          const float lse2 = m_ref + __log2f(lt);
-          p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
-              lse2 * 0.69314718055994531f;
-        }
+      }
+      if (valid && wg == 0) {
+        const float lse2 = m_ref + __log2f(lt);
+        p.lse[static_cast<int64_t>(w.head) * p.seqs.total_tokens + tok] =
+            lse2 * 0.69314718055994531f;
       }
     }
   }
@@ -568,8 +627,16 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   const int64_t units = sv.cu_seqlens == nullptr
                             ? static_cast<int64_t>(sv.nseq) * p.nq
                             : sv.total_sf_rows / 128;
-  const int64_t nblocks = units * p.hq;
-  LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
+  const int64_t nitems = units * p.hq;
+  LPFA_CHECK_ARG(nitems > 0 && nitems < (1ll << 31));
+  p.nitems = nitems;
+  static int nsm = 0;
+  if (nsm == 0) {
+    int dev = 0;
+    LPFA_CHECK_CUDA(cudaGetDevice(&dev));
+    LPFA_CHECK_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  }
+  const int64_t nblocks = nitems < nsm ? nitems : nsm;   // one CTA per SM
   const size_t smem = FwdCfg<D>::kTotal + 1024;
   static bool attr = false;
   if (!attr) {
