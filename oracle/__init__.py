@@ -15,5 +15,6 @@ Modules:
   layouts    the MMA-ready scale arrangements, written from the tensor-core
              scale-factor layout description, for checking the quantizer's
              second scale output.
+  norm       RMSNorm followed by MX quantization (the fused producer).
 """
-from . import mx, attention  # noqa: F401
+from . import mx, attention, norm  # noqa: F401
