@@ -147,6 +147,38 @@ lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
                              void* out_sf_mma_t, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Fused RMSNorm + MX quantization ([P1] paragraph 2: fused RMSNorm+Quantize
+ * kernels producing FP8 output with dual scale factor layouts in one pass).
+ *
+ * x: bf16 [T, heads, head_dim] (device, 16-byte aligned), one token row of
+ * N = heads * head_dim values per token; weight: bf16 [N] (device, 16-byte
+ * aligned); eps > 0.  For every token
+ *   y = x / sqrt(mean(x^2) + eps) * weight,
+ * formed in fp32 by a fixed sequence of correctly rounded operations: ss =
+ * the fp32 sum of the exact squares, 32 partial sums (partial l over the
+ * 8-element chunks l, l + 32, ... of the row, element by element) combined
+ * pairwise at distance 16, 8, 4, 2, 1; rstd = 1 / sqrt(ss / N + eps);
+ * y = (x * rstd) * weight, each product rounded to fp32.  y is then quantized
+ * exactly as lpfa_mx_quantize quantizes its input (same rule, same outputs
+ * and layouts), with blk = LPFA_BLK_1X32 or LPFA_BLK_32X32 (the square blocks
+ * give one payload with the two tensor-core scale arrangements out_sf_mma and
+ * out_sf_mma_t); LPFA_BLK_32X1 returns LPFA_ERR_UNSUPPORTED.
+ *
+ * out_rstd: fp32 [T] (device) or NULL; receives rstd of every token.
+ * HBM sees x once: a CTA reads its 32 token rows for the sums of squares and
+ * again, from L2, for the payload.
+ * Errors: null or misaligned pointers, eps <= 0 or non-finite, heads outside
+ * [1, 4096] -> LPFA_ERR_INVALID_ARG; head_dim not 64/128 -> UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_rmsnorm_mx_quantize(const lpfa_seqs* seqs, const void* x,
+                                     const void* weight, int64_t heads,
+                                     int64_t head_dim, float eps,
+                                     lpfa_block blk, void* out_e4m3,
+                                     void* out_sf, void* out_sf_mma,
+                                     void* out_sf_mma_t, float* out_rstd,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
  * Block-scaled MXFP8 GEMM (measures the dense MX MMA rate in the same run as
  * the attention kernels; also the tcgen05 block-scale bring-up).
  *   D[M, N] (fp32, row-major, ldd = N) = A[M, K] * B[N, K]^T

@@ -242,6 +242,226 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused RMSNorm + MX quantization ("Low Precision Flash Attention 4 ...",
+// paragraph 2: fused RMSNorm+Quantize kernels producing FP8 output with dual
+// scale factor layouts in one pass).  y = x / sqrt(mean(x^2) + eps) * w over
+// each token's H * D values, then the quantizer's 1x32 or 32x32 blocks and
+// scale layouts on y.  The codes are decided on fp32 y formed by a fixed
+// sequence of correctly rounded operations (no contraction into FMA):
+//   ss   = fp32 sum of the exact squares; lane l of a warp adds the row's
+//          8-element chunks l, l + 32, ... element by element, then a
+//          butterfly adds partner sums at lane distance 16, 8, 4, 2, 1;
+//   rstd = 1 / sqrt(ss / N + eps);     y = (x * rstd) * w.
+// CTA = one 32-row padded block, all heads.  Phase 1: the block's rstd (four
+// rows per warp), phase 2: each warp quantizes whole heads of the block,
+// reading x again (from L2: the CTA has just read it), so HBM sees x once.
+
+struct NormArgs {
+  const __nv_bfloat16* w;   // [H * D]
+  float eps;
+  float* rstd;              // [T] or null
+};
+
+// a 16-byte load the compiler may not merge with an earlier load of the
+// same address
+__device__ __forceinline__ uint4 ld_global_v4(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// y for the 8 bf16 of one 16-byte chunk of x and of w
+__device__ __forceinline__ void norm8(const uint4& xv, const uint4& wv, float rs, float* y) {
+  const uint32_t* xu = reinterpret_cast<const uint32_t*>(&xv);
+  const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    y[2 * i] = __fmul_rn(__fmul_rn(__uint_as_float(xu[i] << 16), rs), __uint_as_float(wu[i] << 16));
+    y[2 * i + 1] = __fmul_rn(__fmul_rn(__uint_as_float(xu[i] & 0xFFFF0000u), rs),
+                             __uint_as_float(wu[i] & 0xFFFF0000u));
+  }
+}
+
+// |y| for the same 8 values, formed from |x| and |w| (round to nearest is
+// sign-symmetric, so these are the magnitudes of norm8's results bit for
+// bit); a separate form keeps the compiler from holding norm8's results of
+// the maxima pass live until the payload pass
+__device__ __forceinline__ uint32_t norm8_amax_bits(const uint4& xv, const uint4& wv, float rs) {
+  const uint32_t* xu = reinterpret_cast<const uint32_t*>(&xv);
+  const uint32_t* wu = reinterpret_cast<const uint32_t*>(&wv);
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a0 = __uint_as_float((xu[i] << 16) & 0x7FFFFFFFu);
+    const float a1 = __uint_as_float(xu[i] & 0x7FFF0000u);
+    const float b0 = __uint_as_float((wu[i] << 16) & 0x7FFFFFFFu);
+    const float b1 = __uint_as_float(wu[i] & 0x7FFF0000u);
+    m = max(m, __float_as_uint(__fmul_rn(__fmul_rn(a0, rs), b0)));
+    m = max(m, __float_as_uint(__fmul_rn(__fmul_rn(a1, rs), b1)));
+  }
+  return m;
+}
+
+// 8 values with one scale code -> 8 E4M3 bytes (two words)
+__device__ __forceinline__ void quant8(const float* y, uint32_t code, uint32_t& w0, uint32_t& w1) {
+  const float inv = inv_scale_from_code(code);
+  w0 = cvt_e4m3x4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+  w1 = cvt_e4m3x4(y[4] * inv, y[5] * inv, y[6] * inv, y[7] * inv);
+  if (code == 0xFFu) w0 = w1 = 0x7F7F7F7Fu;
+}
+
+template <int kMode, int kNcb>  // mode 0: 1x32, 2: 32x32
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)
+    rms_mx_quantize_kernel(const QuantArgs a, const NormArgs nrm) {
+  static_assert(kMode == 0 || kMode == 2, "1x32 or 32x32 blocks");
+  constexpr int kTpl = 32 / kNcb;                  // tokens per load
+  __shared__ float s_rstd[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t rb = blockIdx.x;
+  const int64_t pr0 = rb * 32;                     // first padded row of the block
+  const int sq = seq_of_sf_row(a.seqs, pr0);
+  const SeqInfo si = seq_info(a.seqs, sq);
+  const int64_t off = pr0 - si.sf_start;           // token offset in sequence
+  const int64_t nvalid64 = static_cast<int64_t>(si.len) - off;
+  const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : static_cast<int>(nvalid64));
+  const int n = a.H * a.D;
+  const int nch = n / 8;                           // 16-byte chunks per row
+
+  // ---- phase 1: rstd of rows warp*4 .. warp*4+3
+#pragma unroll 1
+  for (int rr = 0; rr < 4; ++rr) {
+    const int row = warp * 4 + rr;
+    float ss = 0.f;
+    if (row < nvalid) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (si.start + off + row) * static_cast<int64_t>(n));
+#pragma unroll 1
+      for (int c0 = lane; c0 < nch; c0 += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + 32 * u;
+          v[u] = c < nch ? src[c] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t* xu = reinterpret_cast<const uint32_t*>(&v[u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float lo = __uint_as_float(xu[i] << 16), hi = __uint_as_float(xu[i] & 0xFFFF0000u);
+            ss = __fadd_rn(ss, __fmul_rn(lo, lo));   // exact squares; the zero
+            ss = __fadd_rn(ss, __fmul_rn(hi, hi));   // chunks past the row add 0
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, d));
+    if (lane == 0) {
+      float r = 0.f;
+      if (row < nvalid) {
+        r = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(n)), nrm.eps)));
+        if (nrm.rstd != nullptr) nrm.rstd[si.start + off + row] = r;
+      }
+      s_rstd[row] = r;
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: one head of the block per warp at a time
+  const int cb = lane % kNcb, t = lane / kNcb;
+  const int64_t tile_row = (rb >> 2) * a.H;        // 512-byte scale tiles of the block
+  const int kb_row = static_cast<int>(rb & 3);     // token block within the tile
+#pragma unroll 1
+  for (int h = warp; h < a.H; h += kWarpsPerBlock) {
+    const int64_t tile_base = (tile_row + h) * 512;
+    // this lane's 32 weights (L1-resident) and x rows: the maxima pass loads
+    // every row of the lane at once; the payload pass loads each row again
+    // (from L1) just before it is used, so that y never has to stay live
+    const uint4* wsrc = reinterpret_cast<const uint4*>(nrm.w + h * a.D + 32 * cb);
+    auto xrow = [&](int row) {
+      return reinterpret_cast<const uint4*>(a.x + ((si.start + off + row) * a.H + h) * a.D + 32 * cb);
+    };
+    uint32_t rcode[kNcb];
+    uint32_t m2 = 0;
+    {
+      uint4 v[kNcb][4];
+#pragma unroll
+      for (int r = 0; r < kNcb; ++r) {
+        const int row = r * kTpl + t;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[r][i] = make_uint4(0, 0, 0, 0);
+        if (row < nvalid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) v[r][i] = xrow(row)[i];
+        }
+      }
+      // block maxima: per row (1x32) or over the whole 32x32 tile
+#pragma unroll
+      for (int r = 0; r < kNcb; ++r) {
+        const float rs = s_rstd[r * kTpl + t];
+        uint32_t m = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) m = max(m, norm8_amax_bits(v[r][i], __ldg(wsrc + i), rs));
+        rcode[r] = e8m0_code_from_amax_bits(m);
+        m2 = max(m2, m);
+      }
+    }
+    uint32_t bcode = 0;                            // 32x32: the block's code
+    if (kMode == 2) {
+#pragma unroll
+      for (int x = kNcb; x < 32; x <<= 1) m2 = max(m2, __shfl_xor_sync(0xFFFFFFFFu, m2, x));
+      bcode = e8m0_code_from_amax_bits(m2);
+    }
+#pragma unroll
+    for (int r = 0; r < kNcb; ++r) {
+      const int row = r * kTpl + t;
+      const bool valid = row < nvalid;
+      const int64_t tok = si.start + off + row;
+      const float rs = s_rstd[row];
+      const uint32_t code = kMode == 0 ? rcode[r] : bcode;
+      if (valid) {
+        uint4 xv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xv[i] = ld_global_v4(xrow(row) + i);
+        uint32_t wq[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float y[8];
+          norm8(xv[i], __ldg(wsrc + i), rs, y);
+          quant8(y, code, wq[2 * i], wq[2 * i + 1]);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.H + h) * a.D + 32 * cb);
+        __stcs(dst + 0, make_uint4(wq[0], wq[1], wq[2], wq[3]));
+        __stcs(dst + 1, make_uint4(wq[4], wq[5], wq[6], wq[7]));
+      }
+      // this row's kNcb codes gathered into one word by the cb = 0 lane
+      const uint32_t c = (kMode == 0 && !valid) ? 0u : code;
+      uint32_t word = c;
+#pragma unroll
+      for (int k = 1; k < kNcb; ++k) word |= __shfl_down_sync(0xFFFFFFFFu, c, k) << (8 * k);
+      if (cb == 0) {
+        if (a.sf_mma != nullptr) {
+          const uint32_t wm = (kMode == 2 && !valid) ? 0u : word;
+          uint8_t* d = a.sf_mma + tile_base + row * 16 + kb_row * 4;
+          if (kNcb == 4) *reinterpret_cast<uint32_t*>(d) = wm;
+          else *reinterpret_cast<uint16_t*>(d) = static_cast<uint16_t>(wm);
+        }
+        if (kMode == 0 && a.sf != nullptr && valid) {
+          uint8_t* d = a.sf + (tok * a.H + h) * kNcb;
+          if (kNcb == 4) *reinterpret_cast<uint32_t*>(d) = word;
+          else *reinterpret_cast<uint16_t*>(d) = static_cast<uint16_t>(word);
+        }
+      }
+      if (kMode == 2 && a.sf_mma_t != nullptr)
+        a.sf_mma_t[tile_base + row * 16 + cb * 4 + kb_row] = static_cast<uint8_t>(bcode);
+    }
+    if (kMode == 2 && a.sf != nullptr && t == 0)
+      a.sf[(rb * a.H + h) * kNcb + cb] = static_cast<uint8_t>(bcode);
+  }
+}
+
 }  // namespace
 }  // namespace lpfa
 
@@ -303,6 +523,62 @@ extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
       if (d128) mx_quantize_kernel<2, 4><<<grid, block, 0, cs>>>(a);
       else mx_quantize_kernel<2, 2><<<grid, block, 0, cs>>>(a);
       break;
+  }
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}
+
+extern "C" lpfa_status lpfa_rmsnorm_mx_quantize(const lpfa_seqs* seqs, const void* x,
+                                                const void* weight, int64_t heads,
+                                                int64_t head_dim, float eps, lpfa_block blk,
+                                                void* out_e4m3, void* out_sf, void* out_sf_mma,
+                                                void* out_sf_mma_t, float* out_rstd,
+                                                void* stream) {
+  SeqView sv;
+  lpfa_status st = make_seq_view(seqs, &sv);
+  if (st != LPFA_OK) return st;
+  LPFA_CHECK_ARG(x != nullptr && weight != nullptr && out_e4m3 != nullptr);
+  LPFA_CHECK_ARG(aligned16(x) && aligned16(weight) && aligned16(out_e4m3));
+  LPFA_CHECK_ARG(heads >= 1 && heads <= 4096);
+  LPFA_CHECK_ARG(eps > 0.f && eps < 3.0e38f);
+  LPFA_CHECK_ARG(out_sf_mma_t == nullptr || blk == LPFA_BLK_32X32);
+  if (blk != LPFA_BLK_1X32 && blk != LPFA_BLK_32X32) return LPFA_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return LPFA_ERR_UNSUPPORTED;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (sv.total_tokens == 0) return LPFA_OK;
+
+  const int64_t Tp = sv.total_sf_rows;
+  const int64_t mma_bytes = (Tp / 128) * heads * 512;
+  if (head_dim < 128) {
+    if (out_sf_mma != nullptr)
+      LPFA_CHECK_CUDA(cudaMemsetAsync(out_sf_mma, 0, mma_bytes, cs));
+    if (out_sf_mma_t != nullptr)
+      LPFA_CHECK_CUDA(cudaMemsetAsync(out_sf_mma_t, 0, mma_bytes, cs));
+  }
+  QuantArgs a;
+  a.seqs = sv;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.out = static_cast<uint8_t*>(out_e4m3);
+  a.sf = static_cast<uint8_t*>(out_sf);
+  a.sf_mma = static_cast<uint8_t*>(out_sf_mma);
+  a.sf_mma_t = static_cast<uint8_t*>(out_sf_mma_t);
+  a.H = static_cast<int32_t>(heads);
+  a.D = static_cast<int32_t>(head_dim);
+  a.ntiles = (Tp / 32) * heads * (head_dim / 32);
+  NormArgs nrm;
+  nrm.w = static_cast<const __nv_bfloat16*>(weight);
+  nrm.eps = eps;
+  nrm.rstd = out_rstd;
+  const int64_t blocks = Tp / 32;                  // one CTA per 32-row block
+  LPFA_CHECK_ARG(blocks < (1ll << 31));
+  dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
+  const bool d128 = head_dim == 128;
+  if (blk == LPFA_BLK_1X32) {
+    if (d128) rms_mx_quantize_kernel<0, 4><<<grid, block, 0, cs>>>(a, nrm);
+    else rms_mx_quantize_kernel<0, 2><<<grid, block, 0, cs>>>(a, nrm);
+  } else {
+    if (d128) rms_mx_quantize_kernel<2, 4><<<grid, block, 0, cs>>>(a, nrm);
+    else rms_mx_quantize_kernel<2, 2><<<grid, block, 0, cs>>>(a, nrm);
   }
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;

@@ -61,6 +61,9 @@ _varlen_sf_rows = _sig("lpfa_varlen_sf_rows", ctypes.c_int, _vp, _i64, _vp, _vp)
 _mx_quantize = _sig("lpfa_mx_quantize", ctypes.c_int,
                     ctypes.POINTER(lpfa_seqs), _vp, _i64, _i64, ctypes.c_int,
                     _vp, _vp, _vp, _vp, _vp)
+_rms_quantize = _sig("lpfa_rmsnorm_mx_quantize", ctypes.c_int,
+                     ctypes.POINTER(lpfa_seqs), _vp, _vp, _i64, _i64, ctypes.c_float,
+                     ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                 _i64, _i64, _i64, _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
@@ -80,7 +83,8 @@ _bwd_noalloc = _sig("lpfa_bwd_noalloc", ctypes.c_int,
 
 #: every symbol include/lpfa.h declares
 EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
-            "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_mx_gemm",
+            "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_rmsnorm_mx_quantize",
+            "lpfa_mx_gemm",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc")
 
@@ -207,6 +211,51 @@ def mx_quantize(x: torch.Tensor, block: int, seqs: Optional[Seqs] = None,
                                    device=dev)
     lpfa_mx_quantize(seqs, x, block, out, sf, sf_mma, sf_mma_t, stream)
     return MXTensor(out, sf, sf_mma, sf_mma_t, block, seqs)
+
+
+def lpfa_rmsnorm_mx_quantize(seqs: Seqs, x: torch.Tensor, weight: torch.Tensor, eps: float,
+                             block: int, out: torch.Tensor, sf=None, sf_mma=None,
+                             sf_mma_t=None, rstd=None, stream=None):
+    """Raw call: x bf16 [T, H, D], weight bf16 [H * D] (contiguous, CUDA);
+    outputs preallocated."""
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert weight.dtype == torch.bfloat16 and weight.is_contiguous()
+    T, H, D = x.shape
+    assert weight.numel() == H * D
+    sc = seqs.c()
+    _ok(_rms_quantize(ctypes.byref(sc), _ptr(x), _ptr(weight), H, D, float(eps), block,
+                      _ptr(out), _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _ptr(rstd),
+                      _stream(stream)), "lpfa_rmsnorm_mx_quantize")
+
+
+def rmsnorm_mx_quantize(x: torch.Tensor, weight: torch.Tensor, eps: float, block: int,
+                        seqs: Optional[Seqs] = None, compact: bool = True,
+                        mma: bool = True, stream=None):
+    """Fused RMSNorm + MX quantization of bf16 [B, S, H, D] or packed
+    [T, H, D] (with ``seqs``); the norm runs over each token's H * D values.
+    Returns (MXTensor of y, rstd fp32 [T])."""
+    if x.dim() == 4:
+        B, S, H, D = x.shape
+        if seqs is None:
+            seqs = dense_seqs(B, S)
+        x = x.reshape(B * S, H, D)
+    T, H, D = x.shape
+    x = x.contiguous()
+    Tp = seqs.total_sf_rows
+    dev = x.device
+    out = torch.empty((T, H, D), dtype=torch.uint8, device=dev)
+    sf = sf_mma = sf_mma_t = None
+    if compact:
+        shape = {LPFA_BLK_1X32: (T, H, D // 32), LPFA_BLK_32X32: (Tp // 32, H, D // 32)}[block]
+        sf = torch.empty(shape, dtype=torch.uint8, device=dev)
+    if mma:
+        sf_mma = torch.empty((Tp // 128, H, 512), dtype=torch.uint8, device=dev)
+        if block == LPFA_BLK_32X32:
+            sf_mma_t = torch.empty((Tp // 128, H, 512), dtype=torch.uint8, device=dev)
+    rstd = torch.empty((T,), dtype=torch.float32, device=dev)
+    lpfa_rmsnorm_mx_quantize(seqs, x, weight.contiguous(), eps, block, out, sf, sf_mma,
+                             sf_mma_t, rstd, stream)
+    return MXTensor(out, sf, sf_mma, sf_mma_t, block, seqs), rstd
 
 
 # ---------------------------------------------------------------- GEMM
