@@ -36,6 +36,7 @@ import workloads  # noqa: E402
 METRIC = "MXFP8 attn fwd/bwd PFLOP/s (B8 H32 S8192 D128 causal); % of FP8 MMA peak"
 WORKLOAD = "llm"
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 : bf16 tensor-core ratio
+NORM_ITERS = 20          # timed launches of the fused RMSNorm + MX quantizer
 E2E_MIN_STEPS = 20       # steps the end-to-end leg times at least
 
 
@@ -267,6 +268,39 @@ def run_lpfa(args, world, rank, local):
     qb = statistics.mean(p[2].elapsed_time(p[3]) for p in parts)
     bw = statistics.mean(p[3].elapsed_time(p[4]) for p in parts)
 
+    # ---- the fused RMSNorm + MX quantizer on the model's hidden state: Q
+    # viewed as [T, H * D] (hidden 4096, 512 MiB, larger than L2), square
+    # blocks with compact and both tensor-core scale layouts and rstd; beside
+    # it, for context, the two-pass form (torch's bf16 rms_norm, then this
+    # library's quantizer)
+    wn = (1.0 + 0.1 * torch.randn(H * D, generator=torch.Generator().manual_seed(7)))
+    wn = wn.bfloat16().to(dev)
+    fused = lambda: L.rmsnorm_mx_quantize(q, wn, 1e-6, L.LPFA_BLK_32X32, seqs)
+    two_pass = lambda: L.mx_quantize(
+        torch.nn.functional.rms_norm(q.view(T, H * D), (H * D,), wn, 1e-6).view(T, H, D),
+        L.LPFA_BLK_32X32, seqs)
+
+    def _time(fn, iters=NORM_ITERS):
+        for _ in range(3):
+            res = fn()
+        torch.cuda.synchronize()
+        a_, b_ = ev(), ev()
+        a_.record()
+        for _ in range(iters):
+            res = fn()
+        b_.record()
+        torch.cuda.synchronize()
+        return a_.elapsed_time(b_) / iters, res
+
+    norm_ms, (mn, rn) = _time(fused)
+    norm_bytes = (q.numel() * 2 + wn.numel() * 2 + mn.data.numel() + mn.sf.numel()
+                  + mn.sf_mma.numel() + mn.sf_mma_t.numel() + rn.numel() * 4)
+    try:
+        two_pass_ms = _time(two_pass)[0]
+    except Exception:  # rms_norm missing from this torch
+        two_pass_ms = None
+    del mn, rn
+
     # ---- end to end through the public API with host buffers
     out_host = {"o": torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory(),
                 "dq": torch.empty((T, H, D), dtype=torch.float16).pin_memory(),
@@ -397,6 +431,11 @@ def run_lpfa(args, world, rank, local):
     else:
         peak = 1700.0 * FP8_OVER_BF16
         peak_src = "fallback 1.7 PFLOP/s bf16 sustained x 2"
+    hbm = peaks.get("hbm_gbs") if peaks else None
+    hbm_src = "measured copy bandwidth, MEASURED_PEAKS.json (of measured)" if hbm else \
+        "fallback 6.8 TB/s"
+    hbm = hbm or 6800.0
+    norm_gbs = norm_bytes / (norm_ms * 1e-3) / 1e9
     bwd_tflops = bwd_flops / bw / 1e9
     fwd_tflops = fwd_flops / fw / 1e9
     total = (fwd_flops + bwd_flops) * world
@@ -426,6 +465,13 @@ def run_lpfa(args, world, rank, local):
                      "frac": bwd_tflops / peak, "traffic": traffic,
                      "peak_source": peak_src + " (of measured)"},
         "mma_rate_in_run": mma,
+        "rmsnorm_quantize": {
+            "workload": f"x [{T}, {H * D}] bf16 (the llm Q tensor as hidden states), 32x32 blocks, "
+                        "compact + both tensor-core scale layouts + rstd",
+            "ms": norm_ms, "bytes_per_launch": norm_bytes, "achieved_gbs": norm_gbs,
+            "peak_gbs": hbm, "frac": norm_gbs / hbm, "peak_source": hbm_src,
+            "two_pass_ms": two_pass_ms,
+            "two_pass": "torch bf16 rms_norm, then lpfa_mx_quantize (context)"},
         "e2e": {"value": total / (e2e_ms * 1e-3) / 1e15, "unit": "PFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
@@ -446,8 +492,9 @@ def run_lpfa(args, world, rank, local):
 
 def run_profile_case(iters: int):
     """One small pass of the hot path for ncu captures: B4 H16 S8192 D128
-    causal (128 MiB per bf16 tensor, larger than L2), fwd + bwd ``iters``
-    times, no timing."""
+    causal (128 MiB per bf16 tensor, larger than L2), the fused RMSNorm + MX
+    quantizer on Q viewed as [32768, 2048], then fwd + bwd, ``iters`` times,
+    no timing."""
     from mxfp8_block_scaled_quantizer_gb300 import build
     build()
     from mxfp8_block_scaled_quantizer_gb300 import lpfa as L
@@ -457,7 +504,9 @@ def run_profile_case(iters: int):
     q, k, v, do = mk(), mk(), mk(), mk()
     seqs = L.dense_seqs(B, S)
     desc = L.attn_desc(seqs, H, H, D, True, D ** -0.5)
+    wn = torch.ones(H * D, device="cuda", dtype=torch.bfloat16)
     for _ in range(iters):
+        L.rmsnorm_mx_quantize(q, wn, 1e-6, L.LPFA_BLK_32X32, seqs)
         mq, mk_, mv = L.quantize_forward_operands(q, k, v, seqs)
         o, lse, ws = L.attention_forward_mx(mq, mk_, mv, desc)
         bq, bk, bv, bdo = L.quantize_backward_operands(q, k, v, do, seqs)
