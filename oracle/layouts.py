@@ -16,6 +16,12 @@ Two arrangements exist for every quantized operand:
   "Operand rows" are tokens for K-major use (contraction over head_dim) and
   head_dim channels for MN-major use (contraction over tokens).
 
+``gemm_operand_mma`` / ``gemm_quantize`` give the same arrangements for a
+GEMM result quantized as the next GEMM's operand (the fused GEMM+Quantize
+producer of "Low Precision Flash Attention 4", paragraph 2): codes are decided
+on the kernel's own fp32 result, so the comparison with the fused output is
+exact.
+
 Padded scale rows (the jagged module of "Low Precision Flash Attention 4",
 paragraph 2): FP8 data stays at unpadded token positions; scale rows of
 sequence s start at the 128-aligned row sf_start[s] = sum_{t<s} ceil(L_t/128)
@@ -124,3 +130,34 @@ def oracle_quantize(x, cu_seqlens, block):
     out.update(payload=payload, sf=sc, sf_mma=mma_from_row_blocks(row, cu),
                sf_mma_t=mma_from_token_blocks(square_to_col(sc, D), D))
     return out
+
+
+# ------------------------------------------------------------------ GEMM outputs
+def gemm_operand_mma(sc):
+    """Tensor-core arrangement of a GEMM operand's scales: sc [R, C/32]
+    (one code per row and 32-element block along the contraction) ->
+    uint8 [R/128][C/128][512], tile (i, j) holding rows 128 i .. and
+    contraction blocks 4 j .. 4 j + 3 at atom_offset(row % 128, block % 4)."""
+    R, nb = sc.shape
+    out = np.zeros((R // 128, -(-nb // 4), 512), dtype=np.uint8)
+    r, kb = np.meshgrid(np.arange(R), np.arange(nb), indexing="ij")
+    out[r // 128, kb // 4, atom_offset(r % 128, kb % 4)] = sc[r, kb]
+    return out
+
+
+def gemm_quantize(d, block):
+    """Oracle of the quantizing GEMM epilogue: the fp32 result d [M, N]
+    quantized in 1x32 blocks along N, or in 32x32 blocks.  Returns dict(
+    payload [M, N], sf (compact: [M, N/32] or [M/32, N/32]), sf_mma (rows =
+    M, contraction over N: [M/128][N/128][512]) and, for 32x32, sf_mma_t
+    (rows = N, contraction over M: [N/128][M/128][512]))."""
+    from . import mx
+    d = np.asarray(d, dtype=np.float64)
+    if block == "1x32":
+        p, sc = mx.quantize_1x32(d)
+        return {"payload": p, "sf": sc, "sf_mma": gemm_operand_mma(sc), "sf_mma_t": None}
+    assert block == "32x32"
+    p, sc = mx.quantize_32x32(d)
+    return {"payload": p, "sf": sc,
+            "sf_mma": gemm_operand_mma(np.repeat(sc, 32, axis=0)),
+            "sf_mma_t": gemm_operand_mma(np.repeat(sc.T, 32, axis=0))}

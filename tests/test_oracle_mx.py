@@ -230,3 +230,22 @@ def test_mma_atom_is_a_permutation():
 def test_sf_row_starts_varlen():
     cu = np.array([0, 5, 133, 261, 262])
     assert layouts.sf_row_starts(cu).tolist() == [0, 128, 256, 384, 512]
+
+
+# ----------------------------------------------------- quantizing GEMM epilogue
+@pytest.mark.parametrize("block", ["1x32", "32x32"])
+def test_gemm_quantize_layouts(block, rng):
+    M, N = 256, 384
+    d = rng.standard_normal((M, N)) * np.exp(rng.uniform(-3, 3, (M, 1)))
+    out = layouts.gemm_quantize(d, block)
+    # every tile byte is the compact code of its (row, block)
+    sc_rows = out["sf"] if block == "1x32" else np.repeat(out["sf"], 32, axis=0)
+    r, kb = np.meshgrid(np.arange(M), np.arange(N // 32), indexing="ij")
+    assert np.array_equal(out["sf_mma"][r // 128, kb // 4, layouts.atom_offset(r % 128, kb % 4)],
+                          sc_rows)
+    if block == "32x32":
+        # transpose invariance of square blocks: quantizing d^T gives the
+        # transposed payload, and its row arrangement is sf_mma_t
+        t = layouts.gemm_quantize(d.T, "32x32")
+        assert np.array_equal(t["payload"], out["payload"].T)
+        assert np.array_equal(t["sf_mma"], out["sf_mma_t"])
