@@ -404,6 +404,24 @@ def run_lpfa(args, world, rank, local):
         g1.record()
         torch.cuda.synchronize()
         mma["lpfa_mx_gemm_tflops"] = 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
+        # the same GEMM with the quantizing epilogue (square blocks, compact
+        # and both tensor-core scale layouts; no fp32 result)
+        qo = torch.empty(M, N, device=dev, dtype=torch.uint8)
+        qsf = torch.empty(M // 32, N // 32, device=dev, dtype=torch.uint8)
+        qm = torch.empty(M // 128, N // 128, 512, device=dev, dtype=torch.uint8)
+        qt = torch.empty(N // 128, M // 128, 512, device=dev, dtype=torch.uint8)
+        gq = lambda: L.lpfa_mx_gemm_quantize(A8, ga.sf_mma, B8, gb.sf_mma, L.LPFA_BLK_32X32,
+                                             qo, qsf, qm, qt)
+        for _ in range(3):
+            gq()
+        torch.cuda.synchronize()
+        g0.record()
+        for _ in range(10):
+            gq()
+        g1.record()
+        torch.cuda.synchronize()
+        mma["lpfa_mx_gemm_quantize_32x32_tflops"] = 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
+        del qo, qsf, qm, qt
         try:
             a8 = A8.view(torch.float8_e4m3fn); b8 = B8.view(torch.float8_e4m3fn)
             sa = ga.sf_mma.view(torch.float8_e8m0fnu).reshape(-1)

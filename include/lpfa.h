@@ -193,6 +193,35 @@ lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
                          int64_t K, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Block-scaled MXFP8 GEMM with a quantizing epilogue ([P1] paragraph 2:
+ * fused GEMM+Quantize kernels producing FP8 output with dual scale factor
+ * layouts in one pass).  The fp32 result D = A * B^T (operands and
+ * constraints as lpfa_mx_gemm; N a multiple of 256) is quantized in
+ * registers with the quantizer's rule (lpfa_mx_quantize) before it leaves
+ * the SM:
+ *   blk = LPFA_BLK_1X32   32 consecutive columns of one row;
+ *   blk = LPFA_BLK_32X32  32 rows x 32 columns (transpose-invariant payload).
+ * Outputs (device, caller-allocated):
+ *   out_e4m3      uint8 [M, N] row-major (16-byte aligned).
+ *   out_sf        compact codes: [M, N/32] (1X32) or [M/32, N/32] (32X32),
+ *                 8-byte aligned, or NULL.
+ *   out_sf_mma    the result as a GEMM operand contracting over N (rows = M):
+ *                 [M/128][N/128][512], byte (r%32)*16 + (r/32)*4 + kb of
+ *                 tile (i, j) for row 128i + r and block 4j + kb; or NULL.
+ *   out_sf_mma_t  32X32 only: as an operand contracting over M (rows = N):
+ *                 [N/128][M/128][512]; or NULL.
+ *   d             fp32 [M, N] as lpfa_mx_gemm, or NULL (not written).
+ * The codes are decided on the fp32 accumulator values that d holds.
+ * Errors: as lpfa_mx_gemm; blk = LPFA_BLK_32X1 -> LPFA_ERR_UNSUPPORTED.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mx_gemm_quantize(const void* a8, const void* sfa_mma,
+                                  const void* b8, const void* sfb_mma,
+                                  int64_t M, int64_t N, int64_t K,
+                                  lpfa_block blk, void* out_e4m3, void* out_sf,
+                                  void* out_sf_mma, void* out_sf_mma_t,
+                                  float* d, void* stream);
+
+/* ------------------------------------------------------------------------
  * Attention descriptor.
  *  heads_q % heads_kv == 0 (GQA: query head h reads kv head
  *  h / (heads_q/heads_kv)); head_dim in {64, 128}.

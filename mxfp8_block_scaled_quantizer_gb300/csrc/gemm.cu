@@ -13,6 +13,14 @@
 //   warps 2-5   epilogue: TMEM -> registers -> fp32 global stores; the
 //               accumulator is released as soon as it has been read so the
 //               next tile's main loop overlaps the stores.
+//
+// Quantizing epilogue (lpfa_mx_gemm_quantize; the fused GEMM+Quantize
+// producer of "Low Precision Flash Attention 4 ...", paragraph 2): the fp32
+// tile is quantized in registers to E4M3 with E8M0 scales, in 1x32 blocks
+// along N (a thread's 32 columns of one row) or 32x32 blocks (a warp's 32
+// rows x 32 columns, maximum by redux.sync), with the scales written in the
+// compact layout and as the next GEMM's operand: rows = M (contraction over
+// N) and, for square blocks, rows = N (contraction over M).
 #include <cuda_runtime.h>
 
 #include "lpfa_device.cuh"
@@ -38,7 +46,11 @@ constexpr int kSfColsPerStage = 12; // 4 (A) + 8 (B, two 128-row tiles)
 struct GemmArgs {
   const uint8_t* sfa;
   const uint8_t* sfb;
-  float* d;
+  float* d;             // fp32 result, or null (quantizing epilogue only)
+  uint8_t* q;           // E4M3 [M, N]
+  uint8_t* qsf;         // compact scales, or null
+  uint8_t* qsf_mma;     // [M/128][N/128][512], or null
+  uint8_t* qsf_mma_t;   // 32x32: [N/128][M/128][512], or null
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, kt;
   uint32_t* err;
@@ -54,6 +66,20 @@ struct __align__(8) GemmSmem {
   int abort;
 };
 
+// 32 fp32 values with one scale code -> 32 E4M3 bytes (8 words)
+__device__ __forceinline__ void quant32(const uint32_t (&r)[32], uint32_t code, uint32_t (&w)[8]) {
+  const float inv = inv_scale_from_code(code);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j] = cvt_e4m3x4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                      __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+  if (code == 0xFFu) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) w[j] = 0x7F7F7F7Fu;
+  }
+}
+
+template <int kQuant>   // -1: fp32 only; 0: 1x32 along N; 2: 32x32
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                    const __grid_constant__ CUtensorMap tma_b,
@@ -189,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = tm * kBM + q * 32 + lane;
       float* drow = g.d + static_cast<int64_t>(row) * g.N + tn * kBN;
       uint32_t r[32];
-#pragma unroll 1
+      uint32_t codes[kBN / 32];                  // this row's (or block's) codes
+#pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         tmem_ld32(tmem_addr(tmem, q * 32, c * 32), r);
         tmem_ld_wait();
@@ -198,11 +225,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->acc_empty);
         }
-        float4* dst = reinterpret_cast<float4*>(drow + c * 32);
+        if (kQuant < 0 || g.d != nullptr) {
+          float4* dst = reinterpret_cast<float4*>(drow + c * 32);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                               __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          for (int j = 0; j < 8; ++j)
+            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+        }
+        if (kQuant >= 0) {
+          // block maximum of |d| as bits (NaN above Inf), then the code
+          uint32_t m = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) m = max(m, r[j] & 0x7FFFFFFFu);
+          if (kQuant == 2) m = __reduce_max_sync(0xFFFFFFFFu, m);
+          const uint32_t code = e8m0_code_from_amax_bits(m);
+          codes[c] = code;
+          uint32_t w[8];
+          quant32(r, code, w);
+          uint4* qdst = reinterpret_cast<uint4*>(g.q + static_cast<int64_t>(row) * g.N + tn * kBN + c * 32);
+          qdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          qdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          // rows = N arrangement (square blocks): column n = tn*256 + 32c +
+          // lane of the N tile, contraction block q of the M tile
+          if (kQuant == 2 && g.qsf_mma_t != nullptr) {
+            const int64_t nt = static_cast<int64_t>(tn) * 2 + c / 4;
+            g.qsf_mma_t[(nt * g.tiles_m + tm) * 512 + lane * 16 + (c % 4) * 4 + q] =
+                static_cast<uint8_t>(code);
+          }
+        }
+      }
+      if (kQuant >= 0) {
+        const int nb = g.N / 32;
+        if (g.qsf != nullptr) {
+          if (kQuant == 0) {
+            uint2* d8 = reinterpret_cast<uint2*>(g.qsf + static_cast<int64_t>(row) * nb + tn * 8);
+            *d8 = make_uint2(codes[0] | codes[1] << 8 | codes[2] << 16 | codes[3] << 24,
+                             codes[4] | codes[5] << 8 | codes[6] << 16 | codes[7] << 24);
+          } else if (lane == 0) {
+            uint2* d8 = reinterpret_cast<uint2*>(g.qsf + static_cast<int64_t>(tm * 4 + q) * nb + tn * 8);
+            *d8 = make_uint2(codes[0] | codes[1] << 8 | codes[2] << 16 | codes[3] << 24,
+                             codes[4] | codes[5] << 8 | codes[6] << 16 | codes[7] << 24);
+          }
+        }
+        if (g.qsf_mma != nullptr) {
+          // rows = M arrangement: row (lane, quarter q) of the M tile, the
+          // four contraction blocks of each 128-column N tile side by side
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int64_t nt = static_cast<int64_t>(tn) * 2 + hf;
+            uint32_t* d4 = reinterpret_cast<uint32_t*>(
+                g.qsf_mma + (static_cast<int64_t>(tm) * (g.N / 128) + nt) * 512 + lane * 16 + q * 4);
+            *d4 = codes[4 * hf] | codes[4 * hf + 1] << 8 | codes[4 * hf + 2] << 16 |
+                  codes[4 * hf + 3] << 24;
+          }
+        }
       }
     }
   }
@@ -220,11 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 using namespace lpfa;
 
-extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
-                                    const void* b8, const void* sfb_mma,
-                                    float* d, int64_t M, int64_t N, int64_t K,
-                                    void* stream) {
-  LPFA_CHECK_ARG(a8 && sfa_mma && b8 && sfb_mma && d);
+namespace {
+lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
+                        const void* sfb_mma, float* d, int64_t M, int64_t N, int64_t K,
+                        int quant, uint8_t* q, uint8_t* qsf, uint8_t* qsf_mma,
+                        uint8_t* qsf_mma_t, void* stream) {
+  LPFA_CHECK_ARG(a8 && sfa_mma && b8 && sfb_mma);
   LPFA_CHECK_ARG(aligned16(a8) && aligned16(b8) && aligned16(sfa_mma) &&
                  aligned16(sfb_mma) && aligned16(d));
   LPFA_CHECK_ARG(M > 0 && N > 0 && K > 0);
@@ -253,6 +330,10 @@ extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
   g.sfa = static_cast<const uint8_t*>(sfa_mma);
   g.sfb = static_cast<const uint8_t*>(sfb_mma);
   g.d = d;
+  g.q = q;
+  g.qsf = qsf;
+  g.qsf_mma = qsf_mma;
+  g.qsf_mma_t = qsf_mma_t;
   g.M = static_cast<int32_t>(M);
   g.N = static_cast<int32_t>(N);
   g.K = static_cast<int32_t>(K);
@@ -262,16 +343,42 @@ extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
   g.err = nullptr;
 
   const size_t smem = kStages * kStageBytes + sizeof(GemmSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    LPFA_CHECK_CUDA(cudaFuncSetAttribute(
-        mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(smem)));
-    attr_set = true;
-  }
   const int ntiles = g.tiles_m * g.tiles_n;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
-  mx_gemm_kernel<<<grid, kThreads, smem, cs>>>(ta, tb, g);
-  LPFA_CHECK_CUDA(cudaGetLastError());
-  return LPFA_OK;
+  auto go = [&](auto kernel) -> lpfa_status {
+    LPFA_CHECK_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem)));
+    kernel<<<grid, kThreads, smem, cs>>>(ta, tb, g);
+    LPFA_CHECK_CUDA(cudaGetLastError());
+    return LPFA_OK;
+  };
+  if (quant < 0) return go(mx_gemm_kernel<-1>);
+  if (quant == 0) return go(mx_gemm_kernel<0>);
+  return go(mx_gemm_kernel<2>);
+}
+}  // namespace
+
+extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
+                                    const void* b8, const void* sfb_mma,
+                                    float* d, int64_t M, int64_t N, int64_t K,
+                                    void* stream) {
+  LPFA_CHECK_ARG(d != nullptr);
+  return launch_gemm(a8, sfa_mma, b8, sfb_mma, d, M, N, K, -1, nullptr, nullptr, nullptr,
+                     nullptr, stream);
+}
+
+extern "C" lpfa_status lpfa_mx_gemm_quantize(const void* a8, const void* sfa_mma,
+                                             const void* b8, const void* sfb_mma,
+                                             int64_t M, int64_t N, int64_t K, lpfa_block blk,
+                                             void* out_e4m3, void* out_sf, void* out_sf_mma,
+                                             void* out_sf_mma_t, float* d, void* stream) {
+  LPFA_CHECK_ARG(out_e4m3 != nullptr && aligned16(out_e4m3));
+  LPFA_CHECK_ARG(out_sf == nullptr || (reinterpret_cast<uintptr_t>(out_sf) & 7u) == 0);
+  LPFA_CHECK_ARG(out_sf_mma == nullptr || aligned16(out_sf_mma));
+  LPFA_CHECK_ARG(out_sf_mma_t == nullptr || blk == LPFA_BLK_32X32);
+  if (blk != LPFA_BLK_1X32 && blk != LPFA_BLK_32X32) return LPFA_ERR_UNSUPPORTED;
+  return launch_gemm(a8, sfa_mma, b8, sfb_mma, d, M, N, K, blk == LPFA_BLK_1X32 ? 0 : 2,
+                     static_cast<uint8_t*>(out_e4m3), static_cast<uint8_t*>(out_sf),
+                     static_cast<uint8_t*>(out_sf_mma), static_cast<uint8_t*>(out_sf_mma_t),
+                     stream);
 }

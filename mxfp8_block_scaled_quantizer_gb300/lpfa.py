@@ -66,6 +66,8 @@ _rms_quantize = _sig("lpfa_rmsnorm_mx_quantize", ctypes.c_int,
                      ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                 _i64, _i64, _i64, _vp)
+_mx_gemm_q = _sig("lpfa_mx_gemm_quantize", ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                  ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
                ctypes.POINTER(lpfa_attn_desc))
 _bwd_ws = _sig("lpfa_bwd_workspace_size", ctypes.c_size_t,
@@ -84,7 +86,7 @@ _bwd_noalloc = _sig("lpfa_bwd_noalloc", ctypes.c_int,
 #: every symbol include/lpfa.h declares
 EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_rmsnorm_mx_quantize",
-            "lpfa_mx_gemm",
+            "lpfa_mx_gemm", "lpfa_mx_gemm_quantize",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc")
 
@@ -264,6 +266,35 @@ def lpfa_mx_gemm(a8, sfa_mma, b8, sfb_mma, d, stream=None):
     N = b8.shape[0]
     _ok(_mx_gemm(_ptr(a8), _ptr(sfa_mma), _ptr(b8), _ptr(sfb_mma), _ptr(d),
                  M, N, K, _stream(stream)), "lpfa_mx_gemm")
+
+
+def lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf=None, sf_mma=None,
+                          sf_mma_t=None, d=None, stream=None):
+    """Raw call: D = A B^T quantized in the epilogue; outputs preallocated."""
+    M, K = a8.shape
+    N = b8.shape[0]
+    _ok(_mx_gemm_q(_ptr(a8), _ptr(sfa_mma), _ptr(b8), _ptr(sfb_mma), M, N, K, block,
+                   _ptr(out), _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _ptr(d),
+                   _stream(stream)), "lpfa_mx_gemm_quantize")
+
+
+def mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block: int, with_fp32: bool = False,
+                     stream=None):
+    """D = A B^T (block-scaled MXFP8 operands, 1x32 along K) quantized to
+    MXFP8 in the epilogue.  Returns (payload [M, N], sf, sf_mma, sf_mma_t,
+    d fp32 or None)."""
+    M, K = a8.shape
+    N = b8.shape[0]
+    dev = a8.device
+    out = torch.empty((M, N), dtype=torch.uint8, device=dev)
+    shape = (M, N // 32) if block == LPFA_BLK_1X32 else (M // 32, N // 32)
+    sf = torch.empty(shape, dtype=torch.uint8, device=dev)
+    sf_mma = torch.empty((M // 128, N // 128, 512), dtype=torch.uint8, device=dev)
+    sf_mma_t = (torch.empty((N // 128, M // 128, 512), dtype=torch.uint8, device=dev)
+                if block == LPFA_BLK_32X32 else None)
+    d = torch.empty((M, N), dtype=torch.float32, device=dev) if with_fp32 else None
+    lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf, sf_mma, sf_mma_t, d, stream)
+    return out, sf, sf_mma, sf_mma_t, d
 
 
 # ---------------------------------------------------------------- attention

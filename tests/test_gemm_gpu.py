@@ -44,3 +44,76 @@ def test_mx_gemm_matches_oracle(L, M, N, K):
     got = d.cpu().numpy().astype(np.float64)
     scale = np.abs(mx.dq_1x32(pa, sa)) @ np.abs(mx.dq_1x32(pb, sb)).T
     assert np.all(np.abs(got - want) <= 1e-5 * scale + 1e-30)
+
+
+# ------------------------------------------------------ quantizing epilogue
+def _operands(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((M, K)) * np.exp(rng.uniform(-3, 3, (M, 1)))
+    b = rng.standard_normal((N, K)) * np.exp(rng.uniform(-3, 3, (1, K)))
+    pa, sa = mx.quantize_1x32(a)
+    pb, sb = mx.quantize_1x32(b)
+    return pa, sa, pb, sb
+
+
+def _dev(z):
+    return torch.from_numpy(np.ascontiguousarray(z)).cuda()
+
+
+@pytest.mark.parametrize("block", ["1x32", "32x32"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (384, 768, 512)])
+def test_mx_gemm_quantize_matches_oracle(L, block, M, N, K):
+    """The fused output equals the oracle's quantization of the kernel's own
+    fp32 result bit for bit (the codes are decided on those values), and the
+    fp32 result is the GEMM within fp32 accumulation error."""
+    pa, sa, pb, sb = _operands(M, N, K, seed=M + N + K)
+    blk = {"1x32": L.LPFA_BLK_1X32, "32x32": L.LPFA_BLK_32X32}[block]
+    q, sf, sf_mma, sf_mma_t, d = L.mx_gemm_quantize(
+        _dev(pa), _dev(_gemm_sf_layout(sa)), _dev(pb), _dev(_gemm_sf_layout(sb)), blk,
+        with_fp32=True)
+    q2, sf2, sf_mma2, sf_mma_t2, _ = L.mx_gemm_quantize(
+        _dev(pa), _dev(_gemm_sf_layout(sa)), _dev(pb), _dev(_gemm_sf_layout(sb)), blk)
+    torch.cuda.synchronize()
+    dk = d.cpu().numpy().astype(np.float64)
+    want_d = mx.mx_gemm(pa, sa, pb, sb)
+    scale = np.abs(mx.dq_1x32(pa, sa)) @ np.abs(mx.dq_1x32(pb, sb)).T
+    assert np.all(np.abs(dk - want_d) <= 1e-5 * scale + 1e-30)
+    want = layouts.gemm_quantize(dk, block)
+    for got in ((q, sf, sf_mma, sf_mma_t), (q2, sf2, sf_mma2, sf_mma_t2)):
+        assert np.array_equal(got[0].cpu().numpy(), want["payload"])
+        assert np.array_equal(got[1].cpu().numpy(), want["sf"])
+        assert np.array_equal(got[2].cpu().numpy(), want["sf_mma"])
+        if block == "32x32":
+            assert np.array_equal(got[3].cpu().numpy(), want["sf_mma_t"])
+
+
+@pytest.mark.parametrize("block", ["1x32", "32x32"])
+def test_mx_gemm_quantize_output_feeds_the_next_gemm(L, block):
+    """The quantized result, with its tensor-core scale arrangement, as the
+    A operand of a second block-scaled GEMM: contraction over N with the rows
+    = M arrangement, and (square blocks) contraction over M with the
+    transposed payload and the rows = N arrangement."""
+    M, N, K, P = 256, 512, 256, 256
+    pa, sa, pb, sb = _operands(M, N, K, seed=3)
+    blk = {"1x32": L.LPFA_BLK_1X32, "32x32": L.LPFA_BLK_32X32}[block]
+    q, sf, sf_mma, sf_mma_t, _ = L.mx_gemm_quantize(
+        _dev(pa), _dev(_gemm_sf_layout(sa)), _dev(pb), _dev(_gemm_sf_layout(sb)), blk)
+    torch.cuda.synchronize()
+    qn, sfn = q.cpu().numpy(), sf.cpu().numpy()
+    rows_sc = sfn if block == "1x32" else np.repeat(sfn, 32, axis=0)      # [M, N/32]
+    pc, sc = mx.quantize_1x32(np.random.default_rng(5).standard_normal((P, N)))
+    e = torch.empty((M, P), dtype=torch.float32, device="cuda")
+    L.lpfa_mx_gemm(q, sf_mma, _dev(pc), _dev(_gemm_sf_layout(sc)), e)
+    torch.cuda.synchronize()
+    want = mx.mx_gemm(qn, rows_sc, pc, sc)
+    scale = np.abs(mx.dq_1x32(qn, rows_sc)) @ np.abs(mx.dq_1x32(pc, sc)).T
+    assert np.all(np.abs(e.cpu().numpy() - want) <= 1e-5 * scale + 1e-30)
+    if block == "32x32":
+        pt, st = mx.quantize_1x32(np.random.default_rng(6).standard_normal((P, M)))
+        f = torch.empty((N, P), dtype=torch.float32, device="cuda")
+        L.lpfa_mx_gemm(_dev(qn.T), sf_mma_t, _dev(pt), _dev(_gemm_sf_layout(st)), f)
+        torch.cuda.synchronize()
+        cols_sc = np.repeat(sfn.T, 32, axis=0)                            # [N, M/32]
+        want_t = mx.mx_gemm(qn.T, cols_sc, pt, st)
+        scale_t = np.abs(mx.dq_1x32(qn.T, cols_sc)) @ np.abs(mx.dq_1x32(pt, st)).T
+        assert np.all(np.abs(f.cpu().numpy() - want_t) <= 1e-5 * scale_t + 1e-30)
