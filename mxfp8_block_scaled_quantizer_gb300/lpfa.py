@@ -234,14 +234,16 @@ def rmsnorm_mx_quantize(x: torch.Tensor, weight: torch.Tensor, eps: float, block
                         seqs: Optional[Seqs] = None, compact: bool = True,
                         mma: bool = True, stream=None):
     """Fused RMSNorm + MX quantization of bf16 [B, S, H, D] or packed
-    [T, H, D] (with ``seqs``); the norm runs over each token's H * D values.
-    Returns (MXTensor of y, rstd fp32 [T])."""
+    [T, H, D] (``seqs`` for a jagged batch, else one sequence); the norm runs
+    over each token's H * D values.  Returns (MXTensor of y, rstd fp32 [T])."""
     if x.dim() == 4:
         B, S, H, D = x.shape
         if seqs is None:
             seqs = dense_seqs(B, S)
         x = x.reshape(B * S, H, D)
     T, H, D = x.shape
+    if seqs is None:
+        seqs = dense_seqs(1, T)
     x = x.contiguous()
     Tp = seqs.total_sf_rows
     dev = x.device
