@@ -190,13 +190,16 @@ def lpfa_mx_quantize(seqs: Seqs, x: torch.Tensor, block: int,
 def mx_quantize(x: torch.Tensor, block: int, seqs: Optional[Seqs] = None,
                 compact: bool = True, mma: bool = True,
                 stream=None) -> MXTensor:
-    """Quantize bf16 [B, S, H, D] or packed [T, H, D] (with ``seqs``)."""
+    """Quantize bf16 [B, S, H, D] or packed [T, H, D] (``seqs`` for a jagged
+    batch, else one sequence)."""
     if x.dim() == 4:
         B, S, H, D = x.shape
         if seqs is None:
             seqs = dense_seqs(B, S)
         x = x.reshape(B * S, H, D)
     T, H, D = x.shape
+    if seqs is None:
+        seqs = dense_seqs(1, T)
     x = x.contiguous()
     Tp = seqs.total_sf_rows
     dev = x.device
