@@ -91,9 +91,10 @@ def square_to_col(sq_sc, D):
     return np.repeat(sq_sc, 32, axis=2)[:, :, :D]
 
 
-def oracle_quantize(x, cu_seqlens, block):
+def oracle_quantize(x, cu_seqlens, block, fmt="e4m3"):
     """Oracle quantization of a token-major tensor x [T, H, D] with the
-    library's output layouts.  block: "1x32", "32x1" or "32x32".
+    library's output layouts.  block: "1x32", "32x1" or "32x32"; fmt: the
+    element format (``mx.FORMATS``).
     Returns dict(payload [T,H,D] uint8, sf (compact), sf_mma, sf_mma_t)."""
     from . import mx
     x = np.asarray(x, dtype=np.float64)
@@ -102,7 +103,7 @@ def oracle_quantize(x, cu_seqlens, block):
     sfs = sf_row_starts(cu)
     out = {"sf_mma_t": None}
     if block == "1x32":
-        p, sc = mx.quantize_1x32(x)
+        p, sc = mx.quantize_1x32(x, fmt)
         out.update(payload=p, sf=sc, sf_mma=mma_from_row_blocks(sc, cu))
         return out
     payload = np.zeros((T, H, D), dtype=np.uint8)
@@ -112,7 +113,7 @@ def oracle_quantize(x, cu_seqlens, block):
             a, b = cu[s], cu[s + 1]
             if b == a:
                 continue
-            p, c = mx.quantize_along_rows(x[a:b])
+            p, c = mx.quantize_along_rows(x[a:b], fmt=fmt)
             payload[a:b] = p
             sc[sfs[s] // 32: sfs[s] // 32 + c.shape[0]] = c
         out.update(payload=payload, sf=sc, sf_mma=mma_from_token_blocks(sc, D))
@@ -123,7 +124,7 @@ def oracle_quantize(x, cu_seqlens, block):
         a, b = cu[s], cu[s + 1]
         if b == a:
             continue
-        p, c = mx.quantize_32x32(np.moveaxis(x[a:b], 2, 1))   # [L, D, H]
+        p, c = mx.quantize_32x32(np.moveaxis(x[a:b], 2, 1), fmt)   # [L, D, H]
         payload[a:b] = np.moveaxis(p, 1, 2)
         sc[sfs[s] // 32: sfs[s] // 32 + c.shape[0]] = np.moveaxis(c, 1, 2)
     row = square_to_row(sc, cu)

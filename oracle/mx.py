@@ -29,6 +29,9 @@ Readings where the pages are silent (each one is listed in the design notes):
   saturated to 448 (no NaN is produced from a finite input); the sign of zero
   is kept (-tiny encodes as 0x80).
 
+* The other OCP MX element formats (E5M2, FP6 E3M2 / E2M3, FP4 E2M1) follow
+  the same block rule with their own emax; see ``FORMATS``.
+
 Parity pins for this module live in ``tests/test_oracle_mx.py``.
 """
 from __future__ import annotations
@@ -87,35 +90,118 @@ def e4m3_encode(x) -> np.ndarray:
     return code
 
 
-def scale_exponent(amax) -> tuple:
-    """(e, code) for block maxima amax >= 0: e = floor(log2 amax) - 8, clamped
-    to [-127, 127]; amax == 0 -> e = -127; non-finite amax -> code 0xFF."""
+# --------------------------------------------------- other MX element formats
+# The OCP MX element formats besides E4M3 ("Low-Precision FlashAttention-4
+# ...", which names MXFP8, MXFP6 and MXFP4 as the block-scaled MMA formats;
+# "Low Precision Flash Attention 4 ...", paragraph 1), written from their
+# definitions: sign, exponent field with bias, mantissa field; emax is the
+# exponent of the largest finite binade, which the scale rule subtracts.
+#   E5M2  5 exponent bits (bias 15), 2 mantissa bits, IEEE-like: exponent
+#         field 31 holds Inf (mantissa 0) and NaN; max 57344; emax 15.
+#   E3M2  (FP6) 3 / bias 3 / 2 bits, no Inf or NaN; max 28; emax 4.
+#   E2M3  (FP6) 2 / bias 1 / 3 bits, no Inf or NaN; max 7.5; emax 2.
+#   E2M1  (FP4) 2 / bias 1 / 1 bit, no Inf or NaN; max 6; emax 2.
+# Codes hold one element each in the low bits of a byte (sign bit on top of
+# the element's field).  A block holding Inf or NaN gets scale code 0xFF; its
+# payload bytes are the format's NaN code (E5M2: 0x7F) or, for the formats
+# without NaN, the largest positive code.
+FORMATS = {
+    # name: (exponent bits, mantissa bits, bias, emax, kind)
+    "e4m3": (4, 3, 7, 8, "fn"),
+    "e5m2": (5, 2, 15, 15, "ieee"),
+    "e3m2": (3, 2, 3, 4, "finite"),
+    "e2m3": (2, 3, 1, 2, "finite"),
+    "e2m1": (2, 1, 1, 2, "finite"),
+}
+
+
+def _fmt_value(code: int, fmt: str) -> float:
+    eb, mb, bias, _, kind = FORMATS[fmt]
+    nbits = 1 + eb + mb
+    sign = -1.0 if (code >> (nbits - 1)) & 1 else 1.0
+    ef = (code >> mb) & ((1 << eb) - 1)
+    m = code & ((1 << mb) - 1)
+    if kind == "ieee" and ef == (1 << eb) - 1:
+        return sign * float("inf") if m == 0 else float("nan")
+    if kind == "fn" and ef == (1 << eb) - 1 and m == (1 << mb) - 1:
+        return float("nan")
+    if ef == 0:
+        return sign * (m / 2.0 ** mb) * 2.0 ** (1 - bias)
+    return sign * (1.0 + m / 2.0 ** mb) * 2.0 ** (ef - bias)
+
+
+def fmt_table(fmt: str) -> np.ndarray:
+    """Decoded value of every code of the format (fp64, exact)."""
+    eb, mb, _, _, _ = FORMATS[fmt]
+    return np.array([_fmt_value(c, fmt) for c in range(1 << (1 + eb + mb))], dtype=np.float64)
+
+
+def fmt_nan_payload(fmt: str) -> int:
+    """Payload byte of a block whose scale is NaN (0xFF)."""
+    eb, mb, _, _, kind = FORMATS[fmt]
+    if kind in ("fn", "ieee"):
+        return 0x7F
+    return (1 << (eb + mb)) - 1          # largest positive code
+
+
+def fmt_encode(x, fmt: str) -> np.ndarray:
+    """Round fp64 values to the format's codes: nearest, ties to the even
+    code, magnitudes above the largest finite value saturate to it, the sign
+    is kept (also of zero)."""
+    if fmt == "e4m3":
+        return e4m3_encode(x)
+    eb, mb, _, _, _ = FORMATS[fmt]
+    nbits = 1 + eb + mb
+    table = fmt_table(fmt)
+    npos = 1 << (nbits - 1)
+    pos = table[:npos]
+    finite = np.isfinite(pos)
+    pos = pos[finite]                    # non-negative finite magnitudes, increasing
+    last = len(pos) - 1
+    assert np.all(np.diff(pos) > 0)
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    ok = ~np.isnan(a)
+    a_safe = np.where(ok, a, 0.0)
+    lo = np.clip(np.searchsorted(pos, a_safe, side="right") - 1, 0, last)
+    hi = np.minimum(lo + 1, last)
+    mid = 0.5 * (pos[lo] + pos[hi])
+    pick_hi = (hi != lo) & ((a_safe > mid) | ((a_safe == mid) & (hi % 2 == 0)))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x), code | np.uint8(1 << (nbits - 1)), code).astype(np.uint8)
+    return np.where(ok, code, np.uint8(fmt_nan_payload(fmt))).astype(np.uint8)
+
+
+def scale_exponent(amax, emax: int = EMAX_E4M3) -> tuple:
+    """(e, code) for block maxima amax >= 0: e = floor(log2 amax) - emax
+    (8 for E4M3), clamped to [-127, 127]; amax == 0 -> e = -127; non-finite
+    amax -> code 0xFF."""
     amax = np.asarray(amax, dtype=np.float64)
     finite = np.isfinite(amax)
     safe = np.where(finite & (amax > 0), amax, 1.0)
     _, fexp = np.frexp(safe)           # safe = f * 2^fexp, f in [0.5, 1)
     floor_log2 = fexp - 1
-    e = floor_log2 - EMAX_E4M3
+    e = floor_log2 - emax
     e = np.where(finite & (amax > 0), e, -E8M0_BIAS)
     e = np.clip(e, -127, 127)
     code = np.where(finite, e + E8M0_BIAS, E8M0_NAN).astype(np.uint8)
     return e.astype(np.int64), code
 
 
-def _quantize_grouped(xg: np.ndarray):
+def _quantize_grouped(xg: np.ndarray, fmt: str = "e4m3"):
     """Quantize blocks laid out as the last axis of ``xg`` (shape [..., n]).
     Returns (payload codes [..., n], scale codes [...])."""
     amax = np.max(np.abs(xg), axis=-1) if xg.shape[-1] else np.zeros(xg.shape[:-1])
-    e, code = scale_exponent(amax)
+    e, code = scale_exponent(amax, FORMATS[fmt][3])
     scaled = np.ldexp(xg, -e[..., None])       # exact power-of-two scaling
-    payload = e4m3_encode(scaled)
+    payload = fmt_encode(scaled, fmt)
     bad = code == E8M0_NAN
     if np.any(bad):
-        payload = np.where(bad[..., None], np.uint8(E4M3_NAN), payload)
+        payload = np.where(bad[..., None], np.uint8(fmt_nan_payload(fmt)), payload)
     return payload.astype(np.uint8), code
 
 
-def quantize_1x32(x) -> tuple:
+def quantize_1x32(x, fmt: str = "e4m3") -> tuple:
     """1x32 blocks along the last axis (length a multiple of 32).
 
     Returns (payload uint8 same shape, scale codes [..., n/32])."""
@@ -123,11 +209,11 @@ def quantize_1x32(x) -> tuple:
     n = x.shape[-1]
     assert n % 32 == 0
     xg = x.reshape(*x.shape[:-1], n // 32, 32)
-    payload, code = _quantize_grouped(xg)
+    payload, code = _quantize_grouped(xg, fmt)
     return payload.reshape(x.shape), code
 
 
-def quantize_along_rows(x, block: int = 32) -> tuple:
+def quantize_along_rows(x, block: int = 32, fmt: str = "e4m3") -> tuple:
     """Blocks of ``block`` consecutive rows (axis 0) per column, starting at
     row 0; the last block may be short (ragged sequence end).
 
@@ -139,12 +225,12 @@ def quantize_along_rows(x, block: int = 32) -> tuple:
     xp = np.concatenate([x, np.zeros((pad,) + x.shape[1:])], 0) if pad else x
     # zero padding cannot raise a block's amax; padded outputs are dropped
     xg = np.moveaxis(xp.reshape(nb, block, *x.shape[1:]), 1, -1)
-    payload, code = _quantize_grouped(xg)
+    payload, code = _quantize_grouped(xg, fmt)
     payload = np.moveaxis(payload, -1, 1).reshape(nb * block, *x.shape[1:])[:r]
     return payload, code
 
 
-def quantize_32x32(x) -> tuple:
+def quantize_32x32(x, fmt: str = "e4m3") -> tuple:
     """Square 32x32 blocks over the first two axes of x [R, C, ...]; blocks
     start at (0, 0); the last row-block may be short, C must be a multiple
     of 32.  Returns (payload [R, C, ...], scales [ceil(R/32), C/32, ...])."""
@@ -159,7 +245,7 @@ def quantize_32x32(x) -> tuple:
     xg = xp.reshape(nb, 32, c // 32, 32, *rest)
     xg = np.moveaxis(xg, (1, 3), (-2, -1))
     xg = xg.reshape(nb, c // 32, *rest, 1024)
-    payload, code = _quantize_grouped(xg)
+    payload, code = _quantize_grouped(xg, fmt)
     payload = payload.reshape(nb, c // 32, *rest, 32, 32)
     payload = np.moveaxis(payload, (-2, -1), (1, 3)).reshape(nb * 32, c, *rest)
     return payload[:r], code

@@ -249,3 +249,84 @@ def test_gemm_quantize_layouts(block, rng):
         t = layouts.gemm_quantize(d.T, "32x32")
         assert np.array_equal(t["payload"], out["payload"].T)
         assert np.array_equal(t["sf_mma"], out["sf_mma_t"])
+
+
+# ------------------------------------------------- other MX element formats
+def _golden_formats():
+    rows, e2m1 = {}, None
+    with open(os.path.join(GOLDEN, "mx_element_formats.txt")) as fh:
+        for line in fh:
+            t = line.split()
+            if not t or t[0].startswith("#"):
+                continue
+            if t[0] == "e2m1_values":
+                e2m1 = [float(v) for v in t[1:]]
+            else:
+                rows[t[0]] = tuple(float(v) for v in t[1:])
+    return rows, e2m1
+
+
+def test_element_format_landmarks_match_golden():
+    rows, e2m1 = _golden_formats()
+    for fmt, (mx_max, mn_norm, mn_sub, emax, n) in rows.items():
+        t = mx.fmt_table(fmt)
+        fin = t[np.isfinite(t)]
+        assert len(t) == n and fin.max() == mx_max and fin[fin > 0].min() == mn_sub
+        eb, mb, bias, fe, _ = mx.FORMATS[fmt]
+        assert fe == emax and _fmt_min_normal(fmt) == mn_norm
+    assert list(mx.fmt_table("e2m1")[:8]) == e2m1
+
+
+def _fmt_min_normal(fmt):
+    eb, mb, bias, _, _ = mx.FORMATS[fmt]
+    return mx.fmt_table(fmt)[1 << mb]          # exponent field 1, mantissa 0
+
+
+def test_e5m2_decode_matches_torch_all_codes():
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy()
+    ours = mx.fmt_table("e5m2")
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e3m2", "e2m3", "e2m1"])
+def test_element_encode_is_nearest_even_with_saturation(fmt, rng):
+    t = mx.fmt_table(fmt)
+    nbits = int(np.log2(len(t)))
+    pos = t[:len(t) // 2]
+    fin = np.isfinite(pos)
+    vmax = pos[fin].max()
+    x = np.concatenate([rng.standard_normal(3000) * vmax / 2, rng.uniform(-2 * vmax, 2 * vmax, 500),
+                        (pos[fin][1:] + pos[fin][:-1]) / 2,       # exact midpoints
+                        -(pos[fin][1:] + pos[fin][:-1]) / 2, [0.0, -0.0]])
+    got = mx.fmt_encode(x, fmt)
+    for xi, c in zip(x, got):
+        a = min(abs(xi), vmax)
+        d = np.abs(pos[fin] - a)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else best[best % 2 == 0][0]
+        assert (c & ((1 << (nbits - 1)) - 1)) == want
+        assert bool(c >> (nbits - 1)) == bool(np.signbit(xi))
+
+
+def test_e5m2_encode_matches_torch_in_range(rng):
+    x = rng.standard_normal(4000) * np.exp(rng.uniform(-12, 12, 4000))
+    x = x[np.abs(x) <= 57344.0]
+    ref = torch.from_numpy(x).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    assert np.array_equal(mx.fmt_encode(x, "e5m2"), ref)
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e3m2", "e2m3", "e2m1"])
+def test_scale_rule_per_format(fmt):
+    emax = mx.FORMATS[fmt][3]
+    for k in range(-40, 41, 7):
+        e, code = mx.scale_exponent(np.array([1.5 * 2.0 ** k]), emax)
+        assert e[0] == max(k - emax, -127) and code[0] == e[0] + 127
+    # the block maximum lands in the top binade of the format: amax * 2^-e
+    # in [2^emax, 2^(emax+1))
+    x = np.random.default_rng(3).standard_normal((50, 32)) * 7.0
+    p, sc = mx.quantize_1x32(x, fmt)
+    amax = np.abs(x).max(axis=1)
+    r = amax * 2.0 ** -(sc.astype(np.int64)[:, 0] - 127)
+    assert np.all((r >= 2.0 ** emax) & (r < 2.0 ** (emax + 1)))
