@@ -147,6 +147,36 @@ lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
                              void* out_sf_mma_t, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The same quantizer for the other OCP MX element formats ([P2] names
+ * MXFP8, MXFP6 and MXFP4 as the block-scaled MMA formats): identical block
+ * shapes, outputs and layouts, one element per payload byte in its low bits
+ * (sign on top of the element's field).  The scale exponent subtracts the
+ * format's emax instead of E4M3's 8:
+ *   LPFA_ELEM_E4M3  emax 8,  max 448    (lpfa_mx_quantize)
+ *   LPFA_ELEM_E5M2  emax 15, max 57344  (IEEE-like Inf/NaN)
+ *   LPFA_ELEM_E3M2  emax 4,  max 28     (FP6, no Inf/NaN)
+ *   LPFA_ELEM_E2M3  emax 2,  max 7.5    (FP6, no Inf/NaN)
+ *   LPFA_ELEM_E2M1  emax 2,  max 6      (FP4, no Inf/NaN)
+ * Elements round to nearest even and saturate to the largest finite
+ * magnitude; a block holding Inf or NaN gets scale 0xFF and payload bytes
+ * 0x7F (E4M3, E5M2) or the largest positive code (0x1F FP6, 0x07 FP4).
+ * Errors: as lpfa_mx_quantize; fmt outside the enum -> INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+typedef enum lpfa_elem {
+  LPFA_ELEM_E4M3 = 0,
+  LPFA_ELEM_E5M2 = 1,
+  LPFA_ELEM_E3M2 = 2,
+  LPFA_ELEM_E2M3 = 3,
+  LPFA_ELEM_E2M1 = 4
+} lpfa_elem;
+
+lpfa_status lpfa_mx_quantize_fmt(const lpfa_seqs* seqs, const void* x,
+                                 int64_t heads, int64_t head_dim,
+                                 lpfa_block blk, lpfa_elem fmt, void* out,
+                                 void* out_sf, void* out_sf_mma,
+                                 void* out_sf_mma_t, void* stream);
+
+/* ------------------------------------------------------------------------
  * Fused RMSNorm + MX quantization ([P1] paragraph 2: fused RMSNorm+Quantize
  * kernels producing FP8 output with dual scale factor layouts in one pass).
  *

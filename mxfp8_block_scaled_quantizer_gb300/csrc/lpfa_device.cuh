@@ -613,6 +613,63 @@ __device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c,
          (static_cast<uint32_t>(cvt_e4m3x2(c, d)) << 16);
 }
 
+// ---------------------------------------------- other MX element formats
+// Quantizer element formats, one element per output byte (low bits, sign on
+// top of the element's field): E4M3, E5M2 (IEEE-like Inf/NaN), FP6 E3M2 and
+// E2M3, FP4 E2M1 (no Inf/NaN).  emax = exponent of the largest finite binade.
+enum : int { kFmtE4M3 = 0, kFmtE5M2 = 1, kFmtE3M2 = 2, kFmtE2M3 = 3, kFmtE2M1 = 4 };
+
+template <int F>
+constexpr uint32_t fmt_emax() {
+  return F == kFmtE4M3 ? 8u : F == kFmtE5M2 ? 15u : F == kFmtE3M2 ? 4u : 2u;
+}
+
+// Payload byte of a block whose scale code is 0xFF: the format's NaN, or for
+// the formats without NaN their largest positive code.
+template <int F>
+constexpr uint32_t fmt_nan_byte() {
+  return F == kFmtE4M3 || F == kFmtE5M2 ? 0x7Fu : F == kFmtE2M1 ? 0x07u : 0x1Fu;
+}
+
+// E8M0 code floor(log2 amax) - emax + 127 from amax's fp32 bits (clamped at
+// 0; Inf/NaN -> 0xFF).
+template <int F>
+__device__ __forceinline__ uint32_t scale_code_from_amax_bits(uint32_t bits) {
+  constexpr uint32_t emax = fmt_emax<F>();
+  const uint32_t ef = (bits >> 23) & 0xFFu;
+  if (ef == 0xFFu) return 0xFFu;
+  return ef > emax ? ef - emax : 0u;
+}
+
+// Four fp32 -> four element bytes (a in byte 0), round to nearest even,
+// saturating to the format's largest finite magnitude.
+template <int F>
+__device__ __forceinline__ uint32_t cvt_x4(float a, float b, float c, float d) {
+  if constexpr (F == kFmtE4M3) {
+    return cvt_e4m3x4(a, b, c, d);
+  } else if constexpr (F == kFmtE2M1) {
+    uint16_t lo, hi;   // two FP4 codes per byte: first operand in the low nibble
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(lo) : "f"(a), "f"(b));
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.u16.u8 %0, t;\n\t}"
+        : "=h"(hi) : "f"(c), "f"(d));
+    return (lo & 0xFu) | ((lo >> 4) & 0xFu) << 8 | (hi & 0xFu) << 16 | ((hi >> 4) & 0xFu) << 24;
+  } else {
+    uint16_t lo, hi;
+    if constexpr (F == kFmtE5M2) {
+      asm("cvt.rn.satfinite.e5m2x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
+      asm("cvt.rn.satfinite.e5m2x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
+    } else if constexpr (F == kFmtE3M2) {
+      asm("cvt.rn.satfinite.e3m2x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
+      asm("cvt.rn.satfinite.e3m2x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
+    } else {
+      asm("cvt.rn.satfinite.e2m3x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
+      asm("cvt.rn.satfinite.e2m3x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
+    }
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+}
+
 // Warp-wide maximum of |x| (NaN-propagating).
 __device__ __forceinline__ float warp_max_abs(float x) {
   float r;

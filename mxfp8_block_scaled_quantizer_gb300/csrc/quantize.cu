@@ -39,7 +39,8 @@ __device__ __forceinline__ uint32_t abs_bits(float f) {
   return __float_as_uint(f) & 0x7FFFFFFFu;
 }
 
-// Quantize 32 floats with one scale code into 32 bytes (8 words).
+// Quantize 32 floats with their scale codes into 32 element bytes (8 words).
+template <int kFmt = kFmtE4M3>
 __device__ __forceinline__ void quant_row(const float (&f)[32],
                                           const uint32_t (&code)[32],
                                           uint32_t (&w)[8]) {
@@ -49,15 +50,17 @@ __device__ __forceinline__ void quant_row(const float (&f)[32],
     float b = f[4 * j + 1] * inv_scale_from_code(code[4 * j + 1]);
     float c = f[4 * j + 2] * inv_scale_from_code(code[4 * j + 2]);
     float d = f[4 * j + 3] * inv_scale_from_code(code[4 * j + 3]);
-    w[j] = cvt_e4m3x4(a, b, c, d);
+    w[j] = cvt_x4<kFmt>(a, b, c, d);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (code[4 * j + q] == 0xFFu) w[j] = (w[j] & ~(0xFFu << (8 * q))) | (0x7Fu << (8 * q));
+      if (code[4 * j + q] == 0xFFu)
+        w[j] = (w[j] & ~(0xFFu << (8 * q))) | (fmt_nan_byte<kFmt>() << (8 * q));
   }
 }
 
 // As quant_row with the codes of the 32 values packed four to a word
 // (element 4i + q takes byte q of cw[i]).
+template <int kFmt = kFmtE4M3>
 __device__ __forceinline__ void quant_row_packed(const float (&f)[32], const uint32_t (&cw)[8],
                                                  uint32_t (&w)[8]) {
 #pragma unroll
@@ -65,10 +68,11 @@ __device__ __forceinline__ void quant_row_packed(const float (&f)[32], const uin
     float x[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) x[q] = f[4 * i + q] * inv_scale_from_code((cw[i] >> (8 * q)) & 0xFFu);
-    w[i] = cvt_e4m3x4(x[0], x[1], x[2], x[3]);
+    w[i] = cvt_x4<kFmt>(x[0], x[1], x[2], x[3]);
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      if (((cw[i] >> (8 * q)) & 0xFFu) == 0xFFu) w[i] = (w[i] & ~(0xFFu << (8 * q))) | (0x7Fu << (8 * q));
+      if (((cw[i] >> (8 * q)) & 0xFFu) == 0xFFu)
+        w[i] = (w[i] & ~(0xFFu << (8 * q))) | (fmt_nan_byte<kFmt>() << (8 * q));
   }
 }
 
@@ -89,7 +93,7 @@ __device__ __forceinline__ void unpack_row(const uint4 (&v)[4], float (&f)[32]) 
 // (Token-per-lane loads, 64 bytes at the token stride, reach ~2/3 of the
 // bandwidth of these.)  Block maxima over tokens reduce across the lanes
 // that share cb.
-template <int kMode, int kNcb>  // mode 0: 1x32, 1: 32x1, 2: 32x32
+template <int kMode, int kNcb, int kFmt>  // mode 0: 1x32, 1: 32x1, 2: 32x32
 __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per SM
     mx_quantize_kernel(const QuantArgs a) {
   constexpr int kTpl = 32 / kNcb;                  // tokens per load
@@ -138,7 +142,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
     }
 #pragma unroll
     for (int x = kNcb; x < 32; x <<= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, x));
-    bcode = e8m0_code_from_amax_bits(m);
+    bcode = scale_code_from_amax_bits<kFmt>(m);
   } else if (kMode == 1) {
     // per channel: maximum over this lane's rows, then over the lanes
     // sharing cb; four channels at a time keeps the live state small
@@ -160,7 +164,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
         uint32_t qq = q[k];
 #pragma unroll
         for (int x = kNcb; x < 32; x <<= 1) qq = max(qq, __shfl_xor_sync(0xFFFFFFFFu, qq, x));
-        word |= e8m0_code_from_amax_bits(qq) << (8 * k);
+        word |= scale_code_from_amax_bits<kFmt>(qq) << (8 * k);
       }
       cw[g4] = word;
     }
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
       uint32_t m = 0;
 #pragma unroll
       for (int j = 0; j < 32; ++j) m = max(m, abs_bits(f[j]));
-      const uint32_t c = e8m0_code_from_amax_bits(m);
+      const uint32_t c = scale_code_from_amax_bits<kFmt>(m);
 #pragma unroll
       for (int j = 0; j < 32; ++j) code[j] = c;
     } else if (kMode == 2) {
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
     }
     if (valid) {
       uint32_t w[8];
-      if (kMode == 1) quant_row_packed(f, cw, w);
-      else quant_row(f, code, w);
+      if (kMode == 1) quant_row_packed<kFmt>(f, cw, w);
+      else quant_row<kFmt>(f, code, w);
       uint4* dst = reinterpret_cast<uint4*>(a.out + (tok * a.H + h) * a.D + 32 * cb);
       __stcs(dst + 0, make_uint4(w[0], w[1], w[2], w[3]));
       __stcs(dst + 1, make_uint4(w[4], w[5], w[6], w[7]));
@@ -467,11 +471,41 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)
 
 using namespace lpfa;
 
+namespace {
+template <int kFmt>
+void launch_quantize(lpfa_block blk, bool d128, dim3 grid, dim3 block, cudaStream_t cs,
+                     const QuantArgs& a) {
+  switch (blk) {
+    case LPFA_BLK_1X32:
+      if (d128) mx_quantize_kernel<0, 4, kFmt><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<0, 2, kFmt><<<grid, block, 0, cs>>>(a);
+      break;
+    case LPFA_BLK_32X1:
+      if (d128) mx_quantize_kernel<1, 4, kFmt><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<1, 2, kFmt><<<grid, block, 0, cs>>>(a);
+      break;
+    case LPFA_BLK_32X32:
+      if (d128) mx_quantize_kernel<2, 4, kFmt><<<grid, block, 0, cs>>>(a);
+      else mx_quantize_kernel<2, 2, kFmt><<<grid, block, 0, cs>>>(a);
+      break;
+  }
+}
+}  // namespace
+
 extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
                                         int64_t heads, int64_t head_dim,
                                         lpfa_block blk, void* out_e4m3,
                                         void* out_sf, void* out_sf_mma,
                                         void* out_sf_mma_t, void* stream) {
+  return lpfa_mx_quantize_fmt(seqs, x, heads, head_dim, blk, LPFA_ELEM_E4M3, out_e4m3, out_sf,
+                              out_sf_mma, out_sf_mma_t, stream);
+}
+
+extern "C" lpfa_status lpfa_mx_quantize_fmt(const lpfa_seqs* seqs, const void* x,
+                                            int64_t heads, int64_t head_dim,
+                                            lpfa_block blk, lpfa_elem fmt, void* out_e4m3,
+                                            void* out_sf, void* out_sf_mma,
+                                            void* out_sf_mma_t, void* stream) {
   SeqView sv;
   lpfa_status st = make_seq_view(seqs, &sv);
   if (st != LPFA_OK) return st;
@@ -481,6 +515,7 @@ extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
   LPFA_CHECK_ARG(blk == LPFA_BLK_1X32 || blk == LPFA_BLK_32X1 ||
                  blk == LPFA_BLK_32X32);
   LPFA_CHECK_ARG(out_sf_mma_t == nullptr || blk == LPFA_BLK_32X32);
+  LPFA_CHECK_ARG(fmt >= LPFA_ELEM_E4M3 && fmt <= LPFA_ELEM_E2M1);
   if (head_dim != 64 && head_dim != 128) return LPFA_ERR_UNSUPPORTED;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (sv.total_tokens == 0) return LPFA_OK;
@@ -510,19 +545,12 @@ extern "C" lpfa_status lpfa_mx_quantize(const lpfa_seqs* seqs, const void* x,
   LPFA_CHECK_ARG(blocks < (1ll << 31));
   dim3 grid(static_cast<unsigned>(blocks)), block(kWarpsPerBlock * 32);
   const bool d128 = head_dim == 128;
-  switch (blk) {
-    case LPFA_BLK_1X32:
-      if (d128) mx_quantize_kernel<0, 4><<<grid, block, 0, cs>>>(a);
-      else mx_quantize_kernel<0, 2><<<grid, block, 0, cs>>>(a);
-      break;
-    case LPFA_BLK_32X1:
-      if (d128) mx_quantize_kernel<1, 4><<<grid, block, 0, cs>>>(a);
-      else mx_quantize_kernel<1, 2><<<grid, block, 0, cs>>>(a);
-      break;
-    case LPFA_BLK_32X32:
-      if (d128) mx_quantize_kernel<2, 4><<<grid, block, 0, cs>>>(a);
-      else mx_quantize_kernel<2, 2><<<grid, block, 0, cs>>>(a);
-      break;
+  switch (fmt) {
+    case LPFA_ELEM_E4M3: launch_quantize<kFmtE4M3>(blk, d128, grid, block, cs, a); break;
+    case LPFA_ELEM_E5M2: launch_quantize<kFmtE5M2>(blk, d128, grid, block, cs, a); break;
+    case LPFA_ELEM_E3M2: launch_quantize<kFmtE3M2>(blk, d128, grid, block, cs, a); break;
+    case LPFA_ELEM_E2M3: launch_quantize<kFmtE2M3>(blk, d128, grid, block, cs, a); break;
+    case LPFA_ELEM_E2M1: launch_quantize<kFmtE2M1>(blk, d128, grid, block, cs, a); break;
   }
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;

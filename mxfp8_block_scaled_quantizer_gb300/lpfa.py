@@ -27,6 +27,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 LPFA_OK, LPFA_ERR_INVALID_ARG, LPFA_ERR_UNSUPPORTED, LPFA_ERR_CUDA, \
     LPFA_ERR_TIMEOUT = range(5)
 LPFA_BLK_1X32, LPFA_BLK_32X1, LPFA_BLK_32X32 = range(3)
+LPFA_ELEM_E4M3, LPFA_ELEM_E5M2, LPFA_ELEM_E3M2, LPFA_ELEM_E2M3, LPFA_ELEM_E2M1 = range(5)
 from . import FWD_KV_TILE  # noqa: E402  (key tile of the forward softmax)
 
 _vp = ctypes.c_void_p
@@ -61,6 +62,9 @@ _varlen_sf_rows = _sig("lpfa_varlen_sf_rows", ctypes.c_int, _vp, _i64, _vp, _vp)
 _mx_quantize = _sig("lpfa_mx_quantize", ctypes.c_int,
                     ctypes.POINTER(lpfa_seqs), _vp, _i64, _i64, ctypes.c_int,
                     _vp, _vp, _vp, _vp, _vp)
+_mx_quantize_fmt = _sig("lpfa_mx_quantize_fmt", ctypes.c_int,
+                        ctypes.POINTER(lpfa_seqs), _vp, _i64, _i64, ctypes.c_int, ctypes.c_int,
+                        _vp, _vp, _vp, _vp, _vp)
 _rms_quantize = _sig("lpfa_rmsnorm_mx_quantize", ctypes.c_int,
                      ctypes.POINTER(lpfa_seqs), _vp, _vp, _i64, _i64, ctypes.c_float,
                      ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
@@ -85,7 +89,8 @@ _bwd_noalloc = _sig("lpfa_bwd_noalloc", ctypes.c_int,
 
 #: every symbol include/lpfa.h declares
 EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
-            "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_rmsnorm_mx_quantize",
+            "lpfa_varlen_sf_rows", "lpfa_mx_quantize", "lpfa_mx_quantize_fmt",
+            "lpfa_rmsnorm_mx_quantize",
             "lpfa_mx_gemm", "lpfa_mx_gemm_quantize",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc")
@@ -177,19 +182,25 @@ class MXTensor:
 
 def lpfa_mx_quantize(seqs: Seqs, x: torch.Tensor, block: int,
                      out: torch.Tensor, sf=None, sf_mma=None, sf_mma_t=None,
-                     stream=None):
-    """Raw call: x bf16 [T, H, D] (contiguous, CUDA); outputs preallocated."""
+                     stream=None, fmt: int = LPFA_ELEM_E4M3):
+    """Raw call: x bf16 [T, H, D] (contiguous, CUDA); outputs preallocated;
+    fmt selects the element format (E4M3 through lpfa_mx_quantize)."""
     assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
     T, H, D = x.shape
     sc = seqs.c()
-    _ok(_mx_quantize(ctypes.byref(sc), _ptr(x), H, D, block, _ptr(out),
-                     _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _stream(stream)),
-        "lpfa_mx_quantize")
+    if fmt == LPFA_ELEM_E4M3:
+        _ok(_mx_quantize(ctypes.byref(sc), _ptr(x), H, D, block, _ptr(out),
+                         _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _stream(stream)),
+            "lpfa_mx_quantize")
+    else:
+        _ok(_mx_quantize_fmt(ctypes.byref(sc), _ptr(x), H, D, block, fmt, _ptr(out),
+                             _ptr(sf), _ptr(sf_mma), _ptr(sf_mma_t), _stream(stream)),
+            "lpfa_mx_quantize_fmt")
 
 
 def mx_quantize(x: torch.Tensor, block: int, seqs: Optional[Seqs] = None,
                 compact: bool = True, mma: bool = True,
-                stream=None) -> MXTensor:
+                stream=None, fmt: int = LPFA_ELEM_E4M3) -> MXTensor:
     """Quantize bf16 [B, S, H, D] or packed [T, H, D] (``seqs`` for a jagged
     batch, else one sequence)."""
     if x.dim() == 4:
@@ -214,7 +225,7 @@ def mx_quantize(x: torch.Tensor, block: int, seqs: Optional[Seqs] = None,
         if block == LPFA_BLK_32X32:
             sf_mma_t = torch.empty((Tp // 128, H, 512), dtype=torch.uint8,
                                    device=dev)
-    lpfa_mx_quantize(seqs, x, block, out, sf, sf_mma, sf_mma_t, stream)
+    lpfa_mx_quantize(seqs, x, block, out, sf, sf_mma, sf_mma_t, stream, fmt)
     return MXTensor(out, sf, sf_mma, sf_mma_t, block, seqs)
 
 

@@ -140,3 +140,31 @@ def test_quantizer_empty_and_single_token(L):
     x = torch.randn(1, 3, 128).to(torch.bfloat16)
     for block in BLOCKS:
         _check(L, x, np.array([0, 1]), block, f"single-{block}")
+
+
+FORMATS = {"e5m2": 1, "e3m2": 2, "e2m3": 3, "e2m1": 4}
+
+
+@pytest.mark.parametrize("fmt", list(FORMATS))
+@pytest.mark.parametrize("block", list(BLOCKS))
+def test_quantizer_other_element_formats(L, fmt, block):
+    """E5M2, FP6 (E3M2, E2M3) and FP4 (E2M1) payloads and scales bit-exact
+    on the outlier workload's Q (wide dynamic range), a ragged packed batch
+    and the edge tensor (zeros, Inf/NaN blocks, saturation)."""
+    w = workloads.get_config("outlier")
+    x = workloads.make_inputs(w)
+    edge = _edge_tensor().clone()
+    edge[40, 0, 3] = float("nan")
+    edge[41, 1, 40] = float("inf")
+    cases = [(x["q"].reshape(-1, *x["q"].shape[2:])[:300], [0, 300]), (edge, None)]
+    for i, (xt, cu) in enumerate(cases):
+        xc = xt.cuda().contiguous()
+        seqs = L.dense_seqs(1, xc.shape[0]) if cu is None else \
+            L.varlen_seqs(torch.as_tensor(cu, dtype=torch.int32))
+        m = L.mx_quantize(xc, BLOCKS[block], seqs, fmt=FORMATS[fmt])
+        torch.cuda.synchronize()
+        got = {k: (None if getattr(m, k) is None else getattr(m, k).cpu().numpy())
+               for k in ("data", "sf", "sf_mma", "sf_mma_t")}
+        cu_o = np.array([0, xt.shape[0]]) if cu is None else np.asarray(cu)
+        want = layouts.oracle_quantize(xt.float().numpy(), cu_o, block, fmt)
+        _compare(got, want, f"{fmt}.{block}.{i}")
