@@ -64,3 +64,35 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert st == lib.LPFA_ERR_UNSUPPORTED          # head_dim 96
     st = lib._mx_gemm(None, None, None, None, None, 128, 256, 128, None)
     assert st == lib.LPFA_ERR_INVALID_ARG
+
+
+def test_new_entry_points_reject_bad_arguments_before_launch(lib):
+    """The element-format quantizer, the fused RMSNorm quantizer and the
+    quantizing GEMM check their arguments on the host (no GPU needed)."""
+    s = lib.lpfa_seqs(1, 128, 128, 128, None, None)
+    p = ctypes.c_void_p(256)                           # aligned, never dereferenced
+    # element format outside the enum
+    st = lib._mx_quantize_fmt(ctypes.byref(s), p, 1, 128, 0, 7, p, None, None, None, None)
+    assert st == lib.LPFA_ERR_INVALID_ARG
+    # transposed scale layout requested for 1x32 blocks
+    st = lib._mx_quantize_fmt(ctypes.byref(s), p, 1, 128, 0, 1, p, None, None, p, None)
+    assert st == lib.LPFA_ERR_INVALID_ARG
+    # fused RMSNorm: eps <= 0, missing weight, 32x1 blocks, head_dim 96
+    st = lib._rms_quantize(ctypes.byref(s), p, p, 1, 128, 0.0, 0, p, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_INVALID_ARG
+    st = lib._rms_quantize(ctypes.byref(s), p, None, 1, 128, 1e-6, 0, p, None, None, None, None,
+                           None)
+    assert st == lib.LPFA_ERR_INVALID_ARG
+    st = lib._rms_quantize(ctypes.byref(s), p, p, 1, 128, 1e-6, 1, p, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_UNSUPPORTED
+    st = lib._rms_quantize(ctypes.byref(s), p, p, 1, 96, 1e-6, 0, p, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_UNSUPPORTED
+    # quantizing GEMM: 32x1 blocks, shapes off the tile grid, null output
+    st = lib._mx_gemm_q(p, p, p, p, 128, 256, 128, 1, p, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_UNSUPPORTED
+    st = lib._mx_gemm_q(p, p, p, p, 128, 384, 128, 0, p, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_UNSUPPORTED          # N not a multiple of 256
+    st = lib._mx_gemm_q(p, p, p, p, 128, 256, 128, 0, None, None, None, None, None, None)
+    assert st == lib.LPFA_ERR_INVALID_ARG
+    st = lib._mx_gemm_q(p, p, p, p, 128, 256, 128, 0, p, None, None, p, None, None)
+    assert st == lib.LPFA_ERR_INVALID_ARG          # transposed layout with 1x32
