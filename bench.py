@@ -13,6 +13,11 @@ inputs (the path shards over (batch, head) with no exchange step); the time
 is the max over ranks and the value counts the work of all ranks (weak
 scaling).  --impl reference times the fp64 CPU oracle on a bounded sample of
 the same workload (rank 0 only).
+
+Beside the step the JSON line reports the fused RMSNorm + MX quantizer and the
+quantizing GEMM (rates in the same run), the end-to-end rate from pinned host
+memory, and the SM clocks sampled by nvidia-smi during the run (raw samples in
+$LPFA_CLOCK_LOG_DIR, default the system temp directory).
 """
 from __future__ import annotations
 
@@ -23,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import torch
@@ -55,7 +61,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+        # raw samples; the summary goes into the JSON line
+        log_dir = os.environ.get("LPFA_CLOCK_LOG_DIR", tempfile.gettempdir())
+        self.path = os.path.join(log_dir, f"bench_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         os.makedirs(os.path.dirname(self.path), exist_ok=True)
