@@ -2,6 +2,14 @@
  * lpfa — MXFP8 block-scaled FlashAttention (forward and backward) for
  * NVIDIA GB300 (sm_103a).  C ABI.
  *
+ * Entry points: the MX quantizer (lpfa_mx_quantize, and lpfa_mx_quantize_fmt
+ * for the other MX element formats), the attention forward and backward
+ * (lpfa_fwd, lpfa_bwd, lpfa_bwd_noalloc) with their workspace queries and
+ * lpfa_check, the jagged scale-row offsets (lpfa_varlen_sf_rows), the fused
+ * producers of quantized operands (lpfa_rmsnorm_mx_quantize,
+ * lpfa_mx_gemm_quantize), the block-scaled GEMM (lpfa_mx_gemm) and the
+ * status / version / device queries.
+ *
  * Sources of the operations (page title, section):
  *  [P1] "Low Precision Flash Attention 4: End-to-End Block-Scaled Attention
  *       for Blackwell" — paragraph 2 (tcgen05 block-scaled MMA; TMEM budget
