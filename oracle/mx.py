@@ -251,14 +251,15 @@ def quantize_32x32(x, fmt: str = "e4m3") -> tuple:
     return payload[:r], code
 
 
-def dequantize(payload, scale_codes, expand) -> np.ndarray:
+def dequantize(payload, scale_codes, expand, fmt: str = "e4m3") -> np.ndarray:
     """Decode payload * 2^(scale - 127); ``expand`` maps the scale array to
     the payload's shape (e.g. a repeat along the block axis)."""
-    return e4m3_decode(payload) * expand(e8m0_decode(scale_codes))
+    vals = e4m3_decode(payload) if fmt == "e4m3" else fmt_table(fmt)[np.asarray(payload, np.uint8)]
+    return vals * expand(e8m0_decode(scale_codes))
 
 
-def dq_1x32(payload, sc):
-    return dequantize(payload, sc, lambda s: np.repeat(s, 32, axis=-1))
+def dq_1x32(payload, sc, fmt: str = "e4m3"):
+    return dequantize(payload, sc, lambda s: np.repeat(s, 32, axis=-1), fmt)
 
 
 def dq_rows(payload, sc, block: int = 32):
@@ -285,8 +286,10 @@ def fake_quant_32x32(x):
     return dq_32x32(*quantize_32x32(x))
 
 
-def mx_gemm(a_payload, a_sc, b_payload, b_sc) -> np.ndarray:
+def mx_gemm(a_payload, a_sc, b_payload, b_sc, a_fmt: str = "e4m3",
+            b_fmt: str = "e4m3") -> np.ndarray:
     """D = A @ B^T with A [M, K], B [N, K] both 1x32-blocked along K (the
-    block-scaled MMA's contraction).  Every product of two decoded operands is
-    exact in fp64, so this is the dense GEMM of the dequantized operands."""
-    return dq_1x32(a_payload, a_sc) @ dq_1x32(b_payload, b_sc).T
+    block-scaled MMA's contraction), each in its own element format.  Every
+    product of two decoded operands is exact in fp64, so this is the dense
+    GEMM of the dequantized operands."""
+    return dq_1x32(a_payload, a_sc, a_fmt) @ dq_1x32(b_payload, b_sc, b_fmt).T

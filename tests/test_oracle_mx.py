@@ -330,3 +330,26 @@ def test_scale_rule_per_format(fmt):
     amax = np.abs(x).max(axis=1)
     r = amax * 2.0 ** -(sc.astype(np.int64)[:, 0] - 127)
     assert np.all((r >= 2.0 ** emax) & (r < 2.0 ** (emax + 1)))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("e2m1", "e2m1"), ("e3m2", "e2m3"), ("e5m2", "e4m3")])
+def test_mx_gemm_mixed_formats_exact(a_fmt, b_fmt):
+    """The oracle GEMM of operands in other element formats against exact
+    rational arithmetic on a small case (every decoded value is a dyadic
+    rational, so the exact product sums are fractions)."""
+    from fractions import Fraction
+    rng = np.random.default_rng(11)
+    a = rng.standard_normal((4, 64))
+    b = rng.standard_normal((3, 64)) * 3.0
+    pa, sa = mx.quantize_1x32(a, a_fmt)
+    pb, sb = mx.quantize_1x32(b, b_fmt)
+    got = mx.mx_gemm(pa, sa, pb, sb, a_fmt, b_fmt)
+    ta, tb = mx.fmt_table(a_fmt), mx.fmt_table(b_fmt)
+    for i in range(4):
+        for j in range(3):
+            acc = Fraction(0)
+            for k in range(64):
+                va = Fraction(ta[pa[i, k]]) * Fraction(2) ** (int(sa[i, k // 32]) - 127)
+                vb = Fraction(tb[pb[j, k]]) * Fraction(2) ** (int(sb[j, k // 32]) - 127)
+                acc += va * vb
+            assert abs(Fraction(got[i, j]) - acc) <= abs(acc) * Fraction(1, 2 ** 50)
