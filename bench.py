@@ -151,7 +151,6 @@ def oracle_sample(rows: int, seed: int = 2):
     the last ``rows`` keys.  Returns (flops of the sample, seconds, text)."""
     import numpy as np
     from oracle import attention as A
-    from mxfp8_block_scaled_quantizer_gb300 import FWD_KV_TILE
     w = workloads.get_config(WORKLOAD)
     g = torch.Generator().manual_seed(seed)
     S, D = w.seqlen, w.head_dim
@@ -160,7 +159,7 @@ def oracle_sample(rows: int, seed: int = 2):
     r = np.arange(S - rows, S)
     t0 = time.perf_counter()
     fw = A.mx_attention_fwd(q, k, v, causal=True, softmax_scale=w.softmax_scale,
-                            rows=r, kv_tile=FWD_KV_TILE)
+                            rows=r, kv_tile=A.FWD_KEY_TILE)
     o16 = torch.from_numpy(np.nan_to_num(fw["o"])).to(torch.bfloat16)
     A.mx_attention_bwd(q, k, v, o16, do, np.nan_to_num(fw["lse"]), causal=True,
                        softmax_scale=w.softmax_scale, q_rows=r, k_rows=r)

@@ -58,6 +58,17 @@ from . import mx
 LOG2E = 1.0 / math.log(2.0)
 LN2 = math.log(2.0)
 
+#: Keys per tile of the forward's online softmax.  With selective rescaling
+#: the reference max, and with it the E4M3 rounding of P, moves at most once
+#: per tile, so the quantization points of P depend on this length.  Reading
+#: of "Low Precision Flash Attention 4 ...", paragraph 3 (P quantized with the
+#: max the softmax already holds): one tile is 256 keys.
+FWD_KEY_TILE = 256
+
+#: Keys per FP16 dQ partial in the backward (each partial, times the static
+#: scale, is rounded to FP16 and added to the FP16 dQ): 128 keys.
+BWD_KEY_TILE = 128
+
 
 # ----------------------------------------------------------------------------
 # helpers: layouts
@@ -187,7 +198,7 @@ def quantize_fwd_operands(qp, kp, vp, cu, quantize=True):
     return qd, kd, vd
 
 
-def mx_fwd_head(q, k, v, *, causal, scale, kv_tile=128, rescale_threshold=8.0,
+def mx_fwd_head(q, k, v, *, causal, scale, kv_tile=FWD_KEY_TILE, rescale_threshold=8.0,
                 quantize=True, rows=None):
     """Blockwise online softmax attention for one head of one sequence.
 
@@ -235,7 +246,7 @@ def mx_fwd_head(q, k, v, *, causal, scale, kv_tile=128, rescale_threshold=8.0,
 
 
 def mx_attention_fwd(q, k, v, *, causal, softmax_scale, cu_seqlens=None,
-                     kv_tile=128, rescale_threshold=8.0, quantize=True,
+                     kv_tile=FWD_KEY_TILE, rescale_threshold=8.0, quantize=True,
                      heads=None, seqs=None, rows=None):
     """MXFP8 block-scaled attention forward over packed [T, H, D] (with
     ``cu_seqlens``) or BSHD inputs.
@@ -330,7 +341,8 @@ def _check_whole_blocks(idx, L):
 
 
 def mx_bwd_head(q, k, v, dod, do_raw, o, lse, *, causal, scale, quantize=True,
-                kv_tile=128, dq_static_scale=1.0, q_rows=None, k_rows=None):
+                kv_tile=BWD_KEY_TILE, dq_static_scale=1.0, q_rows=None,
+                k_rows=None):
     """Backward for one head of one sequence.
 
     q, k, v, dod: dequantized operands [L, D]; do_raw and o: the bf16-valued
@@ -381,7 +393,7 @@ def mx_bwd_head(q, k, v, dod, do_raw, o, lse, *, causal, scale, quantize=True,
 
 
 def mx_attention_bwd(q, k, v, o, do, lse, *, causal, softmax_scale,
-                     cu_seqlens=None, kv_tile=128, dq_static_scale=1.0,
+                     cu_seqlens=None, kv_tile=BWD_KEY_TILE, dq_static_scale=1.0,
                      quantize=True, heads=None, seqs=None, q_rows=None,
                      k_rows=None):
     """MXFP8 block-scaled attention backward over packed or BSHD inputs.

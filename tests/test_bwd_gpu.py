@@ -9,7 +9,6 @@ import torch
 
 import workloads
 from oracle import attention as A
-from mxfp8_block_scaled_quantizer_gb300 import FWD_KV_TILE
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +54,7 @@ def _oracle(x, w, heads=None, seqs=None, q_rows=None, k_rows=None,
         [h for kh in heads for h in range(kh * grp, (kh + 1) * grp)]
     fw = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=w.causal,
                             softmax_scale=w.softmax_scale, cu_seqlens=cu,
-                            seqs=seqs, rows=fwd_rows, heads=qheads, kv_tile=FWD_KV_TILE)
+                            seqs=seqs, rows=fwd_rows, heads=qheads, kv_tile=A.FWD_KEY_TILE)
     o16 = torch.from_numpy(np.nan_to_num(fw["o"])).to(torch.bfloat16)
     bw = A.mx_attention_bwd(x["q"], x["k"], x["v"], o16, x["do"],
                             np.nan_to_num(fw["lse"]), causal=w.causal,

@@ -11,7 +11,6 @@ import torch
 
 import workloads
 from oracle import attention as A
-from mxfp8_block_scaled_quantizer_gb300 import FWD_KV_TILE
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +50,7 @@ def test_fwd_tiny_full(L):
     x = workloads.make_inputs(w)
     o, lse = _run(L, x, w)
     ref = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=w.causal,
-                             softmax_scale=w.softmax_scale, kv_tile=FWD_KV_TILE)
+                             softmax_scale=w.softmax_scale, kv_tile=A.FWD_KEY_TILE)
     assert relfro(o, ref["o"]) <= TOL_O
     assert np.abs(lse - ref["lse"]).max() <= TOL_LSE
     ex = A.exact_attention(x["q"], x["k"], x["v"], causal=w.causal,
@@ -65,7 +64,7 @@ def test_fwd_outlier_sampled_heads(L):
     o, lse = _run(L, x, w)
     heads = [0, 9, 15]
     ref = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=True,
-                             softmax_scale=w.softmax_scale, heads=heads, kv_tile=FWD_KV_TILE)
+                             softmax_scale=w.softmax_scale, heads=heads, kv_tile=A.FWD_KEY_TILE)
     for h in heads:
         assert relfro(o[:, :, h], ref["o"][:, :, h]) <= TOL_O, h
         assert np.abs(lse[h] - ref["lse"][h]).max() <= TOL_LSE, h
@@ -84,7 +83,7 @@ def test_fwd_full_size_sampled(L, name):
     heads = [0, w.heads_q - 1]
     ref = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=w.causal,
                              softmax_scale=w.softmax_scale, heads=heads,
-                             seqs=[0, w.batch - 1], rows=rows, kv_tile=FWD_KV_TILE)
+                             seqs=[0, w.batch - 1], rows=rows, kv_tile=A.FWD_KEY_TILE)
     ot = _tok(o); rt = _tok(ref["o"])
     for b in (0, w.batch - 1):
         for h in heads:
@@ -112,7 +111,7 @@ def test_fwd_varlen_sampled_sequences(L):
     ref = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=False,
                              softmax_scale=w.softmax_scale,
                              cu_seqlens=x["cu_seqlens"].numpy(), heads=heads,
-                             seqs=seqs, kv_tile=FWD_KV_TILE)
+                             seqs=seqs, kv_tile=A.FWD_KEY_TILE)
     cu = x["cu_seqlens"].numpy()
     for s in seqs:
         a, b = cu[s], cu[s + 1]
@@ -137,7 +136,7 @@ def test_fwd_edge_shapes(L, case, tau):
     o, lse = _run(L, x, w, tau)
     ref = A.mx_attention_fwd(x["q"], x["k"], x["v"], causal=w.causal,
                              softmax_scale=w.softmax_scale,
-                             rescale_threshold=tau, kv_tile=FWD_KV_TILE)
+                             rescale_threshold=tau, kv_tile=A.FWD_KEY_TILE)
     assert relfro(o, ref["o"]) <= TOL_O
     assert np.abs(lse - ref["lse"]).max() <= TOL_LSE
 
@@ -154,7 +153,7 @@ def test_fwd_varlen_causal_ragged(L):
                                     cu_seqlens=cu)
     torch.cuda.synchronize()
     ref = A.mx_attention_fwd(q, k, v, causal=True, softmax_scale=1 / math.sqrt(128),
-                             cu_seqlens=cu.numpy(), kv_tile=FWD_KV_TILE)
+                             cu_seqlens=cu.numpy(), kv_tile=A.FWD_KEY_TILE)
     assert relfro(o.float().cpu().numpy(), ref["o"]) <= TOL_O
     assert np.abs(lse.cpu().numpy() - ref["lse"]).max() <= TOL_LSE
 
