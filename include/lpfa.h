@@ -304,6 +304,23 @@ lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
                      const void* v8, const void* sfv_mma, void* o, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Self-test of the forward's bounded waits (failure detection; the pages
+ * have no counterpart).  Runs lpfa_fwd's kernel with every wait bounded by
+ * wait_limit_us microseconds (1 .. 2e6) instead of 2 s, and with the copy of
+ * each CTA's first key/value tile withheld, so that the MMA warp's wait for
+ * that tile expires: the kernel records the error word, raises its abort
+ * flag, drains the copies and MMAs it issued, frees its tensor memory and
+ * returns.  Arguments and errors as lpfa_fwd; returns LPFA_OK once the
+ * launch is queued, after which lpfa_check(workspace, stream) returns
+ * LPFA_ERR_TIMEOUT.  o and lse are left undefined; the stream and the
+ * context stay usable. */
+lpfa_status lpfa_fwd_wait_expiry_selftest(const lpfa_attn_desc* desc, const void* q8,
+                                          const void* sfq_mma, const void* k8,
+                                          const void* sfk_mma, const void* v8,
+                                          const void* sfv_mma, void* o, float* lse,
+                                          void* workspace, size_t workspace_bytes,
+                                          uint32_t wait_limit_us, void* stream);
+
 /* Backward ([P1] paragraphs 2-3).
  *  q8, k8, do8: e4m3 payloads of 32X32 quantization, with both scale
  *  arrangements (sf*_mma: contraction over head_dim; sf*_mma_t: contraction

@@ -5,6 +5,8 @@
 
 #include <cstdlib>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "lpfa_internal.h"
 
@@ -18,17 +20,37 @@ bool debug_enabled() {
   return v != 0;
 }
 
+namespace {
+std::mutex g_device_cache_mutex;
+}  // namespace
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(g_device_cache_mutex);
   if (cache[dev] == 0) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     cache[dev] = n > 0 ? n : 1;
   }
   return cache[dev];
+}
+
+// A kernel's dynamic shared-memory opt-in belongs to the device that is
+// current when it is set, so it is recorded per (kernel, device, size).
+lpfa_status set_max_dynamic_smem(const void* func, int bytes) {
+  static std::vector<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  LPFA_CHECK_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_device_cache_mutex);
+  for (const auto& t : done)
+    if (std::get<0>(t) == func && std::get<1>(t) == dev && std::get<2>(t) >= bytes)
+      return LPFA_OK;
+  LPFA_CHECK_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  done.emplace_back(func, dev, bytes);
+  return LPFA_OK;
 }
 
 lpfa_status make_seq_view(const lpfa_seqs* s, SeqView* out) {

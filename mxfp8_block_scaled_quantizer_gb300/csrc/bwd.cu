@@ -872,24 +872,16 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
   if (D == 128) {
     const size_t smem = BwdCfg<128>::kSmTotal + 1024;
-    static bool attr = false;
-    if (!attr) {
-      LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel<128>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem)));
-      attr = true;
-    }
+    if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_bwd_kernel<128>),
+                                   static_cast<int>(smem))) != LPFA_OK)
+      return st;
     mx_attn_bwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
         tq, tk, tv, tdo, tdq, p);
   } else {
     const size_t smem = BwdCfg<64>::kSmTotal + 1024;
-    static bool attr = false;
-    if (!attr) {
-      LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_bwd_kernel<64>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem)));
-      attr = true;
-    }
+    if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_bwd_kernel<64>),
+                                   static_cast<int>(smem))) != LPFA_OK)
+      return st;
     mx_attn_bwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
         tq, tk, tv, tdo, tdq, p);
   }

@@ -78,6 +78,9 @@ struct FwdParams {
   int32_t causal;
   float scale_log2;     // softmax_scale * log2(e)
   float threshold;      // log2 units
+  uint64_t wait_ns;     // bound of every wait (kWaitLimitNs normally)
+  int32_t withhold_kv;  // self-test: this CTA-local K/V tile is never loaded
+                        // (-1 normally), so the waits on it must expire
 };
 
 template <int D>
@@ -258,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the Q tile (and its scale tile) is free once the previous item's
       // last S MMA has completed
       if (k > 0) {
-        ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11);
+        ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11, p.wait_ns);
         if (!ok) break;
       }
       mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
@@ -275,8 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < ntiles; ++j, ++gt) {
         const int s = gt % kStages;
         const uint32_t ph = (gt / kStages) & 1;
-        ok = mbar_wait_sleep(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10);
+        ok = mbar_wait_sleep(&bars->kv_empty[s], ph ^ 1, p.err, abort, 10, p.wait_ns);
         if (!ok) break;
+        if (gt == p.withhold_kv) continue;
         uint8_t* kbuf = sm + C::kStage0 + s * C::kStageBytes;
         uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
         uint64_t* bar = &bars->kv_full[s];
@@ -294,13 +298,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued[s] = static_cast<int>(ph);
       }
     }
-    if (!ok) {
-      for (int s = 0; s < kStages; ++s)
-        if (issued[s] >= 0)
-          mbar_wait_sleep(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
-      if (q_issued >= 0)
-        mbar_wait_sleep(&bars->q_full, static_cast<uint32_t>(q_issued), nullptr, nullptr, 0);
-    }
+    // No copy may still be landing when the CTA exits, whichever warp ended
+    // the loops: wait for the last phase issued on every buffer (already
+    // complete in a run that did not abort).
+    for (int s = 0; s < kStages; ++s)
+      if (issued[s] >= 0)
+        mbar_wait_sleep(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+    if (q_issued >= 0)
+      mbar_wait_sleep(&bars->q_full, static_cast<uint32_t>(q_issued), nullptr, nullptr, 0);
   } else if (warp == 1 || warp == 10) {
     // --------------------------------------------------------- MMA issuers
     // A warp issues at most one tcgen05 instruction every ~60-90 cycles, and
@@ -325,8 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // overwritten once every softmax warp holds its row of the previous S
       auto issue_s = [&](int g) -> bool {
         const int s = g % kStages;
-        if (g > 0 && !mbar_wait_sleep(&bars->s_free, (g - 1) & 1, p.err, abort, 23)) return false;
-        if (!mbar_wait_sleep(&bars->kv_full[s], (g / kStages) & 1, p.err, abort, 21)) return false;
+        if (g > 0 && !mbar_wait_sleep(&bars->s_free, (g - 1) & 1, p.err, abort, 23, p.wait_ns)) return false;
+        if (!mbar_wait_sleep(&bars->kv_full[s], (g / kStages) & 1, p.err, abort, 21, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
         const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         WorkItem w;
         if (!work_item(p, idx, w)) continue;
         const int ntiles = item_tiles(p, w);
-        ok = mbar_wait_sleep(&bars->q_full, k & 1, p.err, abort, 20);
+        ok = mbar_wait_sleep(&bars->q_full, k & 1, p.err, abort, 20, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
@@ -366,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O: its P-full comes after the softmax read the previous item's O.
       auto issue_pv = [&](int g, bool first) -> bool {
         const int s = g % kStages;
-        if (!mbar_wait_sleep(&bars->p_full, g & 1, p.err, abort, 22)) return false;
+        if (!mbar_wait_sleep(&bars->p_full, g & 1, p.err, abort, 22, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
         const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;                              // this half's partial sum
       const int lim = p.causal ? min(w.len, qi + 1) : w.len;   // keys < lim visible
       for (int j = 0; j < ntiles && ok; ++j, ++gt) {
-        ok = mbar_wait_sleep(&bars->s_full, gt & 1, p.err, abort, 30);
+        ok = mbar_wait_sleep(&bars->s_full, gt & 1, p.err, abort, 30, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[4][32];
@@ -455,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         xm[wg * 128 + row] = hmax;
         __syncwarp();
         if (lane == 0) mbar_arrive(xbar);
-        ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 33);
+        ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 33, p.wait_ns);
         if (!ok) break;
         ++gx;
         const float tmax = fmaxf(hmax, xm[(1 - wg) * 128 + row]);
@@ -503,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is stable only between two PVs); an item's first tile follows the
         // previous item's epilogue, which waited for its last PV
         if (j > 0) {
-          ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 31);
+          ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 31, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
           // the previous tile's S and PV are done: its K/V stage may be refilled
@@ -537,10 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       xsum[wg * 128 + row] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(xbar);
-      ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 34);
+      ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 34, p.wait_ns);
       if (!ok) break;
       ++gx;
-      ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 32);
+      ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 32, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
       // the item's last S and PV are done: its K/V stage may be refilled
@@ -590,7 +595,8 @@ template <int D>
 lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
                        const void* q8, const void* sfq, const void* k8,
                        const void* sfk, const void* v8, const void* sfv,
-                       void* o, float* lse, uint32_t* err, cudaStream_t cs) {
+                       void* o, float* lse, uint32_t* err, uint64_t wait_ns,
+                       int32_t withhold_kv, cudaStream_t cs) {
   const CUtensorMapSwizzle sw =
       D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk, tv;
@@ -623,6 +629,8 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   p.causal = desc->causal ? 1 : 0;
   p.scale_log2 = desc->softmax_scale * 1.4426950408889634f;
   p.threshold = desc->rescale_threshold;
+  p.wait_ns = wait_ns;
+  p.withhold_kv = withhold_kv;
 
   const int64_t units = sv.cu_seqlens == nullptr
                             ? static_cast<int64_t>(sv.nseq) * p.nq
@@ -630,21 +638,12 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   const int64_t nitems = units * p.hq;
   LPFA_CHECK_ARG(nitems > 0 && nitems < (1ll << 31));
   p.nitems = nitems;
-  static int nsm = 0;
-  if (nsm == 0) {
-    int dev = 0;
-    LPFA_CHECK_CUDA(cudaGetDevice(&dev));
-    LPFA_CHECK_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  }
+  const int nsm = num_sms();
   const int64_t nblocks = nitems < nsm ? nitems : nsm;   // one CTA per SM
   const size_t smem = FwdCfg<D>::kTotal + 1024;
-  static bool attr = false;
-  if (!attr) {
-    LPFA_CHECK_CUDA(cudaFuncSetAttribute(mx_attn_fwd_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem)));
-    attr = true;
-  }
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D>),
+                                 static_cast<int>(smem))) != LPFA_OK)
+    return st;
   mx_attn_fwd_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
@@ -673,12 +672,13 @@ extern "C" size_t lpfa_fwd_workspace_size(const lpfa_attn_desc* desc) {
   return 256;
 }
 
-extern "C" lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
-                                const void* sfq_mma, const void* k8,
-                                const void* sfk_mma, const void* v8,
-                                const void* sfv_mma, void* o, float* lse,
-                                void* workspace, size_t workspace_bytes,
-                                void* stream) {
+namespace {
+
+lpfa_status fwd_impl(const lpfa_attn_desc* desc, const void* q8, const void* sfq_mma,
+                     const void* k8, const void* sfk_mma, const void* v8,
+                     const void* sfv_mma, void* o, float* lse, void* workspace,
+                     size_t workspace_bytes, uint64_t wait_ns, int32_t withhold_kv,
+                     void* stream) {
   SeqView sv;
   lpfa_status st = validate_attn(desc, &sv);
   if (st != LPFA_OK) return st;
@@ -688,14 +688,35 @@ extern "C" lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
                  aligned16(o));
   LPFA_CHECK_ARG(workspace != nullptr && workspace_bytes >= 256 &&
                  (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0);
-  if (desc->causal && sv.cu_seqlens == nullptr) {
-    // Sq == Sk by construction (self-attention over the same sequences)
-  }
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (sv.total_tokens == 0) return LPFA_OK;
   LPFA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 256, cs));
   uint32_t* err = static_cast<uint32_t*>(workspace);
   if (desc->head_dim == 128)
-    return launch_fwd<128>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err, cs);
-  return launch_fwd<64>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err, cs);
+    return launch_fwd<128>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
+                           wait_ns, withhold_kv, cs);
+  return launch_fwd<64>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
+                        wait_ns, withhold_kv, cs);
+}
+
+}  // namespace
+
+extern "C" lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
+                                const void* sfq_mma, const void* k8,
+                                const void* sfk_mma, const void* v8,
+                                const void* sfv_mma, void* o, float* lse,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return fwd_impl(desc, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, workspace,
+                  workspace_bytes, kWaitLimitNs, -1, stream);
+}
+
+extern "C" lpfa_status lpfa_fwd_wait_expiry_selftest(
+    const lpfa_attn_desc* desc, const void* q8, const void* sfq_mma, const void* k8,
+    const void* sfk_mma, const void* v8, const void* sfv_mma, void* o, float* lse,
+    void* workspace, size_t workspace_bytes, uint32_t wait_limit_us, void* stream) {
+  LPFA_CHECK_ARG(wait_limit_us >= 1 && wait_limit_us <= 2000000u);
+  return fwd_impl(desc, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, workspace,
+                  workspace_bytes, static_cast<uint64_t>(wait_limit_us) * 1000ull, 0,
+                  stream);
 }

@@ -346,8 +346,9 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   const int ntiles = g.tiles_m * g.tiles_n;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   auto go = [&](auto kernel) -> lpfa_status {
-    LPFA_CHECK_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem)));
+    lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
+                                          static_cast<int>(smem));
+    if (st != LPFA_OK) return st;
     kernel<<<grid, kThreads, smem, cs>>>(ta, tb, g);
     LPFA_CHECK_CUDA(cudaGetLastError());
     return LPFA_OK;

@@ -97,17 +97,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Waits for `parity` on `bar`.  Returns false (after reporting) when the
-// wait expires or when `abort` (shared flag) is already set by another warp.
+// wait expires (after `limit_ns`) or when `abort` (shared flag) is already
+// set by another warp.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint32_t* err, volatile int* abort,
-                                          uint32_t site) {
+                                          uint32_t site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort != nullptr) *abort = 1;
         report_error(err, ERR_WAIT_TIMEOUT, site);
         return false;
@@ -122,13 +124,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // the polling thread suspended between tests.
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
                                                 uint32_t* err, volatile int* abort,
-                                                uint32_t site) {
+                                                uint32_t site,
+                                                uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (abort != nullptr && *abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       if (abort != nullptr) *abort = 1;
       report_error(err, ERR_WAIT_TIMEOUT, site);
       return false;

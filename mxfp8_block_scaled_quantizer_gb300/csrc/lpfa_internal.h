@@ -59,6 +59,10 @@ lpfa_status validate_attn(const lpfa_attn_desc* desc, SeqView* sv);
 // Number of SMs of the current device (cached per device).
 int num_sms();
 
+// cudaFuncAttributeMaxDynamicSharedMemorySize for a kernel on the current
+// device, set once per (kernel, device).
+lpfa_status set_max_dynamic_smem(const void* func, int bytes);
+
 // cuTensorMapEncodeTiled through the driver entry point.
 lpfa_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype,
                         uint32_t rank, const void* base, const uint64_t* dims,

@@ -81,6 +81,9 @@ _fwd = _sig("lpfa_fwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
 _bwd = _sig("lpfa_bwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
+_fwd_expiry = _sig("lpfa_fwd_wait_expiry_selftest", ctypes.c_int,
+                   ctypes.POINTER(lpfa_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                   _vp, _vp, ctypes.c_size_t, ctypes.c_uint32, _vp)
 _check = _sig("lpfa_check", ctypes.c_int, _vp, _vp)
 _bwd_noalloc = _sig("lpfa_bwd_noalloc", ctypes.c_int,
                     ctypes.POINTER(lpfa_attn_desc), _vp, _vp, _vp, _vp, _vp,
@@ -93,7 +96,8 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_rmsnorm_mx_quantize",
             "lpfa_mx_gemm", "lpfa_mx_gemm_quantize",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
-            "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc")
+            "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc",
+            "lpfa_fwd_wait_expiry_selftest")
 
 
 class LpfaError(RuntimeError):
@@ -348,8 +352,20 @@ def lpfa_bwd(desc, q8, sfq, sfq_t, k8, sfk, sfk_t, v8, sfv, do8, sfdo,
              _stream(stream)), "lpfa_bwd")
 
 
+def lpfa_fwd_wait_expiry_selftest(desc, q8, sfq, k8, sfk, v8, sfv, o, lse, ws,
+                                  wait_limit_us, stream=None):
+    _ok(_fwd_expiry(ctypes.byref(desc), _ptr(q8), _ptr(sfq), _ptr(k8), _ptr(sfk),
+                    _ptr(v8), _ptr(sfv), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                    wait_limit_us, _stream(stream)), "lpfa_fwd_wait_expiry_selftest")
+
+
 def lpfa_check(ws: torch.Tensor, stream=None):
     _ok(_check(_ptr(ws), _stream(stream)), "lpfa_check")
+
+
+def check_status(ws: torch.Tensor, stream=None) -> int:
+    """lpfa_check's status code, without raising."""
+    return int(_check(_ptr(ws), _stream(stream)))
 
 
 # ------------------------------------------------------- convenience layer

@@ -143,6 +143,28 @@ def exact_bwd_head(q, k, v, do, causal, scale):
     return scale * ds @ k, scale * ds.T @ q, dv
 
 
+def exact_fwd_head_chunked(q, k, v, causal, scale, chunk=2048):
+    """``exact_fwd_head`` computed over blocks of ``chunk`` query rows, so
+    that long sequences need O(chunk * L) memory.  Query row i of the block
+    starting at r0 is row r0 + i of the head; the causal mask keeps keys
+    j <= r0 + i."""
+    L = q.shape[0]
+    o = np.empty((L, v.shape[1]))
+    lse = np.empty(L)
+    for r0 in range(0, L, chunk):
+        r1 = min(r0 + chunk, L)
+        kend = r1 if causal else k.shape[0]
+        s = scale * (q[r0:r1] @ k[:kend].T)
+        if causal:
+            s = np.where(_causal_mask(r1 - r0, kend, q0=r0), -np.inf, s)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        o[r0:r1] = (p / l) @ v[:kend]
+        lse[r0:r1] = (m + np.log(l))[:, 0]
+    return o, lse
+
+
 def exact_attention(q, k, v, *, causal, softmax_scale, cu_seqlens=None,
                     do=None):
     """Exact attention over packed or BSHD inputs (fp64).  Returns a dict with

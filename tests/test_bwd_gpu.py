@@ -45,7 +45,7 @@ def _gpu_fwd_bwd(L, x, w, dq_scale=1.0):
 
 
 def _oracle(x, w, heads=None, seqs=None, q_rows=None, k_rows=None,
-            fwd_rows=None):
+            fwd_rows=None, dq_scale=1.0):
     """Oracle forward (its own O, LSE) then backward on a sample: ``heads``
     are kv heads (all their query heads are computed)."""
     cu = x["cu_seqlens"].numpy() if w.varlen else None
@@ -59,7 +59,8 @@ def _oracle(x, w, heads=None, seqs=None, q_rows=None, k_rows=None,
     bw = A.mx_attention_bwd(x["q"], x["k"], x["v"], o16, x["do"],
                             np.nan_to_num(fw["lse"]), causal=w.causal,
                             softmax_scale=w.softmax_scale, cu_seqlens=cu,
-                            heads=heads, seqs=seqs, q_rows=q_rows, k_rows=k_rows)
+                            heads=heads, seqs=seqs, q_rows=q_rows, k_rows=k_rows,
+                            dq_static_scale=dq_scale)
     return bw, o16, fw["lse"]
 
 
@@ -170,6 +171,72 @@ def test_bwd_full_size_sampled(L, name):
             _check(got, ref, qr, kr, f"{name} b{b} kv{kh}")
 
 
+def test_bwd_full_size_first_key_tile_end_to_end(L):
+    """llm, last sequence and head: the first 128 keys are seen by all 8192
+    queries (the longest query loop of the causal backward, 128 steps); their
+    dK, dV and the first 128 rows of dQ against the oracle running its own
+    forward over every query row."""
+    w = workloads.get_config("llm")
+    x = workloads.make_inputs(w)
+    got = _gpu_fwd_bwd(L, x, w)
+    S, b, kh = w.seqlen, w.batch - 1, w.heads_kv - 1
+    rows = np.arange(0, 128)
+    ref, _, _ = _oracle(x, w, heads=[kh], seqs=[b], q_rows=rows, k_rows=rows)
+    sel = (b * S + rows, kh)
+    _check(got, ref, sel, sel, "llm first key tile")
+
+
+@pytest.mark.parametrize("name,pairs", [("llm", [(0, 0), (7, 31)]),
+                                        ("gqa_long", [(0, 7)])])
+def test_bwd_full_size_isolated(L, name, pairs):
+    """Isolated form at full size: both backwards get the same O and LSE,
+    the oracle's exact fp64 attention of the sampled (sequence, kv head)
+    pairs (all query heads of the group; other heads keep the GPU forward's
+    O and LSE and are not compared).  Compared: the first and the last 128
+    keys (dK, dV: the longest and the shortest causal query loops, 512 steps
+    per query head for the first key tile of gqa_long) and the first and last
+    128 query rows of dQ."""
+    w = workloads.get_config(name)
+    x = workloads.make_inputs(w)
+    S, D = w.seqlen, w.head_dim
+    grp = w.heads_q // w.heads_kv
+    T = w.batch * S
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = L.mx_attention_forward(q, k, v, causal=True,
+                                    softmax_scale=w.softmax_scale)
+    # the oracle's inputs hold only oracle values (zeros elsewhere)
+    o_or = torch.zeros(T, w.heads_q, D, dtype=torch.bfloat16)
+    lse_or = np.zeros((w.heads_q, T))
+    qt, kt, vt = (_tok(x[n]) for n in ("q", "k", "v"))
+    for b, kh in pairs:
+        for h in range(kh * grp, (kh + 1) * grp):
+            oh, lh = A.exact_fwd_head_chunked(
+                qt[b * S:(b + 1) * S, h].double().numpy(),
+                kt[b * S:(b + 1) * S, kh].double().numpy(),
+                vt[b * S:(b + 1) * S, kh].double().numpy(), True, w.softmax_scale)
+            o_or[b * S:(b + 1) * S, h] = torch.from_numpy(oh).to(torch.bfloat16)
+            lse_or[h, b * S:(b + 1) * S] = lh
+            o.view(T, w.heads_q, D)[b * S:(b + 1) * S, h] = \
+                o_or[b * S:(b + 1) * S, h].cuda()
+            lse[h, b * S:(b + 1) * S] = torch.from_numpy(lh).float().cuda()
+    dq, dk, dv = L.mx_attention_backward(q, k, v, o, do, lse, causal=True,
+                                         softmax_scale=w.softmax_scale)
+    torch.cuda.synchronize()
+    got = [t.float().cpu().numpy() for t in (dq, dk, dv)]
+    rows = np.concatenate([np.arange(0, 128), np.arange(S - 128, S)])
+    shape = x["q"].shape
+    for b, kh in pairs:
+        ref = A.mx_attention_bwd(x["q"], x["k"], x["v"], o_or.reshape(shape),
+                                 x["do"], lse_or, causal=True,
+                                 softmax_scale=w.softmax_scale, heads=[kh],
+                                 seqs=[b], q_rows=rows, k_rows=rows)
+        for part in (rows[:128], rows[128:]):
+            kr = (b * S + part, kh)
+            for h in range(kh * grp, (kh + 1) * grp):
+                _check(got, ref, (b * S + part, h), kr,
+                       f"{name} b{b} kv{kh} h{h} rows {part[0]}..")
+
+
 def test_bwd_varlen_sampled_sequences(L):
     w = workloads.get_config("varlen")
     x = workloads.make_inputs(w)
@@ -186,10 +253,14 @@ def test_bwd_varlen_sampled_sequences(L):
 
 
 def test_bwd_dq_static_scale(L):
+    """dq_static_scale = 8 against the oracle at the same scale (FP16
+    partials times 8, divided out at the end); dK and dV do not depend on it."""
     w = workloads.custom(seed=3, batch=1, seqlen=256, heads_q=2, heads_kv=2,
                          head_dim=128, causal=True)
     x = workloads.make_inputs(w)
     g1 = _gpu_fwd_bwd(L, x, w, 1.0)
     g8 = _gpu_fwd_bwd(L, x, w, 8.0)
-    assert relfro(g8[0], g1[0]) < 5e-3
+    ref8, _, _ = _oracle(x, w, dq_scale=8.0)
+    allr = (slice(None),)
+    _check(g8, ref8, allr, allr, "dq_static_scale=8")
     assert np.array_equal(g8[1], g1[1]) and np.array_equal(g8[2], g1[2])

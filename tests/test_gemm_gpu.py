@@ -117,3 +117,68 @@ def test_mx_gemm_quantize_output_feeds_the_next_gemm(L, block):
         want_t = mx.mx_gemm(qn.T, cols_sc, pt, st)
         scale_t = np.abs(mx.dq_1x32(qn.T, cols_sc)) @ np.abs(mx.dq_1x32(pt, st)).T
         assert np.all(np.abs(f.cpu().numpy() - want_t) <= 1e-5 * scale_t + 1e-30)
+
+
+# E4M3 magnitudes (torch's decoder) and the decision boundaries between them:
+# the midpoints, and 0 (the sign of a zero code)
+_GRID = torch.arange(0, 127, dtype=torch.uint8).view(
+    torch.float8_e4m3fn).to(torch.float64).numpy()
+_BOUNDS = np.concatenate([[0.0], 0.5 * (_GRID[:-1] + _GRID[1:])])
+
+
+def _blocks(x, block):
+    M, N = x.shape
+    if block == "1x32":
+        return x.reshape(M, N // 32, 32)
+    return x.reshape(M // 32, 32, N // 32, 32).transpose(0, 2, 1, 3).reshape(
+        M // 32, N // 32, 1024)
+
+
+def _open_blocks(exact, bound, block):
+    """Blocks whose codes the accumulation bound leaves open: the block
+    maximum's binade (the scale) can change within the bound, or some
+    element lies within the bound of a rounding boundary at that scale."""
+    xb, bb = np.abs(_blocks(exact, block)), _blocks(bound, block)
+    amax, bmax = xb.max(-1), bb.max(-1)
+    lo = np.floor(np.log2(np.maximum(amax - bmax, 1e-300)))
+    hi = np.floor(np.log2(amax + bmax))
+    e = np.floor(np.log2(np.maximum(amax, 1e-300))) - 8
+    y, dy = xb * 2.0 ** -e[..., None], bb * 2.0 ** -e[..., None]
+    i = np.searchsorted(_BOUNDS, y)
+    up = _BOUNDS[np.minimum(i, len(_BOUNDS) - 1)]
+    down = _BOUNDS[np.maximum(i - 1, 0)]
+    near = (np.abs(up - y) <= dy) | (np.abs(y - down) <= dy)
+    return (lo != hi) | near.any(-1)
+
+
+@pytest.mark.parametrize("block", ["1x32", "32x32"])
+def test_mx_gemm_quantize_codes_against_exact_product(L, block):
+    """The fused codes against the oracle's quantization of the exact fp64
+    product.  A block may differ only where the fp32 accumulation bound
+    (1e-5 of sum |a||b|) leaves its decision open; how many blocks were open
+    and how many differed is printed."""
+    M, N, K = 384, 768, 128
+    pa, sa, pb, sb = _operands(M, N, K, seed=77)
+    blk = {"1x32": L.LPFA_BLK_1X32, "32x32": L.LPFA_BLK_32X32}[block]
+    q, sf, _, _, d = L.mx_gemm_quantize(
+        _dev(pa), _dev(_gemm_sf_layout(sa)), _dev(pb), _dev(_gemm_sf_layout(sb)), blk,
+        with_fp32=True)
+    torch.cuda.synchronize()
+    exact = mx.mx_gemm(pa, sa, pb, sb)
+    absprod = np.abs(mx.dq_1x32(pa, sa)) @ np.abs(mx.dq_1x32(pb, sb)).T
+    bound = 1e-5 * absprod
+    # observed accumulation error, for the record (decides nothing)
+    print("max |d - exact| / sum|a||b| =",
+          float(np.max(np.abs(d.cpu().numpy() - exact) / absprod)))
+    want = layouts.gemm_quantize(exact, block)
+    got_p, got_s = q.cpu().numpy(), sf.cpu().numpy()
+    scale_b = got_s if block == "32x32" else got_s.reshape(M, N // 32)
+    want_s = want["sf"] if block == "32x32" else want["sf"].reshape(M, N // 32)
+    differ = np.any(_blocks(got_p, block) != _blocks(want["payload"], block), -1) | \
+        (scale_b != want_s)
+    open_ = _open_blocks(exact, bound, block)
+    print(f"{block}: {differ.sum()} of {differ.size} blocks differ, "
+          f"{open_.sum()} open")
+    assert not np.any(differ & ~open_)
+    if block == "1x32":
+        assert open_.mean() < 0.5        # the check decides most blocks

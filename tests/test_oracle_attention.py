@@ -256,3 +256,15 @@ def test_bwd_causal_sampling_consistent(rng):
     assert np.array_equal(part["dq"][160:200], full["dq"][160:200])
     assert np.array_equal(part["dk"][96:128], full["dk"][96:128])
     assert np.array_equal(part["dv"][96:128], full["dv"][96:128])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_exact_chunked_equals_whole_head(rng, causal):
+    """Query-row blocks (one ragged) give the whole-head result."""
+    L, d = 150, 16
+    q, k, v, _ = _rand(rng, L, 1, 1, d)
+    o, lse = A.exact_fwd_head(q[:, 0], k[:, 0], v[:, 0], causal, 0.4)
+    oc, lc = A.exact_fwd_head_chunked(q[:, 0], k[:, 0], v[:, 0], causal, 0.4,
+                                      chunk=64)
+    assert np.allclose(oc, o, rtol=1e-13, atol=1e-14)
+    assert np.allclose(lc, lse, rtol=1e-14, atol=1e-14)

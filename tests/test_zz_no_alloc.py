@@ -4,8 +4,11 @@ CUDA allocator because it can synchronise the device).  It keeps its scratch
 in the library's static device array instead of a caller workspace.
 
 The GPU test calls it through the C ABI twice in a row and compares each
-result with lpfa_bwd's (same inputs, caller-allocated workspace) within the
-backward tolerance.  The file is named so that pytest collects it last.
+result with lpfa_bwd's (same inputs, caller-allocated workspace): both run
+the same kernel, whose dK and dV accumulate in a fixed order, so those must be
+bit-identical; dQ is a sum of FP16 reduce-adds whose order varies from run to
+run, so it must agree to within a few FP16 roundings.  The file is named so
+that pytest collects it last.
 """
 import ctypes
 
@@ -15,7 +18,9 @@ import torch
 
 import workloads
 
-TOL = 5e-2
+# three 128-key partials per dQ element here, each add rounded to FP16
+# (relative 2^-11): the two orders differ by a few units of that
+DQ_TOL = 2e-3
 
 
 @pytest.fixture(scope="module")
@@ -64,7 +69,8 @@ def test_noalloc_matches_workspace_backward_twice(L):
                            bk.sf_mma, bk.sf_mma_t, bv.data, bv.sf_mma, bdo.data,
                            bdo.sf_mma, bdo.sf_mma_t, o, do, lse, dq, dk, dv)
         torch.cuda.synchronize()
-        for got, want in ((dq, ref[0]), (dk, ref[1]), (dv, ref[2])):
+        for got in (dq, dk, dv):
             assert torch.isfinite(got).all()
-            assert _relfro(got, want) <= TOL
+        assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+        assert _relfro(dq, ref[0]) <= DQ_TOL
     assert np.isfinite(float(dq.float().abs().max()))
