@@ -55,10 +55,26 @@ def _peaks():
         return None
 
 
+def smi_gpu_id(local: int) -> str:
+    """The GPU's identity for nvidia-smi --id: its UUID (nvidia-smi numbers
+    GPUs physically and ignores CUDA_VISIBLE_DEVICES, so the CUDA ordinal can
+    name another process's GPU), else its PCI bus id, else the ordinal."""
+    try:
+        props = torch.cuda.get_device_properties(local)
+        uuid = str(getattr(props, "uuid", "") or "")
+        if uuid:
+            return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if hasattr(props, "pci_bus_id"):
+            return f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except Exception:
+        pass
+    return str(local)
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
-    def __init__(self, index: int):
+    def __init__(self, index):
         self.index = index
         self.proc = None
         # raw samples; the summary goes into the JSON line
@@ -108,11 +124,12 @@ class ClockSampler:
                     if v.lower() == "active":
                         reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"],
+                    "gpu": self.index}
         loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
         return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
                 "power_w_max": max(power), "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons), "gpu": self.index}
 
 
 def _dist():
@@ -248,7 +265,7 @@ def run_lpfa(args, world, rank, local):
             e[4].record()
             times.append(e)
 
-    clk = ClockSampler(local).__enter__()   # sample from warm-up to end of e2e
+    clk = ClockSampler(smi_gpu_id(local)).__enter__()   # warm-up to end of e2e
     time.sleep(1.0)                          # let the sampler start
     for _ in range(args.warmup):
         step()
@@ -391,8 +408,48 @@ def run_lpfa(args, world, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
-    # ---- in-run MX MMA rate (block-scaled GEMM 8192^3) and cuBLAS reference
+    # the pinned-memory copy rates that bound the end-to-end leg: uploads
+    # alone, downloads alone, and both at once on their two streams
+    dev_out = {n: torch.empty(t.shape, dtype=t.dtype, device=dev) for n, t in out_host.items()}
+
+    def _copies(up, down, reps=3):
+        c0, c1 = ev(), ev()
+        c0.record(cur)
+        for _ in range(reps):
+            h2d_s.wait_stream(cur)
+            d2h_s.wait_stream(cur)
+            if up:
+                with torch.cuda.stream(h2d_s):
+                    for n in names:
+                        dev_in[0][n].copy_(host[n], non_blocking=True)
+            if down:
+                with torch.cuda.stream(d2h_s):
+                    for n, t in dev_out.items():
+                        out_host[n].copy_(t, non_blocking=True)
+            cur.wait_stream(h2d_s)
+            cur.wait_stream(d2h_s)
+        c1.record(cur)
+        torch.cuda.synchronize()
+        return c0.elapsed_time(c1) / reps
+
+    t_up = _copies(True, False)
+    t_down = _copies(False, True)
+    t_both = _copies(True, True)
+    copy_rates = {"h2d_gbs_alone": h2d / (t_up * 1e-3) / 1e9,
+                  "d2h_gbs_alone": d2h / (t_down * 1e-3) / 1e9,
+                  "both_ms": t_both, "h2d_ms_alone": t_up, "d2h_ms_alone": t_down,
+                  "note": "2 GiB up + 2 GiB down per step; with both directions at "
+                          "once the copies take both_ms, the floor of the e2e step"}
+    del dev_out
+
+    # ---- in-run MX MMA rates: the tensor pipe alone (lpfa_mma_peak), the
+    # block-scaled GEMM 8192^3 of this library and of cuBLAS
     mma = {}
+    try:
+        mma["lpfa_mma_peak_tflops"] = L.lpfa_mma_peak() / 1e12
+    except Exception as exc:
+        mma["lpfa_mma_peak_tflops"] = None
+        mma["mma_peak_note"] = repr(exc)[:160]
     try:
         M = N = K = 8192
         a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
@@ -450,12 +507,27 @@ def run_lpfa(args, world, rank, local):
         mma["error"] = repr(exc)[:160]
 
     peaks = _peaks()
-    if peaks and peaks.get("bf16_tflops_sustained"):
-        peak = FP8_OVER_BF16 * peaks["bf16_tflops_sustained"]
-        peak_src = "measured bf16 sustained x 2 (nominal fp8:bf16), MEASURED_PEAKS.json"
+    # Roofline denominator: the fastest dense block-scaled MXFP8 GEMM measured
+    # in this run (this library's or cuBLAS's, M = N = K = 8192).  Beside it:
+    # the tensor pipe's own rate (no memory traffic; an upper bound no GEMM
+    # reaches), the measured burst bf16 GEMM rate x 2 (the nominal fp8:bf16
+    # ratio) and the datasheet's ~4.5 PF/s.
+    gemm_rates = {k: mma.get(k) for k in ("lpfa_mx_gemm_tflops", "cublas_mxfp8_tflops")
+                  if mma.get(k)}
+    bf16_burst_x2 = FP8_OVER_BF16 * (peaks or {}).get("bf16_tflops", 0.0) or None
+    if gemm_rates:
+        src_key = max(gemm_rates, key=gemm_rates.get)
+        peak = gemm_rates[src_key]
+        peak_src = {"lpfa_mx_gemm_tflops": "lpfa_mx_gemm",
+                    "cublas_mxfp8_tflops": "cuBLAS MXFP8 (torch._scaled_mm)"}[src_key] + \
+            " 8192^3, measured in this run (of measured)"
+    elif bf16_burst_x2:
+        peak = bf16_burst_x2
+        peak_src = "measured bf16 burst x 2 (nominal fp8:bf16), MEASURED_PEAKS.json (of measured)"
     else:
-        peak = 1700.0 * FP8_OVER_BF16
-        peak_src = "fallback 1.7 PFLOP/s bf16 sustained x 2"
+        peak = 1900.0 * FP8_OVER_BF16
+        peak_src = "fallback 1.9 PFLOP/s bf16 burst x 2 (of fallback)"
+    pipe = mma.get("lpfa_mma_peak_tflops")
     hbm = peaks.get("hbm_gbs") if peaks else None
     hbm_src = "measured copy bandwidth, MEASURED_PEAKS.json (of measured)" if hbm else \
         "fallback 6.8 TB/s"
@@ -485,10 +557,18 @@ def run_lpfa(args, world, rank, local):
         "fwd": {"tflops": fwd_tflops, "ms": fw, "frac_of_peak": fwd_tflops / peak},
         "bwd": {"tflops": bwd_tflops, "ms": bw, "frac_of_peak": bwd_tflops / peak},
         "quantize_ms": {"fwd_operands": qf, "bwd_operands": qb},
-        "roofline": {"bound": "tensor", "kernel": "mx_attn_bwd (lpfa_bwd call)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "mx_attn_bwd_kernel (lpfa_bwd call: D_i preprocess + main kernel)",
                      "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": bwd_tflops / peak, "traffic": traffic,
-                     "peak_source": peak_src + " (of measured)"},
+                     "peak_source": peak_src,
+                     "context": {
+                         "mma_pipe_tflops": pipe,
+                         "bwd_frac_of_pipe": bwd_tflops / pipe if pipe else None,
+                         "fwd_frac_of_pipe": fwd_tflops / pipe if pipe else None,
+                         "bf16_burst_x2_tflops": bf16_burst_x2,
+                         "bwd_frac_of_bf16_burst_x2": bwd_tflops / bf16_burst_x2 if bf16_burst_x2 else None,
+                         "datasheet_tflops": 4500.0}},
         "mma_rate_in_run": mma,
         "rmsnorm_quantize": {
             "workload": f"x [{T}, {H * D}] bf16 (the llm Q tensor as hidden states), 32x32 blocks, "
@@ -499,10 +579,20 @@ def run_lpfa(args, world, rank, local):
             "two_pass": "torch bf16 rms_norm, then lpfa_mx_quantize (context)"},
         "e2e": {"value": total / (e2e_ms * 1e-3) / 1e15, "unit": "PFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "steps": e2e_steps},
+                "ms_per_step": e2e_ms, "steps": e2e_steps, "copies": copy_rates},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    # clock-independent view: kernel time in SM clock cycles at the median
+    # clock sampled under load
+    mhz = line["clocks"].get("sm_mhz")
+    if mhz:
+        line["fwd"]["mcycles"] = fw * mhz * 1e-3
+        line["bwd"]["mcycles"] = bw * mhz * 1e-3
+        line["fwd"]["flop_per_cycle_per_sm"] = fwd_flops / (fw * mhz * 1e3) / \
+            torch.cuda.get_device_properties(dev).multi_processor_count
+        line["bwd"]["flop_per_cycle_per_sm"] = bwd_flops / (bw * mhz * 1e3) / \
+            torch.cuda.get_device_properties(dev).multi_processor_count
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:

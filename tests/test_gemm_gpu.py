@@ -154,9 +154,11 @@ def _open_blocks(exact, bound, block):
 @pytest.mark.parametrize("block", ["1x32", "32x32"])
 def test_mx_gemm_quantize_codes_against_exact_product(L, block):
     """The fused codes against the oracle's quantization of the exact fp64
-    product.  A block may differ only where the fp32 accumulation bound
-    (1e-5 of sum |a||b|) leaves its decision open; how many blocks were open
-    and how many differed is printed."""
+    product.  A block may differ only where the accumulation bound leaves its
+    decision open; how many blocks were open and how many differed is
+    printed.  Bound: 1e-6 of sum |a||b| at K = 128 (4 fp32 additions of exact
+    32-term block products), ten times the largest difference measured on
+    this GPU (9.8e-8)."""
     M, N, K = 384, 768, 128
     pa, sa, pb, sb = _operands(M, N, K, seed=77)
     blk = {"1x32": L.LPFA_BLK_1X32, "32x32": L.LPFA_BLK_32X32}[block]
@@ -166,7 +168,7 @@ def test_mx_gemm_quantize_codes_against_exact_product(L, block):
     torch.cuda.synchronize()
     exact = mx.mx_gemm(pa, sa, pb, sb)
     absprod = np.abs(mx.dq_1x32(pa, sa)) @ np.abs(mx.dq_1x32(pb, sb)).T
-    bound = 1e-5 * absprod
+    bound = 1e-6 * absprod
     # observed accumulation error, for the record (decides nothing)
     print("max |d - exact| / sum|a||b| =",
           float(np.max(np.abs(d.cpu().numpy() - exact) / absprod)))
@@ -180,5 +182,5 @@ def test_mx_gemm_quantize_codes_against_exact_product(L, block):
     print(f"{block}: {differ.sum()} of {differ.size} blocks differ, "
           f"{open_.sum()} open")
     assert not np.any(differ & ~open_)
-    if block == "1x32":
-        assert open_.mean() < 0.5        # the check decides most blocks
+    # the check decides most blocks
+    assert open_.mean() < (0.1 if block == "1x32" else 0.6)
