@@ -7,8 +7,9 @@
  * (lpfa_fwd, lpfa_bwd, lpfa_bwd_noalloc) with their workspace queries and
  * lpfa_check, the jagged scale-row offsets (lpfa_varlen_sf_rows), the fused
  * producers of quantized operands (lpfa_rmsnorm_mx_quantize,
- * lpfa_mx_gemm_quantize), the block-scaled GEMM (lpfa_mx_gemm) and the
- * status / version / device queries.
+ * lpfa_mx_gemm_quantize), the block-scaled GEMM (lpfa_mx_gemm), the
+ * tensor-pipe rate microbench (lpfa_mma_peak), the forward's bounded-wait
+ * self-test and the status / version / device queries.
  *
  * Sources of the operations (page title, section):
  *  [P1] "Low Precision Flash Attention 4: End-to-End Block-Scaled Attention
@@ -231,6 +232,20 @@ lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
                          int64_t K, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Tensor-pipe rate of block-scaled MXFP8 MMAs, for the roofline of the
+ * attention kernels ([P1] paragraph 2: tcgen05.mma.block_scale).  One CTA
+ * per SM issues M128 N256 K32 kind::mxf8f6f4 block-scaled MMAs (E4M3
+ * operands resident in shared memory, UE8M0 scales in tensor memory) back to
+ * back for about 17 ms; *flops_per_s receives 2*M*N*K per MMA times the MMAs
+ * of all CTAs over the CUDA-event time of that launch (after a warm-up
+ * launch).  Synchronises `stream`.  Allocates no device memory (its error
+ * word is a static device variable).  Errors: flops_per_s NULL ->
+ * LPFA_ERR_INVALID_ARG; a launch failure -> LPFA_ERR_CUDA; the kernel's
+ * bounded wait expired -> LPFA_ERR_TIMEOUT.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mma_peak(double* flops_per_s, void* stream);
+
+/* ------------------------------------------------------------------------
  * Block-scaled MXFP8 GEMM with a quantizing epilogue ([P1] paragraph 2:
  * fused GEMM+Quantize kernels producing FP8 output with dual scale factor
  * layouts in one pass).  The fp32 result D = A * B^T (operands and
@@ -304,6 +319,17 @@ lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
                      const void* v8, const void* sfv_mma, void* o, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* Forward in bf16 ([P1] paragraph 1: the MXFP8 kernels are measured against
+ * their bf16 counterparts).  The same algorithm and kernel structure as
+ * lpfa_fwd with kind::f16 MMAs on bf16 operands and no block scales: S = c q
+ * k^T in fp32, the same online softmax (rescale_threshold as in the
+ * descriptor), P rounded to bf16 for the PV product, l summed in fp32.
+ *  q [T, Hq, D], k, v [T, Hkv, D]: bf16, token-major, 16-byte aligned.
+ *  o, lse, workspace, errors: as lpfa_fwd. */
+lpfa_status lpfa_fwd_bf16(const lpfa_attn_desc* desc, const void* q, const void* k,
+                          const void* v, void* o, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Self-test of the forward's bounded waits (failure detection; the pages
  * have no counterpart).  Runs lpfa_fwd's kernel with every wait bounded by
  * wait_limit_us microseconds (1 .. 2e6) instead of 2 s, and with the copy of
@@ -339,6 +365,18 @@ lpfa_status lpfa_bwd(const lpfa_attn_desc* desc,
                      const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward in bf16 ([P1] paragraph 1: the bf16 counterpart the MXFP8 kernels
+ * are measured against).  lpfa_bwd's kernel with kind::f16 MMAs on bf16
+ * operands and no block scales: P^T and dS^T are rounded to bf16 for their
+ * products, dQ is accumulated in FP16 with the static scale as in lpfa_bwd.
+ *  q [T, Hq, D], k, v [T, Hkv, D], o, dout [T, Hq, D]: bf16 (dout is both
+ *  the dO operand and the D_i input); lse, dq, dk, dv, workspace, errors: as
+ *  lpfa_bwd.  head_dim 128 only (64 -> LPFA_ERR_UNSUPPORTED). */
+lpfa_status lpfa_bwd_bf16(const lpfa_attn_desc* desc, const void* q, const void* k,
+                          const void* v, const void* o, const void* dout, const float* lse,
+                          void* dq, void* dk, void* dv, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * lpfa_bwd_noalloc — the backward for callers that cannot allocate device

@@ -45,16 +45,28 @@ namespace {
 
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
-constexpr int kStages = 5;   // Q / dO ring: loads run several steps ahead
-constexpr int kDqBufs = 4;   // dQ staging tiles per compute warp (reduce-adds in flight)
 constexpr int kThreads = 320;
 constexpr int kTmemCols = 512;
 
-// Layout for head_dim D (64 or 128).
-template <int D>
+// Layout for head_dim D (64 or 128).  B16 selects the bf16 variant (kind::f16
+// MMAs on bf16 operands, P^T and dS^T rounded to bf16, no block scales),
+// which exists to measure the MXFP8 kernel against the same algorithm in
+// bf16.  Operand tiles are stored as chunks of at most 128 bytes per row (one
+// swizzle span): a bf16 row of 128 channels is two chunks, [chunk][rows][128 B].
+template <int D, bool B16>
 struct BwdCfg {
-  static constexpr uint32_t kSw = D == 128 ? 2u : 4u;   // 128B / 64B swizzle
-  static constexpr uint32_t kSbo = 8 * D;                // 8 rows of D bytes
+  static constexpr int kEl = B16 ? 2 : 1;                // bytes per element
+  static constexpr int kRowB = D * kEl;                  // bytes per token row
+  static constexpr int kChunkB = kRowB < 128 ? kRowB : 128;
+  static constexpr int kNCh = kRowB / kChunkB;           // chunks per row
+  static constexpr uint32_t kSw = kChunkB == 128 ? 2u : 4u;   // 128B / 64B swizzle
+  static constexpr uint32_t kSbo = 8 * kChunkB;               // 8 rows of a chunk
+  static constexpr int kStages = B16 ? 3 : 5;   // Q / dO ring: loads run steps ahead
+  static constexpr int kDqBufs = B16 ? 2 : 4;   // dQ staging tiles per compute warp
+  static constexpr int kKSteps = kRowB / 32;    // MMA K-steps over head_dim (32 bytes each)
+  static constexpr int kQPerStep = 32 / kEl;    // queries / keys contracted per MMA
+  // P^T and dS^T of a warpgroup's 32 queries: TMEM columns per key row
+  static constexpr uint32_t kPCols = 8 * kEl;
   // TMEM columns
   static constexpr uint32_t kColDK = 0, kColDV = D, kColS = 2 * D,
                             kColDP = 2 * D + 64, kColDQ = 2 * D + 128;
@@ -68,25 +80,29 @@ struct BwdCfg {
   // each, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
   static constexpr uint32_t kColOnesL = kColSF + 48, kColOnesD = kColSF + 56;
   // shared memory (bytes from a 1024-aligned base)
-  static constexpr int kSmK = 0;                                  // 128 x D (SW D)
-  static constexpr int kSmV = (kBN * D + 1023) / 1024 * 1024;     // 128 x D
-  // A operand of dQ^T = K^T dS^T needs 128-byte rows: for D = 64 a copy of
-  // the K tile zero-padded to 128 channels (64..127 give rows of zeros that
-  // are never read back); for D = 128 the K tile itself
-  static constexpr int kSmKT = kSmV + kBN * D;
-  static constexpr int kKTBytes = D == 128 ? 0 : kBN * 128;
+  static constexpr int kSmK = 0;                                  // 128 x D
+  static constexpr int kSmV = (kBN * kRowB + 1023) / 1024 * 1024; // 128 x D
+  // A operand of dQ^T = K^T dS^T needs 128 rows (channels): for fp8 D = 64 a
+  // copy of the K tile zero-padded to 128 channels (64..127 give rows of
+  // zeros that are never read back); otherwise the K tile itself
+  static constexpr int kSmKT = kSmV + kBN * kRowB;
+  static constexpr int kKTBytes = kRowB == 64 ? kBN * 128 : 0;
   static constexpr int kSmStage0 = kSmKT + kKTBytes;              // Q, dO, SFs, LSE2, Delta
   static constexpr int kStQ = 0;
-  static constexpr int kStdO = kBQ * D;
-  static constexpr int kStSF = 2 * kBQ * D;                       // SFQ, SFQt, SFdO, SFdOt
-  static constexpr int kStLse = kStSF + 4 * 512;                  // 64 floats
+  static constexpr int kStdO = kBQ * kRowB;
+  static constexpr int kStSF = 2 * kBQ * kRowB;                   // SFQ, SFQt, SFdO, SFdOt
+  static constexpr int kStLse = kStSF + (B16 ? 0 : 4 * 512);      // 64 floats
   static constexpr int kStDelta = kStLse + kBQ * 4;               // 64 floats
   // accumulator seeds: [64 queries][16 bf16] K-major, 32-byte swizzle; row q
   // holds hi, lo of -LSE_q / c (k = 0, 1) and of -D_q (k = 2, 3)
   static constexpr int kStSeed = ((kStDelta + kBQ * 4) + 255) / 256 * 256;
   static constexpr int kStageBytes = ((kStSeed + kBQ * 32) + 1023) / 1024 * 1024;
-  static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes; // 128 x 64 B (SW64)
-  static constexpr int kSmSFdS = kSmDS + kBN * kBQ;               // 512 B
+  // dS^T tile [128 keys][64 queries]: 64-byte rows, 64B swizzle (fp8) or
+  // 128-byte rows, 128B swizzle (bf16)
+  static constexpr int kDsRowB = kBQ * kEl;
+  static constexpr uint32_t kDsSw = kDsRowB == 128 ? 2u : 4u;
+  static constexpr int kSmDS = kSmStage0 + kStages * kStageBytes;
+  static constexpr int kSmSFdS = kSmDS + kBN * kDsRowB;           // 512 B
   static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
   // dQ staging: per compute warp kDqBufs [32 queries][32 channels] fp16
   // tiles, 64-byte rows, 64B swizzle (2 KB each, 1024-aligned)
@@ -117,6 +133,7 @@ struct BwdParams {
   float dq_mult;         // softmax_scale * dq_static_scale
 };
 
+template <int kStages>
 struct BwdBars {
   uint64_t kv_full;
   uint64_t q_full[kStages];    // Q, dO, scales landed and the seed tile written
@@ -195,7 +212,16 @@ __device__ __forceinline__ uint32_t warp_max_nonneg_bits(float x) {
   return __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(x));
 }
 
-template <int D>
+// Shared-memory descriptor offset (16-byte units) of K-step kb (32 bytes of
+// K) of a K-major operand tile stored in chunks of kChunkB-byte rows, `rows`
+// rows each.
+template <int kChunkB>
+__device__ __forceinline__ constexpr uint64_t kstep_off(int kb, int rows) {
+  return static_cast<uint64_t>((kb / (kChunkB / 32)) * rows * kChunkB +
+                               (kb % (kChunkB / 32)) * 32) >> 4;
+}
+
+template <int D, bool B16>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_attn_bwd_kernel(const __grid_constant__ CUtensorMap tma_q,
                        const __grid_constant__ CUtensorMap tma_k,
@@ -203,11 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tma_do,
                        const __grid_constant__ CUtensorMap tma_dq,
                        const BwdParams p) {
-  using C = BwdCfg<D>;
+  using C = BwdCfg<D, B16>;
+  constexpr int kStages = C::kStages;
+  constexpr int kDqBufs = C::kDqBufs;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  BwdBars* bars = reinterpret_cast<BwdBars*>(sm + C::kSmBar);
+  BwdBars<kStages>* bars = reinterpret_cast<BwdBars<kStages>*>(sm + C::kSmBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -276,12 +304,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int32_t row_k = static_cast<int32_t>(w.start + k0);
     const int64_t ksf = (w.sf_tile0 + w.ktile) * p.hkv + w.kvh;
-    mbar_arrive_expect_tx_elect(&bars->kv_full, 2 * kBN * D + 3 * 512);
-    tma_load_3d_elect(sm + C::kSmK, &tma_k, 0, w.kvh, row_k, &bars->kv_full);
-    tma_load_3d_elect(sm + C::kSmV, &tma_v, 0, w.kvh, row_k, &bars->kv_full);
-    bulk_load_elect(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
-    bulk_load_elect(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
-    bulk_load_elect(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+    mbar_arrive_expect_tx_elect(&bars->kv_full, 2 * kBN * C::kRowB + (B16 ? 0 : 3 * 512));
+#pragma unroll
+    for (int c = 0; c < C::kNCh; ++c) {
+      const int32_t x = c * (C::kChunkB / C::kEl);
+      tma_load_3d_elect(sm + C::kSmK + c * kBN * C::kChunkB, &tma_k, x, w.kvh, row_k,
+                        &bars->kv_full);
+      tma_load_3d_elect(sm + C::kSmV + c * kBN * C::kChunkB, &tma_v, x, w.kvh, row_k,
+                        &bars->kv_full);
+    }
+    if constexpr (!B16) {
+      bulk_load_elect(sm + C::kSmSFkv, p.sfk + ksf * 512, 512, &bars->kv_full);
+      bulk_load_elect(sm + C::kSmSFkv + 512, p.sfk_t + ksf * 512, 512, &bars->kv_full);
+      bulk_load_elect(sm + C::kSmSFkv + 1024, p.sfv + ksf * 512, 512, &bars->kv_full);
+    }
     // Zeroed seed tiles (32-byte swizzle: the 16-byte half k/8 of row r
     // sits at half (k/8) ^ ((r >> 2) & 1)).  The first q_full arrival below
     // publishes them to the tensor pipe.
@@ -305,16 +341,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = step_head(i), q0 = step_q0(i);
       uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
       uint64_t* bar = &bars->q_full[s];
-      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * D + 4 * 512);
+      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * C::kRowB + (B16 ? 0 : 4 * 512));
       const int32_t row_q = static_cast<int32_t>(w.start + q0);
-      tma_load_3d_elect(st + C::kStQ, &tma_q, 0, h, row_q, bar);
-      tma_load_3d_elect(st + C::kStdO, &tma_do, 0, h, row_q, bar);
+#pragma unroll
+      for (int c = 0; c < C::kNCh; ++c) {
+        const int32_t x = c * (C::kChunkB / C::kEl);
+        tma_load_3d_elect(st + C::kStQ + c * kBQ * C::kChunkB, &tma_q, x, h, row_q, bar);
+        tma_load_3d_elect(st + C::kStdO + c * kBQ * C::kChunkB, &tma_do, x, h, row_q, bar);
+      }
       const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
-      const int64_t qsf = (pr / 128) * p.hq + h;
-      bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
-      bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
-      bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
-      bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+      if constexpr (!B16) {
+        const int64_t qsf = (pr / 128) * p.hq + h;
+        bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
+        bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
+        bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
+        bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+      }
       const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
       uint64_t* lbar = &bars->lse_full[s];
       mbar_arrive_expect_tx_elect(lbar, 2 * kBQ * 4);
@@ -367,16 +409,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows (MN-major operands) to the 14-bit address field, which never
     // carries (shared memory addresses stay below 256 KB).  The step loop is
     // unrolled by the ring depth so that stage indices are constants.
-    constexpr uint32_t id_st = idesc_mxf8(128, kBQ, 0, 0);     // S^T, dP^T
-    constexpr uint32_t id_acc = idesc_mxf8(128, D, 0, 1);     // dV, dK (B MN-major)
-    constexpr uint32_t id_dq = idesc_mxf8(128, kBQ, 1, 1);     // dQ^T (A, B MN-major)
+    constexpr uint32_t id_st = B16 ? idesc_bf16(128, kBQ, 0, 0)
+                                   : idesc_mxf8(128, kBQ, 0, 0);   // S^T, dP^T
+    constexpr uint32_t id_acc = B16 ? idesc_bf16(128, D, 0, 1)
+                                    : idesc_mxf8(128, D, 0, 1);    // dV, dK (B MN-major)
+    constexpr uint32_t id_dq = B16 ? idesc_bf16(128, kBQ, 1, 1)
+                                   : idesc_mxf8(128, kBQ, 1, 1);   // dQ^T (A, B MN-major)
+    // MN-major operands of several 128-byte chunks per row repeat the swizzle
+    // pattern along MN every chunk (the leading offset); K-major operands
+    // ignore it
     const uint64_t dk_ = make_sdesc(smem_u32(sm + C::kSmK), 16, C::kSbo, C::kSw);
     const uint64_t dv_ = make_sdesc(smem_u32(sm + C::kSmV), 16, C::kSbo, C::kSw);
-    const uint64_t dkt = make_sdesc(D == 128 ? smem_u32(sm + C::kSmK) : smem_u32(sm + C::kSmKT),
-                                    16, 1024, 2);
-    const uint64_t dds = make_sdesc(smem_u32(sm + C::kSmDS), 16, 8 * kBQ, 4);
-    const uint64_t dq_ = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStQ), 16, C::kSbo, C::kSw);
-    const uint64_t ddo = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStdO), 16, C::kSbo, C::kSw);
+    const uint64_t dkt = make_sdesc(C::kKTBytes == 0 ? smem_u32(sm + C::kSmK) : smem_u32(sm + C::kSmKT),
+                                    C::kNCh > 1 ? kBN * C::kChunkB : 16, 1024, 2);
+    const uint64_t dds = make_sdesc(smem_u32(sm + C::kSmDS), 16, 8 * C::kDsRowB, C::kDsSw);
+    constexpr uint32_t kQLbo = C::kNCh > 1 ? kBQ * C::kChunkB : 16;
+    const uint64_t dq_ = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStQ), kQLbo, C::kSbo, C::kSw);
+    const uint64_t ddo = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStdO), kQLbo, C::kSbo, C::kSw);
     const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSmStage0 + C::kStSF));
     // seed MMAs (bf16, K = 16): S^T <- -LSE / c, dP^T <- -D, broadcast over keys
     constexpr uint32_t id_seed = idesc_bf16(128, kBQ, 0, 0);
@@ -385,9 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 50);
     if (ok) {
       tc_fence_after();
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFK, sf_tile_desc(smem_u32(sm + C::kSmSFkv)));
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
+      if constexpr (!B16) {
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFK, sf_tile_desc(smem_u32(sm + C::kSmSFkv)));
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFKt, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 512)));
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFV, sf_tile_desc(smem_u32(sm + C::kSmSFkv + 1024)));
+      }
     }
     // S^T(i) = K Q_i^T and dP^T(i) = V dO_i^T (contraction over head_dim)
     auto issue_st = [&](int i, int s) -> bool {
@@ -395,20 +446,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
       const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
+      if constexpr (!B16) {
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
+      }
       mma_bf16_ts_elect(tmem + C::kColS, tmem + C::kColOnesL, dseed + so, id_seed, 0);
 #pragma unroll
-      for (int kb = 0; kb < D / 32; ++kb)
-        mma_mxf8_ss_elect(tmem + C::kColS, dk_ + 2 * kb, dq_ + so + 2 * kb,
-                          idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
-                          tmem + C::kColSFQ + 2 * half, 1);
+      for (int kb = 0; kb < C::kKSteps; ++kb) {
+        const uint64_t ka = kstep_off<C::kChunkB>(kb, kBN), kq = kstep_off<C::kChunkB>(kb, kBQ);
+        if constexpr (B16)
+          mma_bf16_ss_elect(tmem + C::kColS, dk_ + ka, dq_ + so + kq, id_st, 1);
+        else
+          mma_mxf8_ss_elect(tmem + C::kColS, dk_ + ka, dq_ + so + kq,
+                            idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
+                            tmem + C::kColSFQ + 2 * half, 1);
+      }
       mma_bf16_ts_elect(tmem + C::kColDP, tmem + C::kColOnesD, dseed + so, id_seed, 0);
 #pragma unroll
-      for (int kb = 0; kb < D / 32; ++kb)
-        mma_mxf8_ss_elect(tmem + C::kColDP, dv_ + 2 * kb, ddo + so + 2 * kb,
-                          idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
-                          tmem + C::kColSFdO + 2 * half, 1);
+      for (int kb = 0; kb < C::kKSteps; ++kb) {
+        const uint64_t ka = kstep_off<C::kChunkB>(kb, kBN), kq = kstep_off<C::kChunkB>(kb, kBQ);
+        if constexpr (B16)
+          mma_bf16_ss_elect(tmem + C::kColDP, dv_ + ka, ddo + so + kq, id_st, 1);
+        else
+          mma_mxf8_ss_elect(tmem + C::kColDP, dv_ + ka, ddo + so + kq,
+                            idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFV,
+                            tmem + C::kColSFdO + 2 * half, 1);
+      }
       tc_commit_elect(&bars->st_ready);
       return true;
     };
@@ -419,27 +482,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
       const uint32_t half = static_cast<uint32_t>((step_q0(i) / kBQ) & 1);
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQt, dsf + so + (512 >> 4));
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdOt, dsf + so + (1536 >> 4));
-      tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdSB, dsfds);
+      // K-step (C::kQPerStep queries or keys) strides of the MN-major
+      // operands: Q / dO rows, K rows (dQ^T's A), dS^T rows
+      constexpr uint64_t kQStep = (C::kQPerStep * C::kChunkB) >> 4;
+      constexpr uint64_t kKtStep = (C::kQPerStep * 128) >> 4;
+      constexpr uint64_t kDsStep = (C::kQPerStep * C::kDsRowB) >> 4;
+      if constexpr (B16) {
+        // block g of the step's queries: P^T at dQ^T columns 32g, dS^T at
+        // 32g + 16, 8 columns (16 queries) per K-step
 #pragma unroll
-      for (int kb = 0; kb < kBQ / 32; ++kb) {
-        const uint32_t sfb = kb + 2 * half;
-        mma_mxf8_ts_elect(tmem + C::kColDV, tmem + C::kColDQ + 32 * kb,
-                          ddo + so + kb * ((32 * D) >> 4), idesc_sf_ids(id_acc, 0, sfb),
-                          tmem + C::kColSFP + 4 * kb, tmem + C::kColSFdOt, (i > 0) || (kb > 0));
-        mma_mxf8_ts_elect(tmem + C::kColDK, tmem + C::kColDQ + 32 * kb + 8,
-                          dq_ + so + kb * ((32 * D) >> 4), idesc_sf_ids(id_acc, 0, sfb),
-                          tmem + C::kColSFdS + 4 * kb, tmem + C::kColSFQt, (i > 0) || (kb > 0));
-      }
-      if (D != 128 && i == 0) {
-        if (!mbar_wait_sleep(&bars->kt_ready, 0, p.err, abort, 54)) return false;
-      }
+        for (int kb = 0; kb < kBQ / C::kQPerStep; ++kb) {
+          const uint32_t col = C::kColDQ + 32 * (kb >> 1) + 8 * (kb & 1);
+          mma_bf16_ts_elect(tmem + C::kColDV, tmem + col, ddo + so + kb * kQStep, id_acc,
+                            (i > 0) || (kb > 0));
+          mma_bf16_ts_elect(tmem + C::kColDK, tmem + col + C::kPCols, dq_ + so + kb * kQStep,
+                            id_acc, (i > 0) || (kb > 0));
+        }
 #pragma unroll
-      for (int kb = 0; kb < kBN / 32; ++kb)
-        mma_mxf8_ss_elect(tmem + C::kColDQ, dkt + kb * ((32 * 128) >> 4),
-                          dds + kb * ((32 * kBQ) >> 4), idesc_sf_ids(id_dq, kb, kb),
-                          tmem + C::kColSFKt, tmem + C::kColSFdSB, kb > 0);
+        for (int kb = 0; kb < kBN / C::kQPerStep; ++kb)
+          mma_bf16_ss_elect(tmem + C::kColDQ, dkt + kb * kKtStep, dds + kb * kDsStep, id_dq,
+                            kb > 0);
+      } else {
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQt, dsf + so + (512 >> 4));
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdOt, dsf + so + (1536 >> 4));
+        tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdSB, dsfds);
+#pragma unroll
+        for (int kb = 0; kb < kBQ / 32; ++kb) {
+          const uint32_t sfb = kb + 2 * half;
+          mma_mxf8_ts_elect(tmem + C::kColDV, tmem + C::kColDQ + 32 * kb,
+                            ddo + so + kb * kQStep, idesc_sf_ids(id_acc, 0, sfb),
+                            tmem + C::kColSFP + 4 * kb, tmem + C::kColSFdOt, (i > 0) || (kb > 0));
+          mma_mxf8_ts_elect(tmem + C::kColDK, tmem + C::kColDQ + 32 * kb + C::kPCols,
+                            dq_ + so + kb * kQStep, idesc_sf_ids(id_acc, 0, sfb),
+                            tmem + C::kColSFdS + 4 * kb, tmem + C::kColSFQt, (i > 0) || (kb > 0));
+        }
+        if (C::kKTBytes != 0 && i == 0) {
+          if (!mbar_wait_sleep(&bars->kt_ready, 0, p.err, abort, 54)) return false;
+        }
+#pragma unroll
+        for (int kb = 0; kb < kBN / 32; ++kb)
+          mma_mxf8_ss_elect(tmem + C::kColDQ, dkt + kb * kKtStep, dds + kb * kDsStep,
+                            idesc_sf_ids(id_dq, kb, kb), tmem + C::kColSFKt,
+                            tmem + C::kColSFdSB, kb > 0);
+      }
       // the compute warps release the Q / dO stage once they see dQ^T(i)
       tc_commit_elect(&bars->dq_full);
       return true;
@@ -473,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = k0 + m;
     const int ctid = threadIdx.x - 64;            // 0..255 among compute threads
     bool ok = true;
-    if (D != 128 && g == 0) {
+    if (C::kKTBytes != 0 && g == 0) {
       // zero-padded 128-byte-row copy of the K tile (64B swizzle -> 128B)
       ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 59);
       if (ok) {
@@ -504,7 +589,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_dq_store = [&](int j, const uint32_t (&rq)[32]) {
       if (quad * 32 >= D) return;                  // no channels here (D = 64)
       const uint32_t sbase = smem_u32(sm + C::kSmDQ + ((warp - 2) * kDqBufs + (j & (kDqBufs - 1))) * 2048);
-      if (lane == 0) bulk_wait_read_le3();        // step j-4's reduce has read it
+      // step j-kDqBufs's reduce has read the slot
+      if (lane == 0) {
+        if constexpr (kDqBufs == 4) bulk_wait_read_le3();
+        else bulk_wait_read_le1();
+      }
       __syncwarp();
       const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
       const int cb = lane >> 3;                   // channel block whose row this lane addresses
@@ -581,10 +670,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // P's block amax is 2^(max x) (2^x is monotonic); its warp reduction
       // is under way while the exponentials run
-      float mx = fmaxf(xv[0], xv[1]);
+      uint32_t ap_bits = 0;
+      if constexpr (!B16) {
+        float mx = fmaxf(xv[0], xv[1]);
 #pragma unroll
-      for (int j = 2; j < 32; j += 2) mx = max3(mx, xv[j], xv[j + 1]);
-      const uint32_t ap_bits = warp_max_nonneg_bits(ex2(mx));
+        for (int j = 2; j < 32; j += 2) mx = max3(mx, xv[j], xv[j + 1]);
+        ap_bits = warp_max_nonneg_bits(ex2(mx));
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) pv[j] = ex2(xv[j]);
       // dS = P (dP - D); TMEM holds dP^T - D (seeded accumulator)
@@ -595,14 +687,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         dsv[j] = lo2(ds);
         dsv[j + 1] = hi2(ds);
       }
-      float md = max3_abs_nan(dsv[0], dsv[1], dsv[2]);
+      // fp8: 32x32 block codes (warp maxima) and E4M3 payloads; bf16: pairs
+      uint32_t wp[4 * C::kEl * 2], wd[4 * C::kEl * 2];
+      uint32_t cp_ = 0, cd = 0;
+      if constexpr (B16) {
 #pragma unroll
-      for (int j = 3; j < 31; j += 2) md = max3_abs_nan(md, dsv[j], dsv[j + 1]);
-      md = max3_abs_nan(md, dsv[31], 0.f);
-      const uint32_t ad_bits = warp_max_nonneg_bits(md);
-      uint32_t wp[8], wd[8];
-      const uint32_t cp_ = quant_block32(pv, ap_bits, wp);
-      const uint32_t cd = quant_block32(dsv, ad_bits, wd);
+        for (int j = 0; j < 16; ++j) {
+          const __nv_bfloat162 a = __floats2bfloat162_rn(pv[2 * j], pv[2 * j + 1]);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(dsv[2 * j], dsv[2 * j + 1]);
+          wp[j] = *reinterpret_cast<const uint32_t*>(&a);
+          wd[j] = *reinterpret_cast<const uint32_t*>(&b);
+        }
+      } else {
+        float md = max3_abs_nan(dsv[0], dsv[1], dsv[2]);
+#pragma unroll
+        for (int j = 3; j < 31; j += 2) md = max3_abs_nan(md, dsv[j], dsv[j + 1]);
+        md = max3_abs_nan(md, dsv[31], 0.f);
+        const uint32_t ad_bits = warp_max_nonneg_bits(md);
+        cp_ = quant_block32(pv, ap_bits, wp);
+        cd = quant_block32(dsv, ad_bits, wd);
+      }
       // the previous step's dQ^T leaves TMEM before this step's fp8 P^T /
       // dS^T take its columns (and its MMA, the last reader of the dS^T
       // shared-memory tile, has completed)
@@ -611,24 +715,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = read_dq(i - 1, rq);
         if (!ok) break;
       }
-      // P^T, dS^T (fp8) at dQ^T columns 32g and 32g + 8; their A-operand
-      // scales at lane m, column base + 4g + m/32
-      tmem_st8(tmem + lb + C::kColDQ + 32 * g, wp);
-      tmem_st8(tmem + lb + C::kColDQ + 32 * g + 8, wd);
-      tmem_st1(tmem + lb + C::kColSFP + 4 * g + quad, cp_);
-      tmem_st1(tmem + lb + C::kColSFdS + 4 * g + quad, cd);
-      // dS^T row chunks 2g, 2g+1 -> shared memory (64-byte rows, 64B swizzle)
+      // P^T, dS^T at dQ^T columns 32g and 32g + kPCols; (fp8) their
+      // A-operand scales at lane m, column base + 4g + m/32
+      if constexpr (B16) {
+        tmem_st16(tmem + lb + C::kColDQ + 32 * g, wp);
+        tmem_st16(tmem + lb + C::kColDQ + 32 * g + C::kPCols, wd);
+      } else {
+        tmem_st8(tmem + lb + C::kColDQ + 32 * g, wp);
+        tmem_st8(tmem + lb + C::kColDQ + 32 * g + C::kPCols, wd);
+        tmem_st1(tmem + lb + C::kColSFP + 4 * g + quad, cp_);
+        tmem_st1(tmem + lb + C::kColSFdS + 4 * g + quad, cd);
+      }
+      // this warpgroup's 16-byte chunks of the key row -> the dS^T tile
+      // (fp8: 64-byte rows, 64B swizzle; bf16: 128-byte rows, 128B swizzle)
       {
-        uint8_t* ds_row = sm + C::kSmDS + m * kBQ;
+        constexpr int kCh = 2 * C::kEl;          // 16-byte chunks per 32 queries
+        uint8_t* ds_row = sm + C::kSmDS + m * C::kDsRowB;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int phys = (2 * g + c) ^ ((m >> 1) & 3);
+        for (int c = 0; c < kCh; ++c) {
+          const int phys = B16 ? ((kCh * g + c) ^ (m & 7)) : ((kCh * g + c) ^ ((m >> 1) & 3));
           *reinterpret_cast<uint4*>(ds_row + 16 * phys) =
               make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
         }
       }
       // B-operand scale of dQ^T: (query n = 32 g + lane, key block quad)
-      sm[C::kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
+      if constexpr (!B16) sm[C::kSmSFdS + lane * 16 + g * 4 + quad] = static_cast<uint8_t>(cd);
       if (i > 0) stage_dq_store(i - 1, rq);
       tmem_st_wait();
       fence_proxy_async_smem();
@@ -773,22 +884,39 @@ extern "C" size_t lpfa_bwd_workspace_size(const lpfa_attn_desc* desc) {
   return bwd_ws_bytes(desc);
 }
 
-extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
-                                const void* sfq_mma, const void* sfq_mma_t,
-                                const void* k8, const void* sfk_mma,
-                                const void* sfk_mma_t, const void* v8,
-                                const void* sfv_mma, const void* do8,
-                                const void* sfdo_mma, const void* sfdo_mma_t,
-                                const void* o, const void* dout,
-                                const float* lse, void* dq, void* dk, void* dv,
-                                void* workspace, size_t workspace_bytes,
-                                void* stream) {
+namespace {
+
+template <int D, bool B16>
+lpfa_status launch_bwd_kernel(const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const CUtensorMap& tdo,
+                              const CUtensorMap& tdq, const BwdParams& p, int64_t nblocks,
+                              cudaStream_t cs) {
+  const size_t smem = BwdCfg<D, B16>::kSmTotal + 1024;
+  lpfa_status st = set_max_dynamic_smem(
+      reinterpret_cast<const void*>(&mx_attn_bwd_kernel<D, B16>), static_cast<int>(smem));
+  if (st != LPFA_OK) return st;
+  mx_attn_bwd_kernel<D, B16><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
+      tq, tk, tv, tdo, tdq, p);
+  return LPFA_OK;
+}
+
+lpfa_status bwd_impl(const lpfa_attn_desc* desc, const void* q8,
+                     const void* sfq_mma, const void* sfq_mma_t,
+                     const void* k8, const void* sfk_mma,
+                     const void* sfk_mma_t, const void* v8,
+                     const void* sfv_mma, const void* do8,
+                     const void* sfdo_mma, const void* sfdo_mma_t,
+                     const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes, bool bf16,
+                     void* stream) {
   SeqView sv;
   lpfa_status st = validate_attn(desc, &sv);
   if (st != LPFA_OK) return st;
-  LPFA_CHECK_ARG(q8 && sfq_mma && sfq_mma_t && k8 && sfk_mma && sfk_mma_t && v8 &&
-                 sfv_mma && do8 && sfdo_mma && sfdo_mma_t && o && dout && lse &&
-                 dq && dk && dv);
+  if (bf16 && desc->head_dim != 128) return LPFA_ERR_UNSUPPORTED;
+  LPFA_CHECK_ARG(q8 && k8 && v8 && do8 && o && dout && lse && dq && dk && dv);
+  LPFA_CHECK_ARG(bf16 || (sfq_mma && sfq_mma_t && sfk_mma && sfk_mma_t && sfv_mma &&
+                          sfdo_mma && sfdo_mma_t));
   const void* ptrs[] = {q8, sfq_mma, sfq_mma_t, k8, sfk_mma, sfk_mma_t, v8, sfv_mma,
                         do8, sfdo_mma, sfdo_mma_t, o, dout, lse, dq, dk, dv};
   for (const void* ptr : ptrs) LPFA_CHECK_ARG(aligned16(ptr));
@@ -822,13 +950,18 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
   }
 
   CUtensorMap tq, tk, tv, tdo;
-  const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  // [tokens][heads][D] elements; a box is one chunk (<= 128 bytes) of `rows`
+  // token rows of one head
+  const int64_t el = bf16 ? 2 : 1;
+  const int64_t chunk = D * el < 128 ? D * el : 128;
+  const CUtensorMapSwizzle sw = chunk == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   auto make = [&](CUtensorMap* m, const void* base, int64_t heads, uint32_t rows) {
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
                         static_cast<uint64_t>(sv.total_tokens)};
-    uint64_t strides[2] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads * D)};
-    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, rows};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, sw);
+    uint64_t strides[2] = {static_cast<uint64_t>(D * el), static_cast<uint64_t>(heads * D * el)};
+    uint32_t box[3] = {static_cast<uint32_t>(chunk / el), 1u, rows};
+    return encode_tmap(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       3, base, dims, strides, box, sw);
   };
   if ((st = make(&tq, q8, hq, kBQ)) != LPFA_OK) return st;
   if ((st = make(&tdo, do8, hq, kBQ)) != LPFA_OK) return st;
@@ -870,21 +1003,13 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
 
   const int64_t nblocks = (sv.total_sf_rows / 128) * hkv;
   LPFA_CHECK_ARG(nblocks > 0 && nblocks < (1ll << 31));
-  if (D == 128) {
-    const size_t smem = BwdCfg<128>::kSmTotal + 1024;
-    if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_bwd_kernel<128>),
-                                   static_cast<int>(smem))) != LPFA_OK)
-      return st;
-    mx_attn_bwd_kernel<128><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
-        tq, tk, tv, tdo, tdq, p);
-  } else {
-    const size_t smem = BwdCfg<64>::kSmTotal + 1024;
-    if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_bwd_kernel<64>),
-                                   static_cast<int>(smem))) != LPFA_OK)
-      return st;
-    mx_attn_bwd_kernel<64><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(
-        tq, tk, tv, tdo, tdq, p);
-  }
+  if (bf16)
+    st = launch_bwd_kernel<128, true>(tq, tk, tv, tdo, tdq, p, nblocks, cs);
+  else if (D == 128)
+    st = launch_bwd_kernel<128, false>(tq, tk, tv, tdo, tdq, p, nblocks, cs);
+  else
+    st = launch_bwd_kernel<64, false>(tq, tk, tv, tdo, tdq, p, nblocks, cs);
+  if (st != LPFA_OK) return st;
   LPFA_CHECK_CUDA(cudaGetLastError());
   if (desc->dq_static_scale != 1.0f) {
     const int64_t n2 = sv.total_tokens * hq * D / 2;
@@ -893,6 +1018,33 @@ extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
     LPFA_CHECK_CUDA(cudaGetLastError());
   }
   return LPFA_OK;
+}
+
+}  // namespace
+
+extern "C" lpfa_status lpfa_bwd(const lpfa_attn_desc* desc, const void* q8,
+                                const void* sfq_mma, const void* sfq_mma_t,
+                                const void* k8, const void* sfk_mma,
+                                const void* sfk_mma_t, const void* v8,
+                                const void* sfv_mma, const void* do8,
+                                const void* sfdo_mma, const void* sfdo_mma_t,
+                                const void* o, const void* dout,
+                                const float* lse, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return bwd_impl(desc, q8, sfq_mma, sfq_mma_t, k8, sfk_mma, sfk_mma_t, v8, sfv_mma, do8,
+                  sfdo_mma, sfdo_mma_t, o, dout, lse, dq, dk, dv, workspace,
+                  workspace_bytes, false, stream);
+}
+
+extern "C" lpfa_status lpfa_bwd_bf16(const lpfa_attn_desc* desc, const void* q,
+                                     const void* k, const void* v, const void* o,
+                                     const void* dout, const float* lse, void* dq,
+                                     void* dk, void* dv, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return bwd_impl(desc, q, nullptr, nullptr, k, nullptr, nullptr, v, nullptr, dout,
+                  nullptr, nullptr, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                  true, stream);
 }
 
 // ---------------------------------------------------------------------------

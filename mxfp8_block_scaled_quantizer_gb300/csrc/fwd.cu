@@ -57,8 +57,6 @@ namespace lpfa {
 namespace {
 
 constexpr int kBlockM = 128;   // queries per CTA
-constexpr int kBlockN = 256;   // keys per key/value tile
-constexpr int kHalfN = 128;    // keys per softmax warpgroup
 constexpr int kThreads = 352;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
@@ -83,20 +81,39 @@ struct FwdParams {
                         // (-1 normally), so the waits on it must expire
 };
 
-template <int D>
+// Tile plan for head_dim D; B16 selects the bf16 variant (kind::f16 MMAs on
+// bf16 operands, no scale factors), which exists to measure the MXFP8 kernel
+// against the same algorithm in bf16.  Operand tiles are stored as chunks of
+// at most 128 bytes per row (one swizzle span): a bf16 row of 128 channels
+// is two chunks, [chunk][rows][128 B].
+template <int D, bool B16>
 struct FwdCfg {
-  static constexpr int kStages = D == 128 ? 3 : 4;
-  static constexpr int kQBytes = kBlockM * D;
-  static constexpr int kKVBytes = kBlockN * D;            // one of K, V
+  static constexpr int kN = B16 ? 128 : 256;              // keys per tile
+  static constexpr int kHalfN = kN / 2;                   // keys per softmax warpgroup
+  static constexpr int kChunks = kHalfN / 32;             // 32-key chunks per warpgroup
+  static constexpr int kEl = B16 ? 2 : 1;                 // bytes per element
+  static constexpr int kRowB = D * kEl;                   // bytes per token row
+  static constexpr int kChunkB = kRowB < 128 ? kRowB : 128;
+  static constexpr int kNCh = kRowB / kChunkB;            // chunks per row
+  static constexpr uint32_t kSw = kChunkB == 128 ? 2u : 4u;   // 128B / 64B swizzle
+  static constexpr uint32_t kSbo = 8 * kChunkB;               // 8 rows of a chunk
+  static constexpr int kStages = D == 128 ? (B16 ? 2 : 3) : 4;
+  static constexpr int kQBytes = kBlockM * kRowB;
+  static constexpr int kKVBytes = kN * kRowB;             // one of K, V
   static constexpr int kQ = 0;
   static constexpr int kStage0 = kQBytes;                 // stage s: K, V
   static constexpr int kStageBytes = 2 * kKVBytes;
   static constexpr int kSfQ = kStage0 + kStages * kStageBytes;
   static constexpr int kSfStage0 = kSfQ + 512;            // SFK[2], SFV[2]
-  static constexpr int kXMax = kSfStage0 + kStages * 2048;  // float [2][2][128]
+  static constexpr int kSfStageBytes = B16 ? 0 : 2048;
+  static constexpr int kXMax = kSfStage0 + kStages * kSfStageBytes;  // float [2][2][128]
   static constexpr int kXSum = kXMax + 2 * 2 * 128 * 4;     // float [2][128]
   static constexpr int kBar = kXSum + 2 * 128 * 4;
   static constexpr int kTotal = kBar + 256;
+  // one MMA instruction contracts 32 bytes of K (32 fp8 or 16 bf16 elements)
+  static constexpr int kKStepsS = kRowB / 32;             // S = Q K^T over head_dim
+  static constexpr int kKStepsPV = kN * kEl / 32;         // O += P V over the tile's keys
+  static constexpr int kKeysPerStep = 32 / kEl;
 };
 
 template <int S>
@@ -182,23 +199,34 @@ __device__ __forceinline__ int64_t round_item(const FwdParams& p, int r) {
   return idx < p.nitems ? idx : -1;
 }
 
-// Key/value tiles of an item.
+// Key/value tiles of an item (tiles of kN keys).
+template <int kN>
 __device__ __forceinline__ int item_tiles(const FwdParams& p, const WorkItem& w) {
   const int q0 = w.qtile * kBlockM;
   const int kv_len = p.causal ? min(w.len, q0 + kBlockM) : w.len;
-  return (kv_len + kBlockN - 1) / kBlockN;
+  return (kv_len + kN - 1) / kN;
 }
 
-template <int D>
+// Shared-memory descriptor offset (16-byte units) of K-step kb of a K-major
+// operand tile stored in chunks of kChunkB-byte rows, `rows` rows each.
+template <int kChunkB>
+__device__ __forceinline__ constexpr uint64_t kstep_off(int kb, int rows) {
+  return static_cast<uint64_t>((kb / (kChunkB / 32)) * rows * kChunkB +
+                               (kb % (kChunkB / 32)) * 32) >> 4;
+}
+
+template <int D, bool B16>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_attn_fwd_kernel(const __grid_constant__ CUtensorMap tma_q,
                        const __grid_constant__ CUtensorMap tma_k,
                        const __grid_constant__ CUtensorMap tma_v,
                        const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, B16>;
   constexpr int kStages = C::kStages;
-  constexpr uint32_t kSw = (D == 128) ? 2u : 4u;     // 128B / 64B swizzle
-  constexpr uint32_t kSbo = 8 * D;                    // 8 rows of D bytes
+  constexpr int kBlockN = C::kN;
+  constexpr int kHalfN = C::kHalfN;
+  constexpr uint32_t kSw = C::kSw;
+  constexpr uint32_t kSbo = C::kSbo;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -257,18 +285,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!work_item(p, idx, w)) continue;
       const int kvh = w.head / p.group;
       const int q0 = w.qtile * kBlockM;
-      const int ntiles = item_tiles(p, w);
+      const int ntiles = item_tiles<kBlockN>(p, w);
       // the Q tile (and its scale tile) is free once the previous item's
       // last S MMA has completed
       if (k > 0) {
         ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11, p.wait_ns);
         if (!ok) break;
       }
-      mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
-      tma_load_3d_elect(sm + C::kQ, &tma_q, 0, w.head, static_cast<int32_t>(w.start + q0),
+      mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + (B16 ? 0 : 512));
+#pragma unroll
+      for (int c = 0; c < C::kNCh; ++c)
+        tma_load_3d_elect(sm + C::kQ + c * kBlockM * C::kChunkB, &tma_q,
+                          c * (C::kChunkB / C::kEl), w.head,
+                          static_cast<int32_t>(w.start + q0), &bars->q_full);
+      if constexpr (!B16)
+        bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
                         &bars->q_full);
-      bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
-                      &bars->q_full);
       q_issued = k & 1;
       ++k;
       // scale tiles of keys past the sequence's padded rows belong to the
@@ -282,18 +314,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (gt == p.withhold_kv) continue;
         uint8_t* kbuf = sm + C::kStage0 + s * C::kStageBytes;
-        uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
         uint64_t* bar = &bars->kv_full[s];
-        mbar_arrive_expect_tx_elect(bar, 2 * C::kKVBytes + 2048);
+        mbar_arrive_expect_tx_elect(bar, 2 * C::kKVBytes + C::kSfStageBytes);
         const int32_t row_k = static_cast<int32_t>(w.start + j * kBlockN);
-        tma_load_3d_elect(kbuf, &tma_k, 0, kvh, row_k, bar);
-        tma_load_3d_elect(kbuf + C::kKVBytes, &tma_v, 0, kvh, row_k, bar);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t t = min(kv_sf0 + 2 * j + h, sf_last);
-          const int64_t off = (t * p.hkv + kvh) * 512;
-          bulk_load_elect(sfb + 512 * h, p.sfk + off, 512, bar);
-          bulk_load_elect(sfb + 1024 + 512 * h, p.sfv + off, 512, bar);
+        for (int c = 0; c < C::kNCh; ++c) {
+          const int32_t x = c * (C::kChunkB / C::kEl);
+          tma_load_3d_elect(kbuf + c * kBlockN * C::kChunkB, &tma_k, x, kvh, row_k, bar);
+          tma_load_3d_elect(kbuf + C::kKVBytes + c * kBlockN * C::kChunkB, &tma_v, x, kvh,
+                            row_k, bar);
+        }
+        if constexpr (!B16) {
+          uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t t = min(kv_sf0 + 2 * j + h, sf_last);
+            const int64_t off = (t * p.hkv + kvh) * 512;
+            bulk_load_elect(sfb + 512 * h, p.sfk + off, 512, bar);
+            bulk_load_elect(sfb + 1024 + 512 * h, p.sfv + off, 512, bar);
+          }
         }
         issued[s] = static_cast<int>(ph);
       }
@@ -322,25 +361,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int gt = 0, k = 0;
     if (warp == 1) {
-      constexpr uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t idesc_s = B16 ? idesc_bf16(kBlockM, kBlockN, 0, 0)
+                                       : idesc_mxf8(kBlockM, kBlockN, 0, 0);
       const uint64_t dq = make_sdesc(smem_u32(sm + C::kQ), 16, kSbo, kSw);
       const uint64_t dk = make_sdesc(smem_u32(sm + C::kStage0), 16, kSbo, kSw);
       const uint32_t tS = tmem + kColS, tSFQ = tmem + kColSFQ, tSFK = tmem + kColSFK;
-      // S = Q K^T (N = 256: two 128-key scale tiles side by side); S may be
-      // overwritten once every softmax warp holds its row of the previous S
+      // S = Q K^T (MXFP8: N = 256, two 128-key scale tiles side by side); S
+      // may be overwritten once every softmax warp holds its row of the
+      // previous S
       auto issue_s = [&](int g) -> bool {
         const int s = g % kStages;
         if (g > 0 && !mbar_wait_sleep(&bars->s_free, (g - 1) & 1, p.err, abort, 23, p.wait_ns)) return false;
         if (!mbar_wait_sleep(&bars->kv_full[s], (g / kStages) & 1, p.err, abort, 21, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
-        const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
-        tc_cp_32x128b_warpx4_elect(tSFK, dsf + fo);
-        tc_cp_32x128b_warpx4_elect(tSFK + 4, dsf + fo + (512 >> 4));
+        if constexpr (B16) {
 #pragma unroll
-        for (int kb = 0; kb < D / 32; ++kb)
-          mma_mxf8_ss_elect(tS, dq + 2 * kb, dk + so + 2 * kb,
-                            idesc_sf_ids(idesc_s, kb, kb), tSFQ, tSFK, kb > 0);
+          for (int kb = 0; kb < C::kKStepsS; ++kb)
+            mma_bf16_ss_elect(tS, dq + kstep_off<C::kChunkB>(kb, kBlockM),
+                              dk + so + kstep_off<C::kChunkB>(kb, kBlockN), idesc_s, kb > 0);
+        } else {
+          const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
+          tc_cp_32x128b_warpx4_elect(tSFK, dsf + fo);
+          tc_cp_32x128b_warpx4_elect(tSFK + 4, dsf + fo + (512 >> 4));
+#pragma unroll
+          for (int kb = 0; kb < C::kKStepsS; ++kb)
+            mma_mxf8_ss_elect(tS, dq + kstep_off<C::kChunkB>(kb, kBlockM),
+                              dk + so + kstep_off<C::kChunkB>(kb, kBlockN),
+                              idesc_sf_ids(idesc_s, kb, kb), tSFQ, tSFK, kb > 0);
+        }
         tc_commit_elect(&bars->s_full);
         return true;
       };
@@ -349,11 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx < 0) break;
         WorkItem w;
         if (!work_item(p, idx, w)) continue;
-        const int ntiles = item_tiles(p, w);
+        const int ntiles = item_tiles<kBlockN>(p, w);
         ok = mbar_wait_sleep(&bars->q_full, k & 1, p.err, abort, 20, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
+        if constexpr (!B16) tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
         for (int j = 0; j < ntiles && ok; ++j, ++gt) ok = issue_s(gt);
         // the item's last reader of the Q tile is issued: the tile is free
         // once it completes
@@ -361,8 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++k;
       }
     } else {
-      constexpr uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
-      const uint64_t dv = make_sdesc(smem_u32(sm + C::kStage0 + C::kKVBytes), 16, kSbo, kSw);
+      constexpr uint32_t idesc_o = B16 ? idesc_bf16(kBlockM, D, 0, 1)
+                                       : idesc_mxf8(kBlockM, D, 0, 1);
+      // V is MN-major (channels contiguous); a row of several 128-byte chunks
+      // repeats the swizzle pattern along N every chunk (the leading offset)
+      const uint64_t dv = make_sdesc(smem_u32(sm + C::kStage0 + C::kKVBytes),
+                                     C::kNCh > 1 ? kBlockN * C::kChunkB : 16, kSbo, kSw);
       const uint32_t tO = tmem + kColO, tP = tmem + kColP;
       const uint32_t tSFP = tmem + kColSFP, tSFV = tmem + kColSFV;
       // O (+)= P V over 256 keys (8 K-steps; scale group = K-step / 4); V
@@ -374,14 +427,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_sleep(&bars->p_full, g & 1, p.err, abort, 22, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
-        const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
-        tc_cp_32x128b_warpx4_elect(tSFV, dsf + fo + (1024 >> 4));
-        tc_cp_32x128b_warpx4_elect(tSFV + 4, dsf + fo + (1536 >> 4));
+        // K-step kb: P columns 8 kb (32 bytes of keys per lane), V rows
+        // kKeysPerStep * kb of every chunk
+        constexpr uint64_t kVStep = (C::kKeysPerStep * C::kChunkB) >> 4;
+        if constexpr (B16) {
 #pragma unroll
-        for (int kb = 0; kb < kBlockN / 32; ++kb)
-          mma_mxf8_ts_elect(tO, tP + 8 * kb, dv + so + kb * ((32 * D) >> 4),
-                            idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
-                            tSFV + 4 * (kb >> 2), (!first) || (kb > 0));
+          for (int kb = 0; kb < C::kKStepsPV; ++kb)
+            mma_bf16_ts_elect(tO, tP + 8 * kb, dv + so + kb * kVStep, idesc_o,
+                              (!first) || (kb > 0));
+        } else {
+          const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
+          tc_cp_32x128b_warpx4_elect(tSFV, dsf + fo + (1024 >> 4));
+          tc_cp_32x128b_warpx4_elect(tSFV + 4, dsf + fo + (1536 >> 4));
+#pragma unroll
+          for (int kb = 0; kb < C::kKStepsPV; ++kb)
+            mma_mxf8_ts_elect(tO, tP + 8 * kb, dv + so + kb * kVStep,
+                              idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
+                              tSFV + 4 * (kb >> 2), (!first) || (kb > 0));
+        }
         tc_commit_elect(&bars->pv_done);
         return true;
       };
@@ -390,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx < 0) break;
         WorkItem w;
         if (!work_item(p, idx, w)) continue;
-        const int ntiles = item_tiles(p, w);
+        const int ntiles = item_tiles<kBlockN>(p, w);
         for (int j = 0; j < ntiles && ok; ++j, ++gt) ok = issue_pv(gt, j == 0);
       }
     }
@@ -419,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       WorkItem w;
       if (!work_item(p, idx, w)) continue;
       const int q0 = w.qtile * kBlockM;
-      const int ntiles = item_tiles(p, w);
+      const int ntiles = item_tiles<kBlockN>(p, w);
       const int qi = q0 + row;                    // query index in sequence
       float m_ref = -INFINITY;                    // log2 units
       float l = 0.f;                              // this half's partial sum
@@ -428,9 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait_sleep(&bars->s_full, gt & 1, p.err, abort, 30, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sv[4][32];
+        constexpr int kCh = C::kChunks;
+        uint32_t sv[kCh][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tSrow + 32 * c, sv[c]);
+        for (int c = 0; c < kCh; ++c) tmem_ld32(tSrow + 32 * c, sv[c]);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -439,15 +503,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool need_mask = (k0 + kHalfN > w.len) || (p.causal && k0 + kHalfN - 1 > q0);
         if (need_mask) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+          for (int c = 0; c < kCh; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (k0 + 32 * c + e >= lim) sv[c][e] = __float_as_uint(-INFINITY);
         }
         // chunk maxima of the raw logits (c2 > 0 keeps the order)
-        float cmax[4];
+        float cmax[kCh];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kCh; ++c) {
           float a = __uint_as_float(sv[c][0]);
 #pragma unroll
           for (int e = 1; e < 31; e += 2)
@@ -455,7 +519,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           cmax[c] = fmaxf(a, __uint_as_float(sv[c][31]));
         }
         // row maximum over both halves
-        const float hmax = fmaxf(fmaxf(cmax[0], cmax[1]), fmaxf(cmax[2], cmax[3]));
+        float hmax = cmax[0];
+#pragma unroll
+        for (int c = 1; c < kCh; ++c) hmax = fmaxf(hmax, cmax[c]);
         float* xm = xmax + (gx & 1) * 256;
         xm[wg * 128 + row] = hmax;
         __syncwarp();
@@ -470,39 +536,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool moved = (m_new != m_ref);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
-        // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
-        uint32_t code[4];
-        uint32_t sfp = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
-          code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
-          sfp |= code[c] << (8 * c);
-        }
-        // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
-        // the scaled values per block and rescales by 2^e
         uint32_t pw[32];
         float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int e = static_cast<int>(code[c]) - 127;
-          const float nb = -(m_use + static_cast<float>(e));
-          const uint64_t nb2 = pack2(nb, nb);
+        uint32_t sfp = 0;
+        if constexpr (B16) {
+          // P = 2^(s*c2 - m) rounded to bf16 for the PV MMA; l sums the fp32
+          // values
+          const uint64_t nb2 = pack2(-m_use, -m_use);
           uint64_t acc = 0;
 #pragma unroll
-          for (int kk = 0; kk < 16; kk += 2) {
-            const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][2 * kk]), __uint_as_float(sv[c][2 * kk + 1])), c2x2, nb2);
-            const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][2 * kk + 2]), __uint_as_float(sv[c][2 * kk + 3])), c2x2, nb2);
-            const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
-            const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
-            acc = add2(acc, pack2(p0, p1));
-            acc = add2(acc, pack2(p2, p3));
-            pw[8 * c + kk / 2] = cvt_e4m3x4(p0, p1, p2, p3);
+          for (int c = 0; c < kCh; ++c) {
+#pragma unroll
+            for (int kk = 0; kk < 32; kk += 4) {
+              const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][kk]), __uint_as_float(sv[c][kk + 1])), c2x2, nb2);
+              const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][kk + 2]), __uint_as_float(sv[c][kk + 3])), c2x2, nb2);
+              const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
+              const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
+              acc = add2(acc, pack2(p0, p1));
+              acc = add2(acc, pack2(p2, p3));
+              const __nv_bfloat162 b0 = __floats2bfloat162_rn(p0, p1);
+              const __nv_bfloat162 b1 = __floats2bfloat162_rn(p2, p3);
+              pw[16 * c + kk / 2] = *reinterpret_cast<const uint32_t*>(&b0);
+              pw[16 * c + kk / 2 + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+            }
           }
-          // 2^e as fp32 (e in [-127, 119]; 2^-127 flushes to 0, harmless: such
-          // blocks hold only zeros)
-          const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
-          lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
+          lsum = lo2(acc) + hi2(acc);
+        } else {
+          // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
+          uint32_t code[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
+            code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
+            sfp |= code[c] << (8 * c);
+          }
+          // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
+          // the scaled values per block and rescales by 2^e
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int e = static_cast<int>(code[c]) - 127;
+            const float nb = -(m_use + static_cast<float>(e));
+            const uint64_t nb2 = pack2(nb, nb);
+            uint64_t acc = 0;
+#pragma unroll
+            for (int kk = 0; kk < 16; kk += 2) {
+              const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][2 * kk]), __uint_as_float(sv[c][2 * kk + 1])), c2x2, nb2);
+              const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][2 * kk + 2]), __uint_as_float(sv[c][2 * kk + 3])), c2x2, nb2);
+              const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
+              const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
+              acc = add2(acc, pack2(p0, p1));
+              acc = add2(acc, pack2(p2, p3));
+              pw[8 * c + kk / 2] = cvt_e4m3x4(p0, p1, p2, p3);
+            }
+            // 2^e as fp32 (e in [-127, 119]; 2^-127 flushes to 0, harmless: such
+            // blocks hold only zeros)
+            const float two_e = e > -127 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : 0.f;
+            lsum = fmaf(lo2(acc) + hi2(acc), two_e, lsum);
+          }
         }
         // the previous P must be consumed before this P overwrites it (and O
         // is stable only between two PVs); an item's first tile follows the
@@ -515,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
         }
         tmem_st32(tmem + kColP + 32 * wg + lane_base, pw);
-        tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
+        if constexpr (!B16) tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
         // selective rescale of O (and l): only warps holding a moved row; each
         // half rescales half of the columns
         if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
@@ -591,28 +681,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool B16>
 lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
                        const void* q8, const void* sfq, const void* k8,
                        const void* sfk, const void* v8, const void* sfv,
                        void* o, float* lse, uint32_t* err, uint64_t wait_ns,
                        int32_t withhold_kv, cudaStream_t cs) {
+  using C = FwdCfg<D, B16>;
   const CUtensorMapSwizzle sw =
-      D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+      C::kChunkB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk, tv;
+  // [tokens][heads][D] elements; a box is one chunk (<= 128 bytes) of `rows`
+  // token rows of one head
   auto make = [&](CUtensorMap* m, const void* base, int64_t heads, uint32_t rows) {
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(heads),
                         static_cast<uint64_t>(sv.total_tokens)};
-    uint64_t strides[2] = {static_cast<uint64_t>(D),
-                           static_cast<uint64_t>(heads * D)};
-    uint32_t box[3] = {static_cast<uint32_t>(D), 1u, rows};
-    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides,
-                       box, sw);
+    uint64_t strides[2] = {static_cast<uint64_t>(C::kRowB),
+                           static_cast<uint64_t>(heads * C::kRowB)};
+    uint32_t box[3] = {static_cast<uint32_t>(C::kChunkB / C::kEl), 1u, rows};
+    return encode_tmap(m, B16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                       3, base, dims, strides, box, sw);
   };
   lpfa_status st;
   if ((st = make(&tq, q8, desc->heads_q, kBlockM)) != LPFA_OK) return st;
-  if ((st = make(&tk, k8, desc->heads_kv, kBlockN)) != LPFA_OK) return st;
-  if ((st = make(&tv, v8, desc->heads_kv, kBlockN)) != LPFA_OK) return st;
+  if ((st = make(&tk, k8, desc->heads_kv, C::kN)) != LPFA_OK) return st;
+  if ((st = make(&tv, v8, desc->heads_kv, C::kN)) != LPFA_OK) return st;
 
   FwdParams p;
   p.seqs = sv;
@@ -640,11 +733,11 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   p.nitems = nitems;
   const int nsm = num_sms();
   const int64_t nblocks = nitems < nsm ? nitems : nsm;   // one CTA per SM
-  const size_t smem = FwdCfg<D>::kTotal + 1024;
-  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D>),
+  const size_t smem = C::kTotal + 1024;
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D, B16>),
                                  static_cast<int>(smem))) != LPFA_OK)
     return st;
-  mx_attn_fwd_kernel<D><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, p);
+  mx_attn_fwd_kernel<D, B16><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
 }
@@ -678,11 +771,12 @@ lpfa_status fwd_impl(const lpfa_attn_desc* desc, const void* q8, const void* sfq
                      const void* k8, const void* sfk_mma, const void* v8,
                      const void* sfv_mma, void* o, float* lse, void* workspace,
                      size_t workspace_bytes, uint64_t wait_ns, int32_t withhold_kv,
-                     void* stream) {
+                     bool bf16, void* stream) {
   SeqView sv;
   lpfa_status st = validate_attn(desc, &sv);
   if (st != LPFA_OK) return st;
-  LPFA_CHECK_ARG(q8 && sfq_mma && k8 && sfk_mma && v8 && sfv_mma && o && lse);
+  LPFA_CHECK_ARG(q8 && k8 && v8 && o && lse);
+  LPFA_CHECK_ARG(bf16 || (sfq_mma && sfk_mma && sfv_mma));
   LPFA_CHECK_ARG(aligned16(q8) && aligned16(k8) && aligned16(v8) &&
                  aligned16(sfq_mma) && aligned16(sfk_mma) && aligned16(sfv_mma) &&
                  aligned16(o));
@@ -692,11 +786,18 @@ lpfa_status fwd_impl(const lpfa_attn_desc* desc, const void* q8, const void* sfq
   if (sv.total_tokens == 0) return LPFA_OK;
   LPFA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 256, cs));
   uint32_t* err = static_cast<uint32_t*>(workspace);
+  if (bf16) {
+    if (desc->head_dim == 128)
+      return launch_fwd<128, true>(desc, sv, q8, nullptr, k8, nullptr, v8, nullptr, o, lse,
+                                   err, wait_ns, withhold_kv, cs);
+    return launch_fwd<64, true>(desc, sv, q8, nullptr, k8, nullptr, v8, nullptr, o, lse, err,
+                                wait_ns, withhold_kv, cs);
+  }
   if (desc->head_dim == 128)
-    return launch_fwd<128>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
-                           wait_ns, withhold_kv, cs);
-  return launch_fwd<64>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
-                        wait_ns, withhold_kv, cs);
+    return launch_fwd<128, false>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse,
+                                  err, wait_ns, withhold_kv, cs);
+  return launch_fwd<64, false>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
+                               wait_ns, withhold_kv, cs);
 }
 
 }  // namespace
@@ -708,7 +809,7 @@ extern "C" lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
                                 void* workspace, size_t workspace_bytes,
                                 void* stream) {
   return fwd_impl(desc, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, workspace,
-                  workspace_bytes, kWaitLimitNs, -1, stream);
+                  workspace_bytes, kWaitLimitNs, -1, false, stream);
 }
 
 extern "C" lpfa_status lpfa_fwd_wait_expiry_selftest(
@@ -718,5 +819,13 @@ extern "C" lpfa_status lpfa_fwd_wait_expiry_selftest(
   LPFA_CHECK_ARG(wait_limit_us >= 1 && wait_limit_us <= 2000000u);
   return fwd_impl(desc, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, workspace,
                   workspace_bytes, static_cast<uint64_t>(wait_limit_us) * 1000ull, 0,
-                  stream);
+                  false, stream);
+}
+
+extern "C" lpfa_status lpfa_fwd_bf16(const lpfa_attn_desc* desc, const void* q,
+                                     const void* k, const void* v, void* o, float* lse,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* stream) {
+  return fwd_impl(desc, q, nullptr, k, nullptr, v, nullptr, o, lse, workspace,
+                  workspace_bytes, kWaitLimitNs, -1, true, stream);
 }

@@ -72,6 +72,7 @@ _mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                 _i64, _i64, _i64, _vp)
 _mx_gemm_q = _sig("lpfa_mx_gemm_quantize", ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                   ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
+_mma_peak = _sig("lpfa_mma_peak", ctypes.c_int, ctypes.POINTER(ctypes.c_double), _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
                ctypes.POINTER(lpfa_attn_desc))
 _bwd_ws = _sig("lpfa_bwd_workspace_size", ctypes.c_size_t,
@@ -81,6 +82,10 @@ _fwd = _sig("lpfa_fwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
 _bwd = _sig("lpfa_bwd", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
             _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
+_fwd_bf16 = _sig("lpfa_fwd_bf16", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
+                 _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
+_bwd_bf16 = _sig("lpfa_bwd_bf16", ctypes.c_int, ctypes.POINTER(lpfa_attn_desc),
+                 _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp)
 _fwd_expiry = _sig("lpfa_fwd_wait_expiry_selftest", ctypes.c_int,
                    ctypes.POINTER(lpfa_attn_desc), _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                    _vp, _vp, ctypes.c_size_t, ctypes.c_uint32, _vp)
@@ -97,7 +102,8 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_mx_gemm", "lpfa_mx_gemm_quantize",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc",
-            "lpfa_fwd_wait_expiry_selftest")
+            "lpfa_fwd_wait_expiry_selftest", "lpfa_mma_peak", "lpfa_fwd_bf16",
+            "lpfa_bwd_bf16")
 
 
 class LpfaError(RuntimeError):
@@ -352,11 +358,29 @@ def lpfa_bwd(desc, q8, sfq, sfq_t, k8, sfk, sfk_t, v8, sfv, do8, sfdo,
              _stream(stream)), "lpfa_bwd")
 
 
+def lpfa_fwd_bf16(desc, q, k, v, o, lse, ws, stream=None):
+    _ok(_fwd_bf16(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                  _ptr(ws), ws.numel(), _stream(stream)), "lpfa_fwd_bf16")
+
+
+def lpfa_bwd_bf16(desc, q, k, v, o, dout, lse, dq, dk, dv, ws, stream=None):
+    _ok(_bwd_bf16(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                  _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(),
+                  _stream(stream)), "lpfa_bwd_bf16")
+
+
 def lpfa_fwd_wait_expiry_selftest(desc, q8, sfq, k8, sfk, v8, sfv, o, lse, ws,
                                   wait_limit_us, stream=None):
     _ok(_fwd_expiry(ctypes.byref(desc), _ptr(q8), _ptr(sfq), _ptr(k8), _ptr(sfk),
                     _ptr(v8), _ptr(sfv), _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
                     wait_limit_us, _stream(stream)), "lpfa_fwd_wait_expiry_selftest")
+
+
+def lpfa_mma_peak(stream=None) -> float:
+    """Block-scaled MXFP8 MMA rate of the tensor pipe (FLOP/s); synchronises."""
+    v = ctypes.c_double(0.0)
+    _ok(_mma_peak(ctypes.byref(v), _stream(stream)), "lpfa_mma_peak")
+    return v.value
 
 
 def lpfa_check(ws: torch.Tensor, stream=None):
@@ -421,6 +445,78 @@ def mx_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
     if check:
         lpfa_check(ws)
     return o.reshape(shape), lse
+
+
+def attention_forward_bf16(q, k, v, desc: lpfa_attn_desc, out=None, lse=None, ws=None,
+                           stream=None):
+    """lpfa_fwd_bf16 on bf16 [T, H, D] operands.  Returns (o, lse, ws)."""
+    T, Hq, D = q.shape
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(fwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    lpfa_fwd_bf16(desc, q, k, v, out, lse, ws, stream)
+    return out, lse, ws
+
+
+def bf16_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
+                           cu_seqlens: Optional[torch.Tensor] = None,
+                           rescale_threshold: float = 8.0, check: bool = True):
+    """The bf16 variant of mx_attention_forward (same kernel with kind::f16
+    MMAs on bf16 operands, P rounded to bf16).  Returns (o, lse)."""
+    shape = q.shape
+    qt, B, S = _as_tokens(q)
+    kt, _, _ = _as_tokens(k)
+    vt, _, _ = _as_tokens(v)
+    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    T, Hq, D = qt.shape
+    desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
+                     rescale_threshold)
+    o, lse, ws = attention_forward_bf16(qt, kt, vt, desc)
+    if check:
+        lpfa_check(ws)
+    return o.reshape(shape), lse
+
+
+def attention_backward_bf16(q, k, v, o, dout, lse, desc: lpfa_attn_desc, dq=None, dk=None,
+                            dv=None, ws=None, stream=None):
+    """lpfa_bwd_bf16 on bf16 [T, H, D] operands.  Returns (dq fp16, dk, dv, ws)."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    dev = q.device
+    if dq is None:
+        dq = torch.empty((T, Hq, D), dtype=torch.float16, device=dev)
+    if dk is None:
+        dk = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    if dv is None:
+        dv = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    if ws is None:
+        ws = torch.empty(bwd_workspace_size(desc), dtype=torch.uint8, device=dev)
+    lpfa_bwd_bf16(desc, q, k, v, o, dout, lse, dq, dk, dv, ws, stream)
+    return dq, dk, dv, ws
+
+
+def bf16_attention_backward(q, k, v, o, do, lse, *, causal: bool, softmax_scale=None,
+                            cu_seqlens: Optional[torch.Tensor] = None,
+                            dq_static_scale: float = 1.0, check: bool = True):
+    """The bf16 variant of mx_attention_backward (head_dim 128).  Returns
+    (dq fp16, dk, dv) shaped like q, k, v."""
+    qt, B, S = _as_tokens(q)
+    kt, _, _ = _as_tokens(k)
+    vt, _, _ = _as_tokens(v)
+    ot, _, _ = _as_tokens(o)
+    dot, _, _ = _as_tokens(do)
+    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    T, Hq, D = qt.shape
+    desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
+                     dq_static_scale=dq_static_scale)
+    dq, dk, dv, ws = attention_backward_bf16(qt, kt, vt, ot, dot, lse, desc)
+    if check:
+        lpfa_check(ws)
+    return dq.reshape(q.shape), dk.reshape(k.shape), dv.reshape(v.shape)
 
 
 def quantize_backward_operands(q, k, v, do, seqs: Seqs, stream=None):
