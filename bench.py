@@ -292,6 +292,38 @@ def run_lpfa(args, world, rank, local):
     qb = statistics.mean(p[2].elapsed_time(p[3]) for p in parts)
     bw = statistics.mean(p[3].elapsed_time(p[4]) for p in parts)
 
+    # ---- the bf16 variants of the same kernels on the same inputs, for the
+    # MXFP8 / bf16 ratio (kernel against kernel; the MXFP8 side also with its
+    # operand quantization)
+    bf16 = {}
+    try:
+        ob, lb, fwsb = torch.empty_like(o), torch.empty_like(lse), torch.empty_like(fws)
+        dqb, dkb, dvb = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+        bwsb = torch.empty_like(bws)
+        fwd_b = lambda: L.attention_forward_bf16(q, k, v, desc, ob, lb, fwsb)
+        bwd_b = lambda: L.attention_backward_bf16(q, k, v, ob, do, lb, desc, dqb, dkb, dvb, bwsb)
+        for _ in range(2):
+            fwd_b(); bwd_b()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, args.steps)):
+            e = [ev() for _ in range(3)]
+            e[0].record(); fwd_b(); e[1].record(); bwd_b(); e[2].record()
+            ts.append(e)
+        torch.cuda.synchronize()
+        L.lpfa_check(fwsb)
+        L.lpfa_check(bwsb)
+        fb = statistics.mean(t[0].elapsed_time(t[1]) for t in ts)
+        bb = statistics.mean(t[1].elapsed_time(t[2]) for t in ts)
+        bf16 = {"fwd_tflops": fwd_flops / fb / 1e9, "bwd_tflops": bwd_flops / bb / 1e9,
+                "fwd_ms": fb, "bwd_ms": bb,
+                "mxfp8_over_bf16": {"fwd": fb / fw, "bwd": bb / bw,
+                                    "fwd_incl_quantize": fb / (fw + qf),
+                                    "bwd_incl_quantize": bb / (bw + qb)}}
+        del ob, lb, fwsb, dqb, dkb, dvb, bwsb
+    except Exception as exc:
+        bf16 = {"error": repr(exc)[:200]}
+
     # ---- the fused RMSNorm + MX quantizer on the model's hidden state: Q
     # viewed as [T, H * D] (hidden 4096, 512 MiB, larger than L2), square
     # blocks with compact and both tensor-core scale layouts and rstd; beside
@@ -557,6 +589,7 @@ def run_lpfa(args, world, rank, local):
         "fwd": {"tflops": fwd_tflops, "ms": fw, "frac_of_peak": fwd_tflops / peak},
         "bwd": {"tflops": bwd_tflops, "ms": bw, "frac_of_peak": bwd_tflops / peak},
         "quantize_ms": {"fwd_operands": qf, "bwd_operands": qb},
+        "bf16": bf16,
         "roofline": {"bound": "tensor",
                      "kernel": "mx_attn_bwd_kernel (lpfa_bwd call: D_i preprocess + main kernel)",
                      "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",

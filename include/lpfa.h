@@ -232,6 +232,37 @@ lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
                          int64_t K, void* stream);
 
 /* ------------------------------------------------------------------------
+ * The same GEMM on operands of other MX element formats ([P1] paragraph 2:
+ * the block-scaled MMA takes MXFP8, MXFP6 and MXFP4 operands): the
+ * kind::mxf8f6f4 MMA with the A and B element types a_fmt, b_fmt (any pair
+ * of lpfa_elem), 1x32 UE8M0 scales along K in the layout of lpfa_mx_gemm.
+ * a, b: [M, K] / [N, K] bytes in the tensor core's operand layout (see
+ * lpfa_mx_pack_operand): for E4M3 and E5M2 one code per byte; for FP6 and
+ * FP4 every 16 consecutive elements of a row take 16 bytes, their codes
+ * packed at the front.
+ * Constraints and errors as lpfa_mx_gemm; a format outside the enum ->
+ * LPFA_ERR_INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mx_gemm_fmt(const void* a, const void* sfa_mma, const void* b,
+                             const void* sfb_mma, float* d, int64_t M, int64_t N,
+                             int64_t K, lpfa_elem a_fmt, lpfa_elem b_fmt, void* stream);
+
+/* Operand bytes for lpfa_mx_gemm_fmt from one-code-per-byte payloads (the
+ * output of lpfa_mx_quantize_fmt).  codes, out: [rows, cols] bytes, cols a
+ * multiple of 16, 16-byte aligned.  Each group of 16 consecutive codes of a
+ * row becomes 16 bytes:
+ *   E4M3, E5M2  unchanged (a copy unless codes == out);
+ *   E3M2, E2M3  a little-endian 96-bit stream, code e at bits 6e..6e+5, in
+ *               bytes 0..11; bytes 12..15 zero;
+ *   E2M1        code e in bits 4(e%2).. of byte e/2 (bytes 0..7); bytes 8..15
+ *               zero.
+ * (The layout kind::mxf8f6f4 MMAs read for 6- and 4-bit operands.)
+ * Errors: NULL / misaligned pointers, cols % 16 != 0, a format outside the
+ * enum -> LPFA_ERR_INVALID_ARG. */
+lpfa_status lpfa_mx_pack_operand(const void* codes, int64_t rows, int64_t cols,
+                                 lpfa_elem fmt, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * Tensor-pipe rate of block-scaled MXFP8 MMAs, for the roofline of the
  * attention kernels ([P1] paragraph 2: tcgen05.mma.block_scale).  One CTA
  * per SM issues M128 N256 K32 kind::mxf8f6f4 block-scaled MMAs (E4M3

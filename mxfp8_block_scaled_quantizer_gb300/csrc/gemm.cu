@@ -53,6 +53,7 @@ struct GemmArgs {
   uint8_t* qsf_mma_t;   // 32x32: [N/128][M/128][512], or null
   int32_t M, N, K;
   int32_t tiles_m, tiles_n, kt;
+  uint32_t idesc;       // instruction descriptor (element types of A and B)
   uint32_t* err;
 };
 
@@ -158,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_mxf8(kBM, kBN, 0, 0);
+      const uint32_t idesc = g.idesc;
       int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
@@ -297,10 +298,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 using namespace lpfa;
 
 namespace {
+// tcgen05 type code of an element format (kind::mxf8f6f4)
+uint32_t mma_type_code(lpfa_elem f) {
+  switch (f) {
+    case LPFA_ELEM_E4M3: return 0;
+    case LPFA_ELEM_E5M2: return 1;
+    case LPFA_ELEM_E2M3: return 3;
+    case LPFA_ELEM_E3M2: return 4;
+    case LPFA_ELEM_E2M1: return 5;
+  }
+  return 0;
+}
+
 lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                         const void* sfb_mma, float* d, int64_t M, int64_t N, int64_t K,
                         int quant, uint8_t* q, uint8_t* qsf, uint8_t* qsf_mma,
-                        uint8_t* qsf_mma_t, void* stream) {
+                        uint8_t* qsf_mma_t, void* stream,
+                        lpfa_elem a_fmt = LPFA_ELEM_E4M3, lpfa_elem b_fmt = LPFA_ELEM_E4M3) {
   LPFA_CHECK_ARG(a8 && sfa_mma && b8 && sfb_mma);
   LPFA_CHECK_ARG(aligned16(a8) && aligned16(b8) && aligned16(sfa_mma) &&
                  aligned16(sfb_mma) && aligned16(d));
@@ -341,6 +355,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   g.tiles_n = static_cast<int32_t>(N / kBN);
   g.kt = static_cast<int32_t>(K / kBK);
   g.err = nullptr;
+  g.idesc = idesc_mx_types(kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt));
 
   const size_t smem = kStages * kStageBytes + sizeof(GemmSmem) + 1024;
   const int ntiles = g.tiles_m * g.tiles_n;
@@ -366,6 +381,73 @@ extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
   LPFA_CHECK_ARG(d != nullptr);
   return launch_gemm(a8, sfa_mma, b8, sfb_mma, d, M, N, K, -1, nullptr, nullptr, nullptr,
                      nullptr, stream);
+}
+
+namespace lpfa {
+namespace {
+// One thread per 16-element group: one-per-byte codes -> the tensor core's
+// operand bytes (FP6: a little-endian 96-bit stream of 6-bit codes, then 4
+// zero bytes; FP4: 8 bytes of nibbles, element 2i low, then 8 zero bytes).
+template <int kBits>
+__global__ void pack_operand_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+                                    int64_t groups) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= groups) return;
+  const uint4 v = in[i];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint64_t lo = 0, hi = 0;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const uint64_t c = (w[e >> 2] >> (8 * (e & 3))) & ((1u << kBits) - 1u);
+    const int pos = kBits * e;
+    if (pos < 64) {
+      lo |= c << pos;
+      if (pos + kBits > 64) hi |= c >> (64 - pos);
+    } else {
+      hi |= c << (pos - 64);
+    }
+  }
+  out[i] = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                      static_cast<uint32_t>(hi), 0u);
+}
+}  // namespace
+}  // namespace lpfa
+
+extern "C" lpfa_status lpfa_mx_pack_operand(const void* codes, int64_t rows, int64_t cols,
+                                            lpfa_elem fmt, void* out, void* stream) {
+  LPFA_CHECK_ARG(codes != nullptr && out != nullptr && aligned16(codes) && aligned16(out));
+  LPFA_CHECK_ARG(rows >= 0 && cols >= 0 && cols % 16 == 0);
+  LPFA_CHECK_ARG(fmt >= LPFA_ELEM_E4M3 && fmt <= LPFA_ELEM_E2M1);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const int64_t groups = rows * (cols / 16);
+  if (groups == 0) return LPFA_OK;
+  if (fmt == LPFA_ELEM_E4M3 || fmt == LPFA_ELEM_E5M2) {
+    if (codes != out)
+      LPFA_CHECK_CUDA(cudaMemcpyAsync(out, codes, static_cast<size_t>(rows * cols),
+                                      cudaMemcpyDeviceToDevice, cs));
+    return LPFA_OK;
+  }
+  LPFA_CHECK_ARG(ceil_div(groups, 256) < (1ll << 31));
+  const unsigned blocks = static_cast<unsigned>(ceil_div(groups, 256));
+  if (fmt == LPFA_ELEM_E2M1)
+    pack_operand_kernel<4><<<blocks, 256, 0, cs>>>(static_cast<const uint4*>(codes),
+                                                   static_cast<uint4*>(out), groups);
+  else
+    pack_operand_kernel<6><<<blocks, 256, 0, cs>>>(static_cast<const uint4*>(codes),
+                                                   static_cast<uint4*>(out), groups);
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}
+
+extern "C" lpfa_status lpfa_mx_gemm_fmt(const void* a, const void* sfa_mma, const void* b,
+                                        const void* sfb_mma, float* d, int64_t M, int64_t N,
+                                        int64_t K, lpfa_elem a_fmt, lpfa_elem b_fmt,
+                                        void* stream) {
+  LPFA_CHECK_ARG(d != nullptr);
+  LPFA_CHECK_ARG(a_fmt >= LPFA_ELEM_E4M3 && a_fmt <= LPFA_ELEM_E2M1);
+  LPFA_CHECK_ARG(b_fmt >= LPFA_ELEM_E4M3 && b_fmt <= LPFA_ELEM_E2M1);
+  return launch_gemm(a, sfa_mma, b, sfb_mma, d, M, N, K, -1, nullptr, nullptr, nullptr,
+                     nullptr, stream, a_fmt, b_fmt);
 }
 
 extern "C" lpfa_status lpfa_mx_gemm_quantize(const void* a8, const void* sfa_mma,

@@ -399,6 +399,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N,
          ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::mxf8f6f4 with A / B element types given by
+// their type codes (E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5) and UE8M0 scales.
+__host__ __device__ constexpr uint32_t idesc_mx_types(uint32_t M, uint32_t N, uint32_t atype,
+                                                     uint32_t btype) {
+  return (atype << 7) | (btype << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
 // Set the scale-factor byte selectors (which byte of each 32-bit TMEM scale
 // column feeds this MMA).
 __device__ __forceinline__ uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id,

@@ -72,6 +72,10 @@ _mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                 _i64, _i64, _i64, _vp)
 _mx_gemm_q = _sig("lpfa_mx_gemm_quantize", ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                   ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
+_mx_gemm_fmt = _sig("lpfa_mx_gemm_fmt", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                    _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp)
+_pack_operand = _sig("lpfa_mx_pack_operand", ctypes.c_int, _vp, _i64, _i64, ctypes.c_int,
+                     _vp, _vp)
 _mma_peak = _sig("lpfa_mma_peak", ctypes.c_int, ctypes.POINTER(ctypes.c_double), _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
                ctypes.POINTER(lpfa_attn_desc))
@@ -103,7 +107,7 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc",
             "lpfa_fwd_wait_expiry_selftest", "lpfa_mma_peak", "lpfa_fwd_bf16",
-            "lpfa_bwd_bf16")
+            "lpfa_bwd_bf16", "lpfa_mx_gemm_fmt", "lpfa_mx_pack_operand")
 
 
 class LpfaError(RuntimeError):
@@ -294,6 +298,25 @@ def lpfa_mx_gemm(a8, sfa_mma, b8, sfb_mma, d, stream=None):
                  M, N, K, _stream(stream)), "lpfa_mx_gemm")
 
 
+def lpfa_mx_gemm_fmt(a, sfa_mma, b, sfb_mma, d, a_fmt, b_fmt, stream=None):
+    """D = A B^T with A, B in the element formats a_fmt, b_fmt (LPFA_ELEM_*),
+    operand bytes in the tensor core's layout ([M, K] / [N, K] bytes)."""
+    M, K = a.shape
+    N = b.shape[0]
+    _ok(_mx_gemm_fmt(_ptr(a), _ptr(sfa_mma), _ptr(b), _ptr(sfb_mma), _ptr(d),
+                     M, N, K, int(a_fmt), int(b_fmt), _stream(stream)), "lpfa_mx_gemm_fmt")
+
+
+def mx_pack_operand(codes: torch.Tensor, fmt: int, out=None, stream=None) -> torch.Tensor:
+    """One-code-per-byte [rows, cols] payload -> lpfa_mx_gemm_fmt operand bytes."""
+    rows, cols = codes.shape
+    if out is None:
+        out = torch.empty_like(codes)
+    _ok(_pack_operand(_ptr(codes), rows, cols, int(fmt), _ptr(out), _stream(stream)),
+        "lpfa_mx_pack_operand")
+    return out
+
+
 def lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf=None, sf_mma=None,
                           sf_mma_t=None, d=None, stream=None):
     """Raw call: D = A B^T quantized in the epilogue; outputs preallocated."""
@@ -393,6 +416,16 @@ def check_status(ws: torch.Tensor, stream=None) -> int:
 
 
 # ------------------------------------------------------- convenience layer
+def _seqs_for(qt: torch.Tensor, B, S, cu_seqlens) -> "Seqs":
+    """BSHD -> B dense sequences; packed [T, H, D] -> the cu_seqlens
+    sequences, or one sequence of T tokens without them."""
+    if cu_seqlens is not None:
+        return varlen_seqs(cu_seqlens)
+    if B is None:
+        return dense_seqs(1, qt.shape[0])
+    return dense_seqs(B, S)
+
+
 def _as_tokens(x: torch.Tensor):
     """[B, S, H, D] -> ([B*S, H, D], B, S); [T, H, D] -> (x, None, None)."""
     if x.dim() == 4:
@@ -436,7 +469,7 @@ def mx_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
     qt, B, S = _as_tokens(q)
     kt, _, _ = _as_tokens(k)
     vt, _, _ = _as_tokens(v)
-    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    seqs = _seqs_for(qt, B, S, cu_seqlens)
     T, Hq, D = qt.shape
     desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
                      rescale_threshold)
@@ -471,7 +504,7 @@ def bf16_attention_forward(q, k, v, *, causal: bool, softmax_scale=None,
     qt, B, S = _as_tokens(q)
     kt, _, _ = _as_tokens(k)
     vt, _, _ = _as_tokens(v)
-    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    seqs = _seqs_for(qt, B, S, cu_seqlens)
     T, Hq, D = qt.shape
     desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
                      rescale_threshold)
@@ -509,7 +542,7 @@ def bf16_attention_backward(q, k, v, o, do, lse, *, causal: bool, softmax_scale=
     vt, _, _ = _as_tokens(v)
     ot, _, _ = _as_tokens(o)
     dot, _, _ = _as_tokens(do)
-    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    seqs = _seqs_for(qt, B, S, cu_seqlens)
     T, Hq, D = qt.shape
     desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
                      dq_static_scale=dq_static_scale)
@@ -565,7 +598,7 @@ def mx_attention_backward(q, k, v, o, dout, lse, *, causal: bool,
     vt, _, _ = _as_tokens(v)
     ot, _, _ = _as_tokens(o)
     dot, _, _ = _as_tokens(dout)
-    seqs = dense_seqs(B, S) if cu_seqlens is None else varlen_seqs(cu_seqlens)
+    seqs = _seqs_for(qt, B, S, cu_seqlens)
     T, Hq, D = qt.shape
     desc = attn_desc(seqs, Hq, kt.shape[1], D, causal, softmax_scale,
                      dq_static_scale=dq_static_scale)

@@ -162,3 +162,29 @@ def gemm_quantize(d, block):
     return {"payload": p, "sf": sc,
             "sf_mma": gemm_operand_mma(np.repeat(sc, 32, axis=0)),
             "sf_mma_t": gemm_operand_mma(np.repeat(sc.T, 32, axis=0))}
+
+
+# ------------------------------------------------------ MMA operand bytes
+def mma_operand_bytes(codes, fmt):
+    """The byte layout block-scaled MMAs read for an operand of element
+    format ``fmt``: codes [R, C] (one code per byte, C a multiple of 16) ->
+    bytes [R, C].  E4M3 / E5M2: unchanged.  FP6 (e3m2, e2m3) and FP4 (e2m1):
+    every 16 consecutive codes of a row form one 16-byte group holding their
+    bits as a little-endian stream (code j at bits b*j .. b*j + b - 1 of the
+    group, b = 6 or 4) followed by zero bytes."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    if fmt in ("e4m3", "e5m2"):
+        return codes.copy()
+    bits = {"e3m2": 6, "e2m3": 6, "e2m1": 4}[fmt]
+    R, C = codes.shape
+    assert C % 16 == 0
+    out = np.zeros((R, C), dtype=np.uint8)
+    mask = (1 << bits) - 1
+    for g in range(C // 16):
+        stream = np.zeros(R, dtype=object)
+        for j in range(16):
+            stream = stream + ((codes[:, 16 * g + j].astype(object) & mask) << (bits * j))
+        for byte in range(bits * 2):           # 16 codes * bits / 8
+            out[:, 16 * g + byte] = np.array([(int(v) >> (8 * byte)) & 0xFF for v in stream],
+                                             dtype=np.uint8)
+    return out

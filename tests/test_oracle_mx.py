@@ -353,3 +353,25 @@ def test_mx_gemm_mixed_formats_exact(a_fmt, b_fmt):
                 vb = Fraction(tb[pb[j, k]]) * Fraction(2) ** (int(sb[j, k // 32]) - 127)
                 acc += va * vb
             assert abs(Fraction(got[i, j]) - acc) <= abs(acc) * Fraction(1, 2 ** 50)
+
+
+def test_mma_operand_bytes_hand_worked():
+    """Packed FP4 / FP6 operand groups worked by hand from the bit-stream
+    rule (code j at bits b*j.., little-endian, zero padding to 16 bytes)."""
+    from oracle import layouts
+    c4 = (np.arange(32) % 16).astype(np.uint8).reshape(1, 32)
+    want4 = [0x10, 0x32, 0x54, 0x76, 0x98, 0xBA, 0xDC, 0xFE] + [0] * 8
+    assert layouts.mma_operand_bytes(c4, "e2m1")[0, :16].tolist() == want4
+    assert layouts.mma_operand_bytes(c4, "e2m1")[0, 16:].tolist() == want4
+    # FP6: code 0x3F in slot 0 -> byte 0 = 0x3F; in slot 1 -> bits 6..11:
+    # byte 0 = 0xC0, byte 1 = 0x0F; in slot 15 -> bits 90..95: byte 11 = 0xFC
+    for slot, want in ((0, {0: 0x3F}), (1, {0: 0xC0, 1: 0x0F}), (15, {11: 0xFC})):
+        c6 = np.zeros((1, 16), dtype=np.uint8)
+        c6[0, slot] = 0x3F
+        got = layouts.mma_operand_bytes(c6, "e3m2")[0]
+        assert {i: int(v) for i, v in enumerate(got) if v} == want, slot
+    # the sign bit of a code stays inside its own field
+    c6 = np.zeros((1, 16), dtype=np.uint8)
+    c6[0, 2] = 0x20                       # FP6 sign alone, slot 2 -> bit 17
+    assert layouts.mma_operand_bytes(c6, "e2m3")[0, 2] == 0x02
+    assert np.array_equal(layouts.mma_operand_bytes(c4, "e5m2"), c4)
