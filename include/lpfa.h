@@ -263,6 +263,44 @@ lpfa_status lpfa_mx_pack_operand(const void* codes, int64_t rows, int64_t cols,
                                  lpfa_elem fmt, void* out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * FP4 operands at the dense FP4 MMA rate ([P1] paragraph 2: MXFP4 and NVFP4
+ * among the block-scaled MMA formats): D[M, N] (fp32) = A[M, K] * B[N, K]^T
+ * with kind::mxf4nvf4 MMAs (K = 64 per instruction).
+ *  a, b: dense E2M1 [M, K/2] / [N, K/2] bytes, element 2i in the low nibble
+ *        of byte i (lpfa_fp4_pack_dense, or lpfa_nvfp4_quantize's output).
+ *  nvfp4 = 0 (MXFP4): 32-element UE8M0 blocks; sfa_mma / sfb_mma in the
+ *        layout of lpfa_mx_gemm ([R/128][K/128][512], four blocks per row
+ *        per tile), e.g. lpfa_mx_quantize_fmt(LPFA_ELEM_E2M1) out_sf_mma.
+ *  nvfp4 = 1 (NVFP4): 16-element UE4M3 blocks; [R/128][K/64][512], row r and
+ *        block kb of a tile at byte (r%32)*16 + (r/32)*4 + kb
+ *        (lpfa_nvfp4_quantize out_sf_mma).
+ * M, N multiples of 128 (N of 256), K a multiple of 256 (else
+ * LPFA_ERR_UNSUPPORTED); other errors as lpfa_mx_gemm.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mx_gemm_fp4(const void* a, const void* sfa_mma, const void* b,
+                             const void* sfb_mma, float* d, int64_t M, int64_t N,
+                             int64_t K, int nvfp4, void* stream);
+
+/* One-code-per-byte E2M1 [rows, cols] (cols % 16 == 0, 16-byte aligned) ->
+ * dense [rows, cols/2] bytes (8-byte aligned), code 2i in the low nibble of
+ * byte i: the operand layout of lpfa_mx_gemm_fp4. */
+lpfa_status lpfa_fp4_pack_dense(const void* codes, int64_t rows, int64_t cols,
+                                void* out, void* stream);
+
+/* NVFP4 quantization ([P1] paragraph 2 names the format; reading): x bf16
+ * [rows, cols] row-major (16-byte aligned, cols % 16 == 0); every 16
+ * consecutive elements of a row form a block with
+ *   s = E4M3(amax / 6)   (fp32 division; round to nearest even, saturating)
+ *   element = E2M1(x / s) (fp32 division; nearest even, saturating at 6),
+ * an all-zero block (or one whose scale rounds to 0) gets scale code 0 and
+ * zero elements; no per-tensor second-level scale.  Outputs: out dense E2M1
+ * [rows, cols/2] (8-byte aligned); out_sf E4M3 codes [rows, cols/16] or
+ * NULL; out_sf_mma [rows/128][cols/64][512] (rows % 128 == 0, cols % 64 ==
+ * 0) in the layout lpfa_mx_gemm_fp4 reads, or NULL.  Inputs are finite. */
+lpfa_status lpfa_nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* out,
+                                void* out_sf, void* out_sf_mma, void* stream);
+
+/* ------------------------------------------------------------------------
  * Tensor-pipe rate of block-scaled MXFP8 MMAs, for the roofline of the
  * attention kernels ([P1] paragraph 2: tcgen05.mma.block_scale).  One CTA
  * per SM issues M128 N256 K32 kind::mxf8f6f4 block-scaled MMAs (E4M3

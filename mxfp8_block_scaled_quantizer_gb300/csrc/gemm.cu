@@ -36,12 +36,31 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK;  // 16 KB
 constexpr int kBBytes = kBN * kBK;  // 32 KB
 constexpr int kSfBytes = 512;
-constexpr int kStageTx = kABytes + kBBytes + 3 * kSfBytes;   // bytes landed
-constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;   // 1024-aligned
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 256;        // TMEM scale buffers after the accumulator
-constexpr int kSfColsPerStage = 12; // 4 (A) + 8 (B, two 128-row tiles)
+
+// MMA kind of the main loop.  A stage holds 128 bytes of K per operand row:
+//   kKindF8F6F4  kind::mxf8f6f4 (1 byte per element slot), 4 MMAs of K = 32,
+//                one 512-byte scale tile per 128 rows (four 32-element E8M0
+//                blocks per row), scale byte sf_id = K-step;
+//   kKindMxf4    kind::mxf4nvf4 scale_vec::2X: dense FP4 (two per byte), 4
+//                MMAs of K = 64, two scale tiles per 128 rows (each four
+//                32-element E8M0 blocks: two MMAs, scale bytes 0-1 / 2-3);
+//   kKindNvf4    kind::mxf4nvf4 scale_vec::4X: dense FP4, 4 MMAs of K = 64,
+//                four scale tiles per 128 rows (each the four 16-element E4M3
+//                scales of one MMA).
+enum : int { kKindF8F6F4 = 0, kKindMxf4 = 1, kKindNvf4 = 2 };
+
+template <int kKind>
+struct GemmCfg {
+  static constexpr int kSfA = kKind == kKindNvf4 ? 4 : kKind == kKindMxf4 ? 2 : 1;  // tiles per 128 rows
+  static constexpr int kSfTiles = 3 * kSfA;                                           // A + two B row tiles
+  static constexpr int kStageTx = kABytes + kBBytes + kSfTiles * kSfBytes;            // bytes landed
+  static constexpr int kStageBytes = (kStageTx + 1023) / 1024 * 1024;                 // 1024-aligned
+  static constexpr int kSfColsPerStage = 4 * kSfTiles;
+  static_assert(kSfCol0 + kStages * kSfColsPerStage <= 512, "TMEM columns");
+};
 
 struct GemmArgs {
   const uint8_t* sfa;
@@ -80,11 +99,16 @@ __device__ __forceinline__ void quant32(const uint32_t (&r)[32], uint32_t code, 
   }
 }
 
-template <int kQuant>   // -1: fp32 only; 0: 1x32 along N; 2: 32x32
+template <int kQuant, int kKind>   // kQuant -1: fp32 only; 0: 1x32 along N; 2: 32x32
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                    const __grid_constant__ CUtensorMap tma_b,
                    const GemmArgs g) {
+  using C = GemmCfg<kKind>;
+  constexpr int kStageTx = C::kStageTx;
+  constexpr int kStageBytes = C::kStageBytes;
+  constexpr int kSfColsPerStage = C::kSfColsPerStage;
+  constexpr int kSfA = C::kSfA;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // stage buffers start 1024-aligned (128-byte swizzle atoms)
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
@@ -136,15 +160,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar, kStageTx);
           tma_load_2d(buf, &tma_a, kt * kBK, tm * kBM, bar);
           tma_load_2d(buf + kABytes, &tma_b, kt * kBK, tn * kBN, bar);
+          // scale tiles: A's kSfA, then each B row tile's kSfA; a row tile's
+          // tiles are consecutive along K in global memory
           uint8_t* sfbuf = buf + kABytes + kBBytes;
-          bulk_load(sfbuf, g.sfa + (static_cast<int64_t>(tm) * g.kt + kt) * kSfBytes,
-                    kSfBytes, bar);
-          bulk_load(sfbuf + kSfBytes,
-                    g.sfb + (static_cast<int64_t>(2 * tn) * g.kt + kt) * kSfBytes,
-                    kSfBytes, bar);
-          bulk_load(sfbuf + 2 * kSfBytes,
-                    g.sfb + (static_cast<int64_t>(2 * tn + 1) * g.kt + kt) * kSfBytes,
-                    kSfBytes, bar);
+          const int64_t ktiles = static_cast<int64_t>(g.kt) * kSfA;
+#pragma unroll
+          for (int t = 0; t < kSfA; ++t) {
+            bulk_load(sfbuf + t * kSfBytes,
+                      g.sfa + (tm * ktiles + kt * kSfA + t) * kSfBytes, kSfBytes, bar);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              bulk_load(sfbuf + (kSfA * (1 + h) + t) * kSfBytes,
+                        g.sfb + ((2 * tn + h) * ktiles + kt * kSfA + t) * kSfBytes, kSfBytes,
+                        bar);
+          }
           issued[stage] = static_cast<int>(phase);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
@@ -178,17 +207,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = smem_u32(buf);
           const uint32_t b_addr = smem_u32(buf + kABytes);
           const uint32_t sf_addr = smem_u32(buf + kABytes + kBBytes);
+          // TMEM: A scale tile t at sfa_t + 4t; B tile t at sfb_t + 8t
+          // (rows 0-127) and + 4 (rows 128-255)
           const uint32_t sfa_t = tmem + kSfCol0 + stage * kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + 4;
-          tc_cp_32x128b_warpx4(sfa_t, sf_tile_desc(sf_addr));
-          tc_cp_32x128b_warpx4(sfb_t, sf_tile_desc(sf_addr + kSfBytes));
-          tc_cp_32x128b_warpx4(sfb_t + 4, sf_tile_desc(sf_addr + 2 * kSfBytes));
+          const uint32_t sfb_t = sfa_t + 4 * kSfA;
+#pragma unroll
+          for (int t = 0; t < kSfA; ++t) {
+            tc_cp_32x128b_warpx4(sfa_t + 4 * t, sf_tile_desc(sf_addr + t * kSfBytes));
+            tc_cp_32x128b_warpx4(sfb_t + 8 * t, sf_tile_desc(sf_addr + (kSfA + t) * kSfBytes));
+            tc_cp_32x128b_warpx4(sfb_t + 8 * t + 4,
+                                 sf_tile_desc(sf_addr + (2 * kSfA + t) * kSfBytes));
+          }
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb) {
             const uint64_t ad = make_sdesc(a_addr + kb * 32, 16, 1024, 2);
             const uint64_t bd = make_sdesc(b_addr + kb * 32, 16, 1024, 2);
-            mma_mxf8_ss(tmem, ad, bd, idesc_sf_ids(idesc, kb, kb), sfa_t, sfb_t,
-                        (kt | kb) != 0);
+            const uint32_t acc = (kt | kb) != 0;
+            if constexpr (kKind == kKindF8F6F4) {
+              mma_mxf8_ss(tmem, ad, bd, idesc_sf_ids(idesc, kb, kb), sfa_t, sfb_t, acc);
+            } else if constexpr (kKind == kKindMxf4) {
+              const uint32_t t = kb >> 1, id = 2 * (kb & 1);
+              mma_mxf4_ss(tmem, ad, bd, idesc_sf_ids(idesc, id, id), sfa_t + 4 * t,
+                          sfb_t + 8 * t, acc);
+            } else {
+              mma_nvf4_ss(tmem, ad, bd, idesc, sfa_t + 4 * kb, sfb_t + 8 * kb, acc);
+            }
           }
           tc_commit(&sh->empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -314,7 +357,8 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                         const void* sfb_mma, float* d, int64_t M, int64_t N, int64_t K,
                         int quant, uint8_t* q, uint8_t* qsf, uint8_t* qsf_mma,
                         uint8_t* qsf_mma_t, void* stream,
-                        lpfa_elem a_fmt = LPFA_ELEM_E4M3, lpfa_elem b_fmt = LPFA_ELEM_E4M3) {
+                        lpfa_elem a_fmt = LPFA_ELEM_E4M3, lpfa_elem b_fmt = LPFA_ELEM_E4M3,
+                        int kind = kKindF8F6F4) {
   LPFA_CHECK_ARG(a8 && sfa_mma && b8 && sfb_mma);
   LPFA_CHECK_ARG(aligned16(a8) && aligned16(b8) && aligned16(sfa_mma) &&
                  aligned16(sfb_mma) && aligned16(d));
@@ -355,9 +399,17 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   g.tiles_n = static_cast<int32_t>(N / kBN);
   g.kt = static_cast<int32_t>(K / kBK);
   g.err = nullptr;
-  g.idesc = idesc_mx_types(kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt));
+  // kind::mxf4nvf4: E2M1 is type 1; bit 23 selects UE8M0 (MXFP4) or UE4M3
+  // (NVFP4) scales
+  g.idesc = kind == kKindF8F6F4
+                ? idesc_mx_types(kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt))
+                : (idesc_mx_types(kBM, kBN, 1, 1) & ~(1u << 23)) |
+                      (kind == kKindMxf4 ? (1u << 23) : 0u);
 
-  const size_t smem = kStages * kStageBytes + sizeof(GemmSmem) + 1024;
+  const size_t smem = kStages * (kind == kKindNvf4   ? GemmCfg<kKindNvf4>::kStageBytes
+                                 : kind == kKindMxf4 ? GemmCfg<kKindMxf4>::kStageBytes
+                                                     : GemmCfg<kKindF8F6F4>::kStageBytes) +
+                      sizeof(GemmSmem) + 1024;
   const int ntiles = g.tiles_m * g.tiles_n;
   const int grid = ntiles < num_sms() ? ntiles : num_sms();
   auto go = [&](auto kernel) -> lpfa_status {
@@ -368,9 +420,11 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
     LPFA_CHECK_CUDA(cudaGetLastError());
     return LPFA_OK;
   };
-  if (quant < 0) return go(mx_gemm_kernel<-1>);
-  if (quant == 0) return go(mx_gemm_kernel<0>);
-  return go(mx_gemm_kernel<2>);
+  if (kind == kKindMxf4) return go(mx_gemm_kernel<-1, kKindMxf4>);
+  if (kind == kKindNvf4) return go(mx_gemm_kernel<-1, kKindNvf4>);
+  if (quant < 0) return go(mx_gemm_kernel<-1, kKindF8F6F4>);
+  if (quant == 0) return go(mx_gemm_kernel<0, kKindF8F6F4>);
+  return go(mx_gemm_kernel<2, kKindF8F6F4>);
 }
 }  // namespace
 
@@ -410,8 +464,48 @@ __global__ void pack_operand_kernel(const uint4* __restrict__ in, uint4* __restr
   out[i] = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
                       static_cast<uint32_t>(hi), 0u);
 }
+// One thread per 16 codes: one-per-byte E2M1 codes -> 8 bytes of nibbles
+// (element 2i in the low nibble), the dense operand of kind::mxf4nvf4.
+__global__ void pack_fp4_dense_kernel(const uint4* __restrict__ in, uint2* __restrict__ out,
+                                      int64_t groups) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= groups) return;
+  const uint4 v = in[i];
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e)
+    o[e >> 3] |= ((w[e >> 2] >> (8 * (e & 3))) & 0xFu) << (4 * (e & 7));
+  out[i] = make_uint2(o[0], o[1]);
+}
 }  // namespace
 }  // namespace lpfa
+
+extern "C" lpfa_status lpfa_fp4_pack_dense(const void* codes, int64_t rows, int64_t cols,
+                                           void* out, void* stream) {
+  LPFA_CHECK_ARG(codes != nullptr && out != nullptr && aligned16(codes));
+  LPFA_CHECK_ARG((reinterpret_cast<uintptr_t>(out) & 7u) == 0);
+  LPFA_CHECK_ARG(rows >= 0 && cols >= 0 && cols % 16 == 0);
+  const int64_t groups = rows * (cols / 16);
+  if (groups == 0) return LPFA_OK;
+  LPFA_CHECK_ARG(ceil_div(groups, 256) < (1ll << 31));
+  pack_fp4_dense_kernel<<<static_cast<unsigned>(ceil_div(groups, 256)), 256, 0,
+                          static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(codes), static_cast<uint2*>(out), groups);
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}
+
+extern "C" lpfa_status lpfa_mx_gemm_fp4(const void* a, const void* sfa_mma, const void* b,
+                                        const void* sfb_mma, float* d, int64_t M, int64_t N,
+                                        int64_t K, int nvfp4, void* stream) {
+  LPFA_CHECK_ARG(d != nullptr && (nvfp4 == 0 || nvfp4 == 1));
+  LPFA_CHECK_ARG(K > 0 && K % 2 == 0);
+  if (K % 256 != 0) return LPFA_ERR_UNSUPPORTED;
+  return launch_gemm(a, sfa_mma, b, sfb_mma, d, M, N, K / 2, -1, nullptr, nullptr, nullptr,
+                     nullptr, stream, LPFA_ELEM_E2M1, LPFA_ELEM_E2M1,
+                     nvfp4 ? kKindNvf4 : kKindMxf4);
+}
 
 extern "C" lpfa_status lpfa_mx_pack_operand(const void* codes, int64_t rows, int64_t cols,
                                             lpfa_elem fmt, void* out, void* stream) {

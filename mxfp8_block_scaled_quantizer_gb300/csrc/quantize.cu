@@ -611,3 +611,82 @@ extern "C" lpfa_status lpfa_rmsnorm_mx_quantize(const lpfa_seqs* seqs, const voi
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// NVFP4 quantizer (lpfa_nvfp4_quantize): 16-element blocks along a row, E2M1
+// elements, one E4M3 scale per block: s = E4M3(amax / 6), element =
+// E2M1(x / s), both round to nearest even with saturation, both divisions
+// single fp32 divisions.  One thread per block.
+// ---------------------------------------------------------------------------
+namespace lpfa {
+namespace {
+__global__ void nvfp4_quantize_kernel(const __nv_bfloat16* __restrict__ x, int64_t rows,
+                                      int64_t cols, uint8_t* __restrict__ out,
+                                      uint8_t* __restrict__ sf, uint8_t* __restrict__ sf_mma) {
+  const int64_t nb = cols / 16;
+  const int64_t blk = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (blk >= rows * nb) return;
+  const int64_t r = blk / nb, b = blk % nb;
+  const uint4* src = reinterpret_cast<const uint4*>(x + r * cols + b * 16);
+  const uint4 v[2] = {src[0], src[1]};
+  float f[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&v[h]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 t = __bfloat1622float2(p2[k]);
+      f[8 * h + 2 * k] = t.x;
+      f[8 * h + 2 * k + 1] = t.y;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  const uint32_t code = cvt_e4m3x2(__fdiv_rn(amax, 6.0f), 0.f) & 0xFFu;
+  // the scale's value: E4M3 -> f16 -> f32, exact (the code in both bytes, so
+  // both halves of the result hold it)
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(code | (code << 8))));
+  const float s = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+  uint32_t o[2] = {0u, 0u};
+  if (s > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+      uint16_t pr;
+      asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.u16.u8 %0, t;\n\t}"
+          : "=h"(pr)
+          : "f"(__fdiv_rn(f[i], s)), "f"(__fdiv_rn(f[i + 1], s)));
+      o[i >> 3] |= static_cast<uint32_t>(pr & 0xFFu) << (8 * ((i >> 1) & 3));
+    }
+  }
+  *reinterpret_cast<uint2*>(out + r * (cols / 2) + b * 8) = make_uint2(o[0], o[1]);
+  const uint8_t c = s > 0.f ? static_cast<uint8_t>(code) : 0u;
+  if (sf != nullptr) sf[r * nb + b] = c;
+  if (sf_mma != nullptr) {
+    const int64_t tile = (r / 128) * (nb / 4) + b / 4;
+    const int64_t rr = r % 128;
+    sf_mma[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + (b % 4)] = c;
+  }
+}
+}  // namespace
+}  // namespace lpfa
+
+extern "C" lpfa_status lpfa_nvfp4_quantize(const void* x, int64_t rows, int64_t cols,
+                                           void* out, void* out_sf, void* out_sf_mma,
+                                           void* stream) {
+  using namespace lpfa;
+  LPFA_CHECK_ARG(x != nullptr && out != nullptr && aligned16(x));
+  LPFA_CHECK_ARG((reinterpret_cast<uintptr_t>(out) & 7u) == 0);
+  LPFA_CHECK_ARG(rows >= 0 && cols >= 0 && cols % 16 == 0);
+  LPFA_CHECK_ARG(out_sf_mma == nullptr || (rows % 128 == 0 && cols % 64 == 0));
+  const int64_t n = rows * (cols / 16);
+  if (n == 0) return LPFA_OK;
+  LPFA_CHECK_ARG(ceil_div(n, 256) < (1ll << 31));
+  nvfp4_quantize_kernel<<<static_cast<unsigned>(ceil_div(n, 256)), 256, 0,
+                          static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const __nv_bfloat16*>(x), rows, cols, static_cast<uint8_t*>(out),
+      static_cast<uint8_t*>(out_sf), static_cast<uint8_t*>(out_sf_mma));
+  LPFA_CHECK_CUDA(cudaGetLastError());
+  return LPFA_OK;
+}

@@ -76,6 +76,10 @@ _mx_gemm_fmt = _sig("lpfa_mx_gemm_fmt", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                     _i64, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp)
 _pack_operand = _sig("lpfa_mx_pack_operand", ctypes.c_int, _vp, _i64, _i64, ctypes.c_int,
                      _vp, _vp)
+_gemm_fp4 = _sig("lpfa_mx_gemm_fp4", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                 ctypes.c_int, _vp)
+_pack_fp4 = _sig("lpfa_fp4_pack_dense", ctypes.c_int, _vp, _i64, _i64, _vp, _vp)
+_nvfp4_q = _sig("lpfa_nvfp4_quantize", ctypes.c_int, _vp, _i64, _i64, _vp, _vp, _vp, _vp)
 _mma_peak = _sig("lpfa_mma_peak", ctypes.c_int, ctypes.POINTER(ctypes.c_double), _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
                ctypes.POINTER(lpfa_attn_desc))
@@ -107,7 +111,8 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_fwd_workspace_size", "lpfa_bwd_workspace_size", "lpfa_fwd",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc",
             "lpfa_fwd_wait_expiry_selftest", "lpfa_mma_peak", "lpfa_fwd_bf16",
-            "lpfa_bwd_bf16", "lpfa_mx_gemm_fmt", "lpfa_mx_pack_operand")
+            "lpfa_bwd_bf16", "lpfa_mx_gemm_fmt", "lpfa_mx_pack_operand",
+            "lpfa_mx_gemm_fp4", "lpfa_fp4_pack_dense", "lpfa_nvfp4_quantize")
 
 
 class LpfaError(RuntimeError):
@@ -315,6 +320,38 @@ def mx_pack_operand(codes: torch.Tensor, fmt: int, out=None, stream=None) -> tor
     _ok(_pack_operand(_ptr(codes), rows, cols, int(fmt), _ptr(out), _stream(stream)),
         "lpfa_mx_pack_operand")
     return out
+
+
+def lpfa_mx_gemm_fp4(a, sfa_mma, b, sfb_mma, d, nvfp4: bool, stream=None):
+    """D = A B^T on dense FP4 operands a [M, K/2], b [N, K/2] (kind::mxf4nvf4);
+    MXFP4 (32-element E8M0 scales) or NVFP4 (16-element E4M3 scales)."""
+    M, K2 = a.shape
+    N = b.shape[0]
+    _ok(_gemm_fp4(_ptr(a), _ptr(sfa_mma), _ptr(b), _ptr(sfb_mma), _ptr(d), M, N, 2 * K2,
+                  int(bool(nvfp4)), _stream(stream)), "lpfa_mx_gemm_fp4")
+
+
+def fp4_pack_dense(codes: torch.Tensor, stream=None) -> torch.Tensor:
+    """One E2M1 code per byte [rows, cols] -> dense [rows, cols/2]."""
+    rows, cols = codes.shape
+    out = torch.empty((rows, cols // 2), dtype=torch.uint8, device=codes.device)
+    _ok(_pack_fp4(_ptr(codes), rows, cols, _ptr(out), _stream(stream)), "lpfa_fp4_pack_dense")
+    return out
+
+
+def nvfp4_quantize(x: torch.Tensor, stream=None):
+    """bf16 [rows, cols] -> (dense E2M1 [rows, cols/2], E4M3 scales
+    [rows, cols/16], tensor-core scale tiles [rows/128, cols/64, 512] or None)."""
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    rows, cols = x.shape
+    out = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+    mma = None
+    if rows % 128 == 0 and cols % 64 == 0:
+        mma = torch.empty((rows // 128, cols // 64, 512), dtype=torch.uint8, device=x.device)
+    _ok(_nvfp4_q(_ptr(x), rows, cols, _ptr(out), _ptr(sf), _ptr(mma), _stream(stream)),
+        "lpfa_nvfp4_quantize")
+    return out, sf, mma
 
 
 def lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf=None, sf_mma=None,

@@ -188,3 +188,11 @@ def mma_operand_bytes(codes, fmt):
             out[:, 16 * g + byte] = np.array([(int(v) >> (8 * byte)) & 0xFF for v in stream],
                                              dtype=np.uint8)
     return out
+
+
+def fp4_dense_bytes(codes):
+    """Dense FP4 operand bytes: codes [R, C] (one E2M1 code per byte, C
+    even) -> [R, C/2], code 2i in the low nibble and code 2i + 1 in the high
+    nibble of byte i."""
+    c = np.asarray(codes, dtype=np.uint8) & 0xF
+    return (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)

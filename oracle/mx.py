@@ -293,3 +293,51 @@ def mx_gemm(a_payload, a_sc, b_payload, b_sc, a_fmt: str = "e4m3",
     product of two decoded operands is exact in fp64, so this is the dense
     GEMM of the dequantized operands."""
     return dq_1x32(a_payload, a_sc, a_fmt) @ dq_1x32(b_payload, b_sc, b_fmt).T
+
+
+# --------------------------------------------------------------- NVFP4
+# NVFP4 ("Low Precision Flash Attention 4 ...", paragraph 2, names it among
+# the formats the block-scaled MMA takes; the pages give no rule).  Reading:
+# blocks of 16 consecutive elements along the contraction, E2M1 elements
+# (largest magnitude 6), one positive E4M3 scale per block, no second-level
+# per-tensor scale.  In fp32, as the kernel computes it:
+#   s = E4M3(amax / 6)                 round to nearest even, saturating
+#   element = E2M1(x / s)              round to nearest even, saturating at 6
+# A block with amax = 0 (or a scale that rounds to 0) has scale code 0 and
+# zero payloads.  The divisions are single fp32 divisions, so their rounding
+# is part of the definition.
+NVFP4_BLOCK = 16
+
+
+def quantize_nvfp4(x) -> tuple:
+    """16-element blocks along the last axis.  Returns (E2M1 codes, one per
+    byte [..., n], E4M3 scale codes [..., n/16])."""
+    x32 = np.asarray(x, dtype=np.float32)
+    n = x32.shape[-1]
+    assert n % NVFP4_BLOCK == 0
+    xg = x32.reshape(*x32.shape[:-1], n // NVFP4_BLOCK, NVFP4_BLOCK)
+    amax = np.max(np.abs(xg), axis=-1)
+    s32 = (amax / np.float32(6.0)).astype(np.float32)     # one fp32 division
+    s_code = e4m3_encode(s32.astype(np.float64))
+    s = e4m3_decode(s_code).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0))
+    y = (xg / safe[..., None]).astype(np.float32)         # one fp32 division
+    codes = fmt_encode(y.astype(np.float64), "e2m1")
+    codes = np.where((s > 0)[..., None], codes, np.uint8(0)).astype(np.uint8)
+    s_code = np.where(s > 0, s_code, np.uint8(0)).astype(np.uint8)
+    return codes.reshape(x32.shape), s_code
+
+
+def dq_nvfp4(codes, s_code):
+    vals = fmt_table("e2m1")[np.asarray(codes, np.uint8)]
+    s = e4m3_decode(s_code)
+    return vals * np.repeat(s, NVFP4_BLOCK, axis=-1)
+
+
+def fp4_gemm(a_codes, a_sc, b_codes, b_sc, scale: str) -> np.ndarray:
+    """D = A @ B^T for E2M1 operands with 32-element E8M0 blocks
+    (scale='mx') or 16-element E4M3 blocks (scale='nv'); every product of two
+    decoded operands is exact in fp64."""
+    if scale == "mx":
+        return dq_1x32(a_codes, a_sc, "e2m1") @ dq_1x32(b_codes, b_sc, "e2m1").T
+    return dq_nvfp4(a_codes, a_sc) @ dq_nvfp4(b_codes, b_sc).T

@@ -375,3 +375,39 @@ def test_mma_operand_bytes_hand_worked():
     c6[0, 2] = 0x20                       # FP6 sign alone, slot 2 -> bit 17
     assert layouts.mma_operand_bytes(c6, "e2m3")[0, 2] == 0x02
     assert np.array_equal(layouts.mma_operand_bytes(c4, "e5m2"), c4)
+
+
+def test_nvfp4_hand_worked_block():
+    """One 16-element NVFP4 block by hand: amax = 3, s = E4M3(3/6 = 0.5) =
+    0.5 (exact), elements x / 0.5 rounded to E2M1 {0, .5, 1, 1.5, 2, 3, 4, 6}
+    with ties to the even code."""
+    x = np.array([3.0, -3.0, 0.5, 0.25, 0.125, 1.1, 0.8, 0.0,
+                  -0.375, 2.5, 1.75, 0.62, -1.0, 0.3, 0.9, 1.5])
+    codes, sc = mx.quantize_nvfp4(x)
+    assert sc.tolist() == [mx.e4m3_encode(0.5)]          # 0.5 = code 0x30
+    y = x / 0.5
+    # y: 6 -6 1 .5 .25 2.2 1.6 0 -.75 5 3.5 1.24 -2 .6 1.8 3
+    want = [6.0, -6.0, 1.0, 0.5, 0.0, 2.0, 1.5, 0.0, -1.0, 4.0, 4.0, 1.0, -2.0, 0.5, 2.0, 3.0]
+    got = mx.fmt_table("e2m1")[codes]
+    assert got.tolist() == want
+    # ties: 0.25 -> 0 (even code 0, not 0.5 = code 1); -0.75 -> -1 (code 2,
+    # even, not -0.5 code 1); 5 -> 4 (code 6, even, not 6 = code 7); 3.5 -> 4
+    assert np.array_equal(mx.dq_nvfp4(codes, sc), np.array(want) * 0.5)
+
+
+def test_nvfp4_scale_rounding_and_zero_block():
+    """amax = 6 * 0.3 = 1.8: s = E4M3(0.3) = 0.3125 (0.3 lies between 0.28125
+    and 0.3125, nearer the latter), so the largest element 1.8 / 0.3125 =
+    5.76 rounds to 6.  An all-zero block has scale code 0 and zero codes."""
+    x = np.zeros((2, 16))
+    x[0, 0] = 1.8
+    codes, sc = mx.quantize_nvfp4(x)
+    assert mx.e4m3_decode(sc[0]) == 0.3125
+    assert mx.fmt_table("e2m1")[codes[0, 0]] == 6.0
+    assert sc[1] == 0 and not codes[1].any()
+
+
+def test_fp4_dense_bytes_hand_worked():
+    from oracle import layouts
+    c = np.array([[1, 2, 0xF, 0, 7, 8]], dtype=np.uint8)
+    assert layouts.fp4_dense_bytes(c).tolist() == [[0x21, 0x0F, 0x87]]
