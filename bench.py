@@ -14,10 +14,14 @@ is the max over ranks and the value counts the work of all ranks (weak
 scaling).  --impl reference times the fp64 CPU oracle on a bounded sample of
 the same workload (rank 0 only).
 
-Beside the step the JSON line reports the fused RMSNorm + MX quantizer and the
-quantizing GEMM (rates in the same run), the end-to-end rate from pinned host
-memory, and the SM clocks sampled by nvidia-smi during the run (raw samples in
-$LPFA_CLOCK_LOG_DIR, default the system temp directory).
+Beside the step the JSON line reports, each measured in the same run: the
+bf16 variants of the forward and backward kernels on the same inputs (the
+MXFP8 / bf16 ratio), the fused RMSNorm + MX quantizer, the tensor pipe's
+block-scaled MMA rate, this library's and cuBLAS's MXFP8 GEMM 8192^3 (the
+fastest of the two is the roofline's peak), the quantizing GEMM, the jagged
+GEMM-Norm backward, the end-to-end rate from pinned host memory with the copy
+rates that bound it, and the SM clocks sampled by nvidia-smi during the run
+(raw samples in $LPFA_CLOCK_LOG_DIR, default the system temp directory).
 """
 from __future__ import annotations
 
@@ -538,6 +542,43 @@ def run_lpfa(args, world, rank, local):
     except Exception as exc:
         mma["error"] = repr(exc)[:160]
 
+    # ---- the jagged GEMM-Norm backward (16 jagged sequences, hidden 4096):
+    # the RMSNorm backward fused with the 32x32 quantization of dY (both
+    # orientations), then dX = dY W and dW = dY^T X on the block-scaled GEMM
+    # with X and W kept quantized from the forward.  The rate counts the two
+    # GEMMs' 4 T N K flops; the quantization of X and W is timed beside it.
+    gn = {}
+    try:
+        cfg = workloads.GEMM_NORM
+        lens = workloads.gemm_norm_lengths(cfg["batch"], cfg["len_min"], cfg["len_max"],
+                                           cfg["seed"] + rank)
+        Tn, Hn = int(lens.sum()), cfg["hidden"]
+        gi = workloads.gemm_norm_inputs(Tn, Hn, Hn, cfg["seed"] + rank)
+        xg, wg, gam, dzg = (gi[n].to(dev) for n in ("x", "w", "gamma", "dz"))
+        del gi
+        yg = xg @ wg.T                                   # the forward's bf16 Y
+        rs = torch.rsqrt(yg.float().pow(2).mean(dim=1) + 1e-6)
+        xq_, wq_ = L.mx_quantize_t(xg), L.mx_quantize_t(wg)
+        ms_gn, _ = _time(lambda: L.gemm_norm_backward(xq_, wq_, yg, rs, gam, dzg), 10)
+        ms_nq, _ = _time(lambda: L.rmsnorm_bwd_mx_quantize(yg, dzg, gam, rs), 10)
+        ms_xw, _ = _time(lambda: (L.mx_quantize_t(xg), L.mx_quantize_t(wg)), 10)
+        gflops = 4.0 * Tn * Hn * Hn
+        nq_bytes = 6.0 * Tn * Hn                         # read Y, dZ; payload twice
+        gn = {"workload": f"jagged: {cfg['batch']} sequences, lengths U[{cfg['len_min']}, "
+                          f"{cfg['len_max']}] (T = {Tn}), hidden N = K = {Hn}",
+              "ms": ms_gn, "tflops": gflops / ms_gn / 1e9,
+              "norm_bwd_quantize_ms": ms_nq,
+              "norm_bwd_quantize_gbs": nq_bytes / (ms_nq * 1e-3) / 1e9,
+              "gemms_ms": ms_gn - ms_nq,
+              "gemms_tflops": gflops / (ms_gn - ms_nq) / 1e9,
+              "quantize_x_w_ms": ms_xw,
+              "tflops_incl_quantize_x_w": gflops / (ms_gn + ms_xw) / 1e9,
+              "context_pages_tflops": 1760.0,
+              "context_note": "the pages' 1.76 PF/s is on other hardware and an unstated shape"}
+        del xg, wg, gam, dzg, yg, rs, xq_, wq_
+    except Exception as exc:
+        gn = {"error": repr(exc)[:200]}
+
     peaks = _peaks()
     # Roofline denominator: the fastest dense block-scaled MXFP8 GEMM measured
     # in this run (this library's or cuBLAS's, M = N = K = 8192).  Beside it:
@@ -603,6 +644,7 @@ def run_lpfa(args, world, rank, local):
                          "bwd_frac_of_bf16_burst_x2": bwd_tflops / bf16_burst_x2 if bf16_burst_x2 else None,
                          "datasheet_tflops": 4500.0}},
         "mma_rate_in_run": mma,
+        "gemm_norm_bwd": gn,
         "rmsnorm_quantize": {
             "workload": f"x [{T}, {H * D}] bf16 (the llm Q tensor as hidden states), 32x32 blocks, "
                         "compact + both tensor-core scale layouts + rstd",

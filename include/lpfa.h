@@ -8,7 +8,8 @@
  * lpfa_check, the jagged scale-row offsets (lpfa_varlen_sf_rows), the fused
  * producers of quantized operands (lpfa_rmsnorm_mx_quantize,
  * lpfa_mx_gemm_quantize), the block-scaled GEMM (lpfa_mx_gemm), the
- * tensor-pipe rate microbench (lpfa_mma_peak), the forward's bounded-wait
+ * tensor-pipe rate microbench (lpfa_mma_peak), the FP6 / FP4 / NVFP4 GEMMs and
+ * quantizers, the jagged GEMM-Norm backward pieces, the forward's bounded-wait
  * self-test and the status / version / device queries.
  *
  * Sources of the operations (page title, section):
@@ -224,8 +225,9 @@ lpfa_status lpfa_rmsnorm_mx_quantize(const lpfa_seqs* seqs, const void* x,
  * A, B: e4m3, K contiguous (row-major [M, K] / [N, K]); sfa_mma, sfb_mma:
  * tensor-core scale layout of their 1x32 (along K) scales,
  * [M/128][K/128][512] and [N/128][K/128][512] bytes (tile (i, kt) holds rows
- * 128i.. and contraction blocks 4kt..4kt+3).  M, N multiples of 128, K a
- * multiple of 128.  Persistent kernel, one CTA per SM.
+ * 128i.. and contraction blocks 4kt..4kt+3).  N a multiple of 256, K of 128;
+ * M any positive value (rows past M read as zeros and are not stored; the A
+ * scales then hold ceil(M/128) row tiles).  Persistent kernel, one CTA per SM.
  * ---------------------------------------------------------------------- */
 lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
                          const void* sfb_mma, float* d, int64_t M, int64_t N,
@@ -299,6 +301,45 @@ lpfa_status lpfa_fp4_pack_dense(const void* codes, int64_t rows, int64_t cols,
  * 0) in the layout lpfa_mx_gemm_fp4 reads, or NULL.  Inputs are finite. */
 lpfa_status lpfa_nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void* out,
                                 void* out_sf, void* out_sf_mma, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Jagged GEMM-Norm backward ([P1] paragraph 4 reports it for throughput
+ * only; [P1] paragraph 2: fused RMSNorm + Quantize with dual scale layouts).
+ * Reading: over the T tokens of a jagged batch (rows of X [T, K], sequences
+ * concatenated), Y = X W^T (W [N, K]), Z = Y r gamma with
+ * r_t = rsqrt(mean_n Y_tn^2 + eps); from dZ [T, N]
+ *   c_t = (1/N) sum_n gamma_n dZ_tn Y_tn,  dY = r (gamma dZ - Y r^2 c),
+ *   dgamma_n = sum_t dZ_tn Y_tn r_t,  dX = dY W,  dW = dY^T X,
+ * with dY, X, W quantized in square 32x32 blocks so that one payload serves
+ * the GEMM over N (dX) and the GEMM over T (dW).  The two GEMMs are
+ * lpfa_mx_gemm calls on the outputs below (dX: A = dY [T, N] with sf_mma,
+ * B = W's transposed payload [K, N] with W's sf_mma_t; dW: A = dY's
+ * transposed payload [N, Tp] with sf_mma_t, B = X's transposed payload
+ * [K, Tp] with X's sf_mma_t).
+ *
+ * lpfa_mx_quantize_t: 32x32 MX quantization of x bf16 [rows, cols]
+ * (row-major, 16-byte aligned; cols a multiple of 128) with the payload in
+ * both orientations.  rows_p = rows rounded up to 128; rows past `rows` are
+ * zeros.  Outputs (device, caller-allocated, 16-byte aligned):
+ *   out       E4M3 [rows, cols]           out_t  E4M3 [cols, rows_p]
+ *   out_sf    compact codes [rows_p/32, cols/32] or NULL
+ *   out_sf_mma    rows = rows, blocks along cols: [rows_p/128][cols/128][512]
+ *   out_sf_mma_t  rows = cols, blocks along rows: [cols/128][rows_p/128][512]
+ *   (either may be NULL; layout of lpfa_mx_gemm's operand scales).
+ * lpfa_rmsnorm_bwd_mx_quantize: the same outputs for dY computed from y (the
+ * forward's bf16 Y [rows, cols]), dz (bf16 [rows, cols]), gamma (bf16
+ * [cols]) and rstd (fp32 [rows]) in fp32, plus dgamma (fp32 [cols]) summed in
+ * a fixed order from dgamma_part (fp32 scratch [rows_p/32, cols]).
+ * Errors: NULL or misaligned pointers, cols % 128 != 0 -> INVALID_ARG.
+ * ---------------------------------------------------------------------- */
+lpfa_status lpfa_mx_quantize_t(const void* x, int64_t rows, int64_t cols, void* out,
+                               void* out_t, void* out_sf, void* out_sf_mma,
+                               void* out_sf_mma_t, void* stream);
+lpfa_status lpfa_rmsnorm_bwd_mx_quantize(const void* y, const void* dz, const void* gamma,
+                                         const float* rstd, int64_t rows, int64_t cols,
+                                         void* out, void* out_t, void* out_sf,
+                                         void* out_sf_mma, void* out_sf_mma_t,
+                                         float* dgamma_part, float* dgamma, void* stream);
 
 /* ------------------------------------------------------------------------
  * Tensor-pipe rate of block-scaled MXFP8 MMAs, for the roofline of the

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->acc_empty);
         }
-        if (kQuant < 0 || g.d != nullptr) {
+        if ((kQuant < 0 || g.d != nullptr) && row < g.M) {
           float4* dst = reinterpret_cast<float4*>(drow + c * 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
@@ -363,7 +363,9 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   LPFA_CHECK_ARG(aligned16(a8) && aligned16(b8) && aligned16(sfa_mma) &&
                  aligned16(sfb_mma) && aligned16(d));
   LPFA_CHECK_ARG(M > 0 && N > 0 && K > 0);
-  if (M % kBM != 0 || N % kBN != 0 || K % kBK != 0) return LPFA_ERR_UNSUPPORTED;
+  // a ragged M (rows past it load as zeros and are not stored) only with the
+  // fp32 output
+  if ((quant >= 0 && M % kBM != 0) || N % kBN != 0 || K % kBK != 0) return LPFA_ERR_UNSUPPORTED;
   LPFA_CHECK_ARG(M < (1 << 20) && N < (1 << 20) && K < (1 << 20));
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
@@ -395,7 +397,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   g.M = static_cast<int32_t>(M);
   g.N = static_cast<int32_t>(N);
   g.K = static_cast<int32_t>(K);
-  g.tiles_m = static_cast<int32_t>(M / kBM);
+  g.tiles_m = static_cast<int32_t>(ceil_div(M, kBM));
   g.tiles_n = static_cast<int32_t>(N / kBN);
   g.kt = static_cast<int32_t>(K / kBK);
   g.err = nullptr;

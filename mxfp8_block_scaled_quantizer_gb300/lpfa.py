@@ -80,6 +80,9 @@ _gemm_fp4 = _sig("lpfa_mx_gemm_fp4", ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _i64
                  ctypes.c_int, _vp)
 _pack_fp4 = _sig("lpfa_fp4_pack_dense", ctypes.c_int, _vp, _i64, _i64, _vp, _vp)
 _nvfp4_q = _sig("lpfa_nvfp4_quantize", ctypes.c_int, _vp, _i64, _i64, _vp, _vp, _vp, _vp)
+_quant_t = _sig("lpfa_mx_quantize_t", ctypes.c_int, _vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _vp)
+_norm_bwd_q = _sig("lpfa_rmsnorm_bwd_mx_quantize", ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64,
+                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _mma_peak = _sig("lpfa_mma_peak", ctypes.c_int, ctypes.POINTER(ctypes.c_double), _vp)
 _fwd_ws = _sig("lpfa_fwd_workspace_size", ctypes.c_size_t,
                ctypes.POINTER(lpfa_attn_desc))
@@ -112,7 +115,8 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_bwd", "lpfa_check", "lpfa_bwd_noalloc",
             "lpfa_fwd_wait_expiry_selftest", "lpfa_mma_peak", "lpfa_fwd_bf16",
             "lpfa_bwd_bf16", "lpfa_mx_gemm_fmt", "lpfa_mx_pack_operand",
-            "lpfa_mx_gemm_fp4", "lpfa_fp4_pack_dense", "lpfa_nvfp4_quantize")
+            "lpfa_mx_gemm_fp4", "lpfa_fp4_pack_dense", "lpfa_nvfp4_quantize",
+            "lpfa_mx_quantize_t", "lpfa_rmsnorm_bwd_mx_quantize")
 
 
 class LpfaError(RuntimeError):
@@ -352,6 +356,64 @@ def nvfp4_quantize(x: torch.Tensor, stream=None):
     _ok(_nvfp4_q(_ptr(x), rows, cols, _ptr(out), _ptr(sf), _ptr(mma), _stream(stream)),
         "lpfa_nvfp4_quantize")
     return out, sf, mma
+
+
+@dataclass
+class MXT:
+    """32x32 quantization with the payload in both orientations."""
+    data: torch.Tensor      # [rows, cols]
+    data_t: torch.Tensor    # [cols, rows_p]
+    sf: torch.Tensor        # [rows_p/32, cols/32]
+    sf_mma: torch.Tensor    # rows = rows: [rows_p/128, cols/128, 512]
+    sf_mma_t: torch.Tensor  # rows = cols: [cols/128, rows_p/128, 512]
+
+
+def _mxt_empty(rows, cols, dev) -> MXT:
+    rp = -(-rows // 128) * 128
+    u8 = dict(dtype=torch.uint8, device=dev)
+    return MXT(torch.empty((rows, cols), **u8), torch.empty((cols, rp), **u8),
+               torch.empty((rp // 32, cols // 32), **u8),
+               torch.empty((rp // 128, cols // 128, 512), **u8),
+               torch.empty((cols // 128, rp // 128, 512), **u8))
+
+
+def mx_quantize_t(x: torch.Tensor, stream=None) -> MXT:
+    """32x32 MX quantization of bf16 [rows, cols], payload in both orientations."""
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.is_contiguous()
+    rows, cols = x.shape
+    m = _mxt_empty(rows, cols, x.device)
+    _ok(_quant_t(_ptr(x), rows, cols, _ptr(m.data), _ptr(m.data_t), _ptr(m.sf), _ptr(m.sf_mma),
+                 _ptr(m.sf_mma_t), _stream(stream)), "lpfa_mx_quantize_t")
+    return m
+
+
+def rmsnorm_bwd_mx_quantize(y, dz, gamma, rstd, stream=None):
+    """dY of Z = RMSNorm(Y) gamma, 32x32-quantized in both orientations, and
+    dgamma (fp32)."""
+    rows, cols = y.shape
+    m = _mxt_empty(rows, cols, y.device)
+    rp = m.data_t.shape[1]
+    part = torch.empty((rp // 32, cols), dtype=torch.float32, device=y.device)
+    dgamma = torch.empty(cols, dtype=torch.float32, device=y.device)
+    _ok(_norm_bwd_q(_ptr(y), _ptr(dz), _ptr(gamma), _ptr(rstd), rows, cols, _ptr(m.data),
+                    _ptr(m.data_t), _ptr(m.sf), _ptr(m.sf_mma), _ptr(m.sf_mma_t), _ptr(part),
+                    _ptr(dgamma), _stream(stream)), "lpfa_rmsnorm_bwd_mx_quantize")
+    return m, dgamma
+
+
+def gemm_norm_backward(xq: MXT, wq: MXT, y, rstd, gamma, dz, stream=None):
+    """The jagged GEMM-Norm backward on MXFP8: xq = mx_quantize_t(X [T, K]),
+    wq = mx_quantize_t(W [N, K]) (both may be kept from the forward), y the
+    forward's bf16 Y [T, N], rstd fp32 [T], gamma bf16 [N], dz bf16 [T, N].
+    Returns (dX fp32 [T, K], dW fp32 [N, K], dgamma fp32 [N])."""
+    T, N = y.shape
+    K = xq.data.shape[1]
+    dyq, dgamma = rmsnorm_bwd_mx_quantize(y, dz, gamma, rstd, stream)
+    dx = torch.empty((T, K), dtype=torch.float32, device=y.device)
+    dw = torch.empty((N, K), dtype=torch.float32, device=y.device)
+    lpfa_mx_gemm(dyq.data, dyq.sf_mma, wq.data_t, wq.sf_mma_t, dx, stream)
+    lpfa_mx_gemm(dyq.data_t, dyq.sf_mma_t, xq.data_t, xq.sf_mma_t, dw, stream)
+    return dx, dw, dgamma
 
 
 def lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf=None, sf_mma=None,

@@ -16,5 +16,7 @@ Modules:
              scale-factor layout description, for checking the quantizer's
              second scale output.
   norm       RMSNorm followed by MX quantization (the fused producer).
+  gemm_norm  the jagged GEMM-Norm backward (exact and at the MXFP8
+             quantization points).
 """
-from . import mx, attention, norm  # noqa: F401
+from . import mx, attention, norm, gemm_norm  # noqa: F401

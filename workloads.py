@@ -145,3 +145,28 @@ def attn_flops(w: Workload, lengths: Optional[torch.Tensor] = None) -> tuple:
     fwd = 4.0 * w.heads_q * sq2 * w.head_dim * f
     bwd = 10.0 * w.heads_q * sq2 * w.head_dim * f
     return fwd, bwd
+
+
+# --------------------------------------------------------------- GEMM-Norm
+# The jagged GEMM-Norm backward's inputs: a jagged batch of token rows (the
+# sequences concatenated, lengths uniform in [len_min, len_max]) through a
+# hidden x hidden projection.  The pages give no shape for it; these stand in.
+GEMM_NORM = {"batch": 16, "len_min": 128, "len_max": 8192, "hidden": 4096, "seed": 5}
+
+
+def gemm_norm_lengths(batch: int, len_min: int, len_max: int, seed: int) -> torch.Tensor:
+    gen = torch.Generator("cpu").manual_seed(seed)
+    return torch.randint(len_min, len_max + 1, (batch,), generator=gen)
+
+
+def gemm_norm_inputs(T: int, N: int, K: int, seed: int) -> dict:
+    """X [T, K] ~ N(0, 1), W [N, K] ~ N(0, 1/K), gamma [N] ~ 1 + 0.1 N(0, 1),
+    dZ [T, N] ~ N(0, 1), drawn in that order from one seeded CPU generator and
+    cast to bf16."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    x = torch.randn(T, K, generator=gen)
+    w = torch.randn(N, K, generator=gen) / math.sqrt(K)
+    gamma = 1.0 + 0.1 * torch.randn(N, generator=gen)
+    dz = torch.randn(T, N, generator=gen)
+    return {"x": x.to(torch.bfloat16), "w": w.to(torch.bfloat16),
+            "gamma": gamma.to(torch.bfloat16), "dz": dz.to(torch.bfloat16)}
