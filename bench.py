@@ -707,6 +707,29 @@ def run_profile_case(iters: int):
     return 0
 
 
+def run_profile_case_gemm_norm(iters: int):
+    """One small pass of the jagged GEMM-Norm backward for ncu captures: 4
+    jagged sequences (lengths U[128, 8192], seed 5), hidden 4096 (X, Y, dZ
+    larger than L2 together), ``iters`` times, no timing."""
+    from mxfp8_block_scaled_quantizer_gb300 import build
+    build()
+    from mxfp8_block_scaled_quantizer_gb300 import lpfa as L
+    lens = workloads.gemm_norm_lengths(4, 128, 8192, 5)
+    T, H = int(lens.sum()), 4096
+    g = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn(T, H, device="cuda", dtype=torch.bfloat16, generator=g)
+    w = (torch.randn(H, H, device="cuda", generator=g) / H ** 0.5).bfloat16()
+    gamma = torch.ones(H, device="cuda", dtype=torch.bfloat16)
+    dz = torch.randn(T, H, device="cuda", dtype=torch.bfloat16, generator=g)
+    y = x @ w.T
+    rstd = torch.rsqrt(y.float().pow(2).mean(dim=1) + 1e-6)
+    for _ in range(iters):
+        xq, wq = L.mx_quantize_t(x), L.mx_quantize_t(w)
+        L.gemm_norm_backward(xq, wq, y, rstd, gamma, dz)
+    torch.cuda.synchronize()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -716,8 +739,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="ITERS",
                     help="run the small ncu capture case ITERS times and exit")
+    ap.add_argument("--case", default="attention", choices=["attention", "gemm_norm"],
+                    help="which small case --profile-case runs")
     args = ap.parse_args()
     if args.profile_case:
+        if args.case == "gemm_norm":
+            return run_profile_case_gemm_norm(args.profile_case)
         return run_profile_case(args.profile_case)
     world, rank, local = _dist()
     try:

@@ -329,7 +329,8 @@ lpfa_status lpfa_nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void*
  * lpfa_rmsnorm_bwd_mx_quantize: the same outputs for dY computed from y (the
  * forward's bf16 Y [rows, cols]), dz (bf16 [rows, cols]), gamma (bf16
  * [cols]) and rstd (fp32 [rows]) in fp32, plus dgamma (fp32 [cols]) summed in
- * a fixed order from dgamma_part (fp32 scratch [rows_p/32, cols]).
+ * a fixed order from dgamma_part (fp32 scratch, 16-byte aligned, of
+ * (rows_p/32) * cols + rows_p floats: the per-block partials, then c_t).
  * Errors: NULL or misaligned pointers, cols % 128 != 0 -> INVALID_ARG.
  * ---------------------------------------------------------------------- */
 lpfa_status lpfa_mx_quantize_t(const void* x, int64_t rows, int64_t cols, void* out,

@@ -53,6 +53,28 @@ lpfa_status set_max_dynamic_smem(const void* func, int bytes) {
   return LPFA_OK;
 }
 
+// Clusters of a kernel with compile-time cluster dimensions that can be
+// resident at once on the current device, recorded per (kernel, device).
+int max_active_clusters(const void* func, int threads, int smem_bytes) {
+  static std::vector<std::tuple<const void*, int, int>> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(g_device_cache_mutex);
+  for (const auto& t : done)
+    if (std::get<0>(t) == func && std::get<1>(t) == dev) return std::get<2>(t);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 1024, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  done.emplace_back(func, dev, n);
+  return n;
+}
+
 lpfa_status make_seq_view(const lpfa_seqs* s, SeqView* out) {
   LPFA_CHECK_ARG(s != nullptr && out != nullptr);
   LPFA_CHECK_ARG(s->nseq >= 1 && s->nseq <= (1 << 20));

@@ -10,9 +10,10 @@
 //               swizzle, K-major) + three 512-byte scale tiles per stage.
 //   warp 1      TMEM allocator and MMA issuer: per stage copies the scale
 //               tiles into TMEM (tcgen05.cp) and issues 4 MMAs of K = 32.
-//   warps 2-5   epilogue: TMEM -> registers -> fp32 global stores; the
-//               accumulator is released as soon as it has been read so the
-//               next tile's main loop overlaps the stores.
+//   warps 2-9   epilogue: two warps per TMEM lane quarter, one per column
+//               half; each reads its 32 rows x 128 columns in four loads and
+//               one wait and releases the accumulator before its fp32 global
+//               stores, so the next tile's main loop overlaps them.
 //
 // Quantizing epilogue (lpfa_mx_gemm_quantize; the fused GEMM+Quantize
 // producer of "Low Precision Flash Attention 4 ...", paragraph 2): the fp32
@@ -36,7 +37,8 @@ constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK;  // 16 KB
 constexpr int kBBytes = kBN * kBK;  // 32 KB
 constexpr int kSfBytes = 512;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;      // producer, MMA issuer, 8 epilogue warps
+constexpr int kEpiChunks = kBN / 64;  // 32-column chunks per epilogue warp
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 256;        // TMEM scale buffers after the accumulator
 
@@ -99,6 +101,70 @@ __device__ __forceinline__ void quant32(const uint32_t (&r)[32], uint32_t code, 
   }
 }
 
+// Epilogue of one 128 x 256 output tile, from the registers holding TMEM
+// lane quarter q (rows 32q.. of 128-row M tile tm), column half h of N tile
+// tn: fp32 stores and / or the quantizing epilogue.
+template <int kQuant>
+__device__ __forceinline__ void epilogue_store(const GemmArgs& g, const uint32_t (&r)[kEpiChunks][32],
+                                               int tm, int tn, int q, int h, int lane) {
+  const int row = tm * kBM + q * 32 + lane;
+  const int col0 = tn * kBN + h * (kBN / 2);
+  float* drow = g.d + static_cast<int64_t>(row) * g.N + col0;
+  uint32_t codes[kEpiChunks];                // this row's (or block's) codes
+#pragma unroll
+  for (int c = 0; c < kEpiChunks; ++c) {
+    if ((kQuant < 0 || g.d != nullptr) && row < g.M) {
+      float4* dst = reinterpret_cast<float4*>(drow + c * 32);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        dst[j] = make_float4(__uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                             __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+    }
+    if (kQuant >= 0) {
+      // block maximum of |d| as bits (NaN above Inf), then the code
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) m = max(m, r[c][j] & 0x7FFFFFFFu);
+      if (kQuant == 2) m = __reduce_max_sync(0xFFFFFFFFu, m);
+      const uint32_t code = e8m0_code_from_amax_bits(m);
+      codes[c] = code;
+      uint32_t w[8];
+      quant32(r[c], code, w);
+      uint4* qdst = reinterpret_cast<uint4*>(g.q + static_cast<int64_t>(row) * g.N + col0 + c * 32);
+      qdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      qdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      // rows = N arrangement (square blocks): column n = col0 + 32c +
+      // lane, i.e. 128-column N tile 2 tn + h, contraction block q of the
+      // M tile
+      if (kQuant == 2 && g.qsf_mma_t != nullptr) {
+        const int64_t nt = static_cast<int64_t>(tn) * 2 + h;
+        g.qsf_mma_t[(nt * g.tiles_m + tm) * 512 + lane * 16 + c * 4 + q] =
+            static_cast<uint8_t>(code);
+      }
+    }
+  }
+  if (kQuant >= 0) {
+    const int nb = g.N / 32;
+    const uint32_t packed = codes[0] | codes[1] << 8 | codes[2] << 16 | codes[3] << 24;
+    if (g.qsf != nullptr) {
+      if (kQuant == 0) {
+        *reinterpret_cast<uint32_t*>(g.qsf + static_cast<int64_t>(row) * nb + col0 / 32) = packed;
+      } else if (lane == 0) {
+        *reinterpret_cast<uint32_t*>(g.qsf + static_cast<int64_t>(tm * 4 + q) * nb + col0 / 32) =
+            packed;
+      }
+    }
+    if (g.qsf_mma != nullptr) {
+      // rows = M arrangement: row (lane, quarter q) of the M tile, the
+      // four contraction blocks of the 128-column N tile 2 tn + h
+      const int64_t nt = static_cast<int64_t>(tn) * 2 + h;
+      *reinterpret_cast<uint32_t*>(
+          g.qsf_mma + (static_cast<int64_t>(tm) * (g.N / 128) + nt) * 512 + lane * 16 + q * 4) =
+          packed;
+    }
+  }
+}
+
 template <int kQuant, int kKind>   // kQuant -1: fp32 only; 0: 1x32 along N; 2: 32x32
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
@@ -126,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh->empty[s], 1);
     }
     mbar_init(&sh->acc_full, 1);
-    mbar_init(&sh->acc_empty, 4);
+    mbar_init(&sh->acc_empty, 8);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_barrier_init();
@@ -247,7 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                 // TMEM lane quarter of this warp
+    // warps 2-9: TMEM lane quarter q (a warp reaches only lanes 32 (warp % 4)
+    // ..), column half h of the 256-column accumulator
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
@@ -256,74 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       acc_phase ^= 1;
       tc_fence_after();
-      const int row = tm * kBM + q * 32 + lane;
-      float* drow = g.d + static_cast<int64_t>(row) * g.N + tn * kBN;
-      uint32_t r[32];
-      uint32_t codes[kBN / 32];                  // this row's (or block's) codes
+      // the half-row in four loads and one wait; the accumulator is released
+      // before any store so the next tile's MMAs overlap the stores
+      uint32_t r[kEpiChunks][32];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        tmem_ld32(tmem_addr(tmem, q * 32, c * 32), r);
-        tmem_ld_wait();
-        if (c == kBN / 32 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->acc_empty);
-        }
-        if ((kQuant < 0 || g.d != nullptr) && row < g.M) {
-          float4* dst = reinterpret_cast<float4*>(drow + c * 32);
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                 __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-        }
-        if (kQuant >= 0) {
-          // block maximum of |d| as bits (NaN above Inf), then the code
-          uint32_t m = 0;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) m = max(m, r[j] & 0x7FFFFFFFu);
-          if (kQuant == 2) m = __reduce_max_sync(0xFFFFFFFFu, m);
-          const uint32_t code = e8m0_code_from_amax_bits(m);
-          codes[c] = code;
-          uint32_t w[8];
-          quant32(r, code, w);
-          uint4* qdst = reinterpret_cast<uint4*>(g.q + static_cast<int64_t>(row) * g.N + tn * kBN + c * 32);
-          qdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          qdst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          // rows = N arrangement (square blocks): column n = tn*256 + 32c +
-          // lane of the N tile, contraction block q of the M tile
-          if (kQuant == 2 && g.qsf_mma_t != nullptr) {
-            const int64_t nt = static_cast<int64_t>(tn) * 2 + c / 4;
-            g.qsf_mma_t[(nt * g.tiles_m + tm) * 512 + lane * 16 + (c % 4) * 4 + q] =
-                static_cast<uint8_t>(code);
-          }
-        }
-      }
-      if (kQuant >= 0) {
-        const int nb = g.N / 32;
-        if (g.qsf != nullptr) {
-          if (kQuant == 0) {
-            uint2* d8 = reinterpret_cast<uint2*>(g.qsf + static_cast<int64_t>(row) * nb + tn * 8);
-            *d8 = make_uint2(codes[0] | codes[1] << 8 | codes[2] << 16 | codes[3] << 24,
-                             codes[4] | codes[5] << 8 | codes[6] << 16 | codes[7] << 24);
-          } else if (lane == 0) {
-            uint2* d8 = reinterpret_cast<uint2*>(g.qsf + static_cast<int64_t>(tm * 4 + q) * nb + tn * 8);
-            *d8 = make_uint2(codes[0] | codes[1] << 8 | codes[2] << 16 | codes[3] << 24,
-                             codes[4] | codes[5] << 8 | codes[6] << 16 | codes[7] << 24);
-          }
-        }
-        if (g.qsf_mma != nullptr) {
-          // rows = M arrangement: row (lane, quarter q) of the M tile, the
-          // four contraction blocks of each 128-column N tile side by side
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int64_t nt = static_cast<int64_t>(tn) * 2 + hf;
-            uint32_t* d4 = reinterpret_cast<uint32_t*>(
-                g.qsf_mma + (static_cast<int64_t>(tm) * (g.N / 128) + nt) * 512 + lane * 16 + q * 4);
-            *d4 = codes[4 * hf] | codes[4 * hf + 1] << 8 | codes[4 * hf + 2] << 16 |
-                  codes[4 * hf + 3] << 24;
-          }
-        }
-      }
+      for (int c = 0; c < kEpiChunks; ++c)
+        tmem_ld32(tmem_addr(tmem, q * 32, (h * kEpiChunks + c) * 32), r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty);
+      epilogue_store<kQuant>(g, r, tm, tn, q, h, lane);
     }
   }
 
@@ -333,6 +345,194 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// ----------------------------------------------------------- CTA pairs
+// The same GEMM on 256 x 256 output tiles, one per CTA pair (cluster of
+// two): the even CTA issues tcgen05.mma.cta_group::2 with M = 256, each CTA
+// holding 128 rows of A, 128 rows (N) of B and its 128 rows of D.  Per MMA
+// each SM reads 8 KB of operands from its shared memory instead of 12 KB,
+// and per stage receives 33 KB instead of 49 KB, for the same work.
+//   producer (warp 0, both CTAs)  TMA of this CTA's A and B halves, its A
+//     scale tile and both B scale tiles (every SM's tensor core needs the
+//     scales of all 256 B rows), each signalling the even CTA's stage barrier
+//     (cta_group::2 completion), whose expected bytes cover both CTAs;
+//   MMA issuer (warp 1 of the even CTA)  scale copies and MMAs for the pair;
+//     commits free the stage in both CTAs and hand the accumulator to both
+//     epilogues;
+//   epilogue (warps 2-9, both CTAs)  as above on this CTA's rows; the odd
+//     CTA releases the accumulator by a remote arrive.
+constexpr int kPairStages = 6;
+constexpr int kPairBBytes = 128 * kBK;                          // B half, 16 KB
+constexpr int kPairSfBytes = 3 * kSfBytes;                      // A + two B tiles
+constexpr int kPairTx = kABytes + kPairBBytes + kPairSfBytes;   // per CTA
+constexpr int kPairStageBytes = (kPairTx + 1023) / 1024 * 1024;
+constexpr int kPairSfCols = 12;                                 // per stage
+static_assert(kSfCol0 + kPairStages * kPairSfCols <= kTmemCols, "TMEM columns");
+
+template <int kQuant>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b,
+                        const __grid_constant__ CUtensorMap tma_sfa,
+                        const __grid_constant__ CUtensorMap tma_sfb, const GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* stage_base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  struct __align__(8) PairSmem {
+    uint64_t full[kPairStages];
+    uint64_t empty[kPairStages];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+  };
+  PairSmem* sh = reinterpret_cast<PairSmem*>(stage_base + kPairStages * kPairStageBytes);
+  volatile int* abort = &sh->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();           // 0: issues the MMAs
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int tiles_m2 = (g.M + 255) / 256;
+  const int ntiles = tiles_m2 * g.tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->acc_full, 1);
+    mbar_init(&sh->acc_empty, 16);                   // 8 epilogue warps per CTA
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+    tma_prefetch_desc(&tma_sfa);
+    tma_prefetch_desc(&tma_sfb);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&sh->tmem_base, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                    // peer barriers initialised
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair; t < ntiles && ok; t += npairs) {
+        const int tm = t % tiles_m2, tn = t / tiles_m2;
+        const int tm128 = 2 * tm + static_cast<int>(rank);
+        for (int kt = 0; kt < g.kt && ok; ++kt) {
+          ok = mbar_wait(&sh->empty[stage], phase ^ 1, g.err, abort, 11);
+          if (!ok) break;
+          uint8_t* buf = stage_base + stage * kPairStageBytes;
+          const uint32_t bar = mapa_shared(smem_u32(&sh->full[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * kPairTx);
+          tma_load_2d_pair(buf, &tma_a, kt * kBK, tm128 * kBM, bar);
+          tma_load_2d_pair(buf + kABytes, &tma_b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
+                           bar);
+          uint8_t* sf = buf + kABytes + kPairBBytes;
+          tma_load_2d_pair(sf, &tma_sfa, 0, tm128 * g.kt + kt, bar);
+          tma_load_2d_pair(sf + kSfBytes, &tma_sfb, 0, (2 * tn) * g.kt + kt, bar);
+          tma_load_2d_pair(sf + 2 * kSfBytes, &tma_sfb, 0, (2 * tn + 1) * g.kt + kt, bar);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    // the whole warp runs the loop converged; lane 0 waits, the elected lane
+    // issues (fewer issue cycles per tcgen05 instruction than a lane branch)
+    if (rank == 0) {
+      const uint32_t idesc = g.idesc;
+      // descriptors of stage 0; a stage adds kPairStageBytes >> 4, a K-step
+      // 32 >> 4 (the 14-bit address field does not carry)
+      const uint64_t ad0 = make_sdesc(smem_u32(stage_base), 16, 1024, 2);
+      const uint64_t bd0 = make_sdesc(smem_u32(stage_base + kABytes), 16, 1024, 2);
+      const uint64_t sd0 = sf_tile_desc(smem_u32(stage_base + kABytes + kPairBBytes));
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int t = pair; t < ntiles && ok; t += npairs, ++local) {
+        if (local > 0) {
+          if (lane == 0) ok = mbar_wait_cluster(&sh->acc_empty, acc_phase ^ 1, g.err, abort, 12);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        for (int kt = 0; kt < g.kt; ++kt) {
+          if (lane == 0) ok = mbar_wait(&sh->full[stage], phase, g.err, abort, 13);
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>(stage * (kPairStageBytes >> 4));
+          // TMEM: A scales at sfa_t, B scales (rows 0-127, 128-255 of N) at
+          // sfa_t + 4, + 8
+          const uint32_t sfa_t = tmem + kSfCol0 + stage * kPairSfCols;
+          tc_cp_pair_32x128b_warpx4_elect(sfa_t, sd0 + so);
+          tc_cp_pair_32x128b_warpx4_elect(sfa_t + 4, sd0 + so + (kSfBytes >> 4));
+          tc_cp_pair_32x128b_warpx4_elect(sfa_t + 8, sd0 + so + (2 * kSfBytes >> 4));
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_pair_mxf8_ss_elect(tmem, ad0 + so + 2 * kb, bd0 + so + 2 * kb,
+                                   idesc_sf_ids(idesc, kb, kb), sfa_t, sfa_t + 4,
+                                   (kt | kb) != 0);
+          tc_commit_pair_mc_elect(&sh->empty[stage], 0x3);
+          if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc_elect(&sh->acc_full, 0x3);
+        acc_phase ^= 1;
+      }
+      if (!ok && lane == 0) *abort = 1;
+      tc_commit_pair_elect(&sh->drain);
+      if (lane == 0) mbar_wait(&sh->drain, 0, nullptr, nullptr, 0);
+      __syncwarp();
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh->acc_empty), 0);
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = pair; t < ntiles && ok; t += npairs) {
+      const int tm = t % tiles_m2, tn = t / tiles_m2;
+      ok = mbar_wait(&sh->acc_full, acc_phase, g.err, abort, 14);
+      if (!ok) break;
+      acc_phase ^= 1;
+      tc_fence_after();
+      uint32_t r[kEpiChunks][32];
+#pragma unroll
+      for (int c = 0; c < kEpiChunks; ++c)
+        tmem_ld32(tmem_addr(tmem, q * 32, (h * kEpiChunks + c) * 32), r[c]);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(acc_empty0);
+      epilogue_store<kQuant>(g, r, 2 * tm + static_cast<int>(rank), tn, q, h, lane);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();                                    // both CTAs done with TMEM
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  cluster_sync();
 }
 
 }  // namespace
@@ -407,6 +607,56 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                 ? idesc_mx_types(kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt))
                 : (idesc_mx_types(kBM, kBN, 1, 1) & ~(1u << 23)) |
                       (kind == kKindMxf4 ? (1u << 23) : 0u);
+
+  // CTA pairs for the MXFP8 / FP6 / FP4-in-byte kinds: any M with the fp32
+  // output, M a multiple of 256 with the quantizing epilogue
+  if (kind == kKindF8F6F4 && (quant < 0 || M % 256 == 0)) {
+    CUtensorMap tsa, tsf_b, tb2;
+    {
+      uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+      uint64_t strides[1] = {static_cast<uint64_t>(K)};
+      uint32_t box[2] = {kBK, 128};
+      lpfa_status st = encode_tmap(&tb2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b8, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != LPFA_OK) return st;
+    }
+    // scale tiles as rows of 128 32-bit words (512 bytes); A rows past the
+    // last 128-row tile read as zeros
+    {
+      uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt};
+      uint64_t strides[1] = {512};
+      uint32_t box[2] = {128, 1};
+      lpfa_status st = encode_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfa_mma, dims, strides,
+                                   box, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != LPFA_OK) return st;
+    }
+    {
+      uint64_t dims[2] = {128, static_cast<uint64_t>(N / 128) * g.kt};
+      uint64_t strides[1] = {512};
+      uint32_t box[2] = {128, 1};
+      lpfa_status st = encode_tmap(&tsf_b, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
+                                   strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st != LPFA_OK) return st;
+    }
+    g.idesc = idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt));
+    const size_t psmem = kPairStages * kPairStageBytes + 256 + 1024;
+    auto go2 = [&](auto kernel) -> lpfa_status {
+      lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
+                                            static_cast<int>(psmem));
+      if (st != LPFA_OK) return st;
+      const int clusters = max_active_clusters(reinterpret_cast<const void*>(kernel), kThreads,
+                                               static_cast<int>(psmem));
+      if (clusters <= 0) return LPFA_ERR_UNSUPPORTED;
+      const int64_t ptiles = ceil_div(M, 2 * kBM) * g.tiles_n;
+      const int pairs = static_cast<int>(ptiles < clusters ? ptiles : clusters);
+      kernel<<<2 * pairs, kThreads, psmem, cs>>>(ta, tb2, tsa, tsf_b, g);
+      LPFA_CHECK_CUDA(cudaGetLastError());
+      return LPFA_OK;
+    };
+    if (quant < 0) return go2(mx_gemm_pair_kernel<-1>);
+    if (quant == 0) return go2(mx_gemm_pair_kernel<0>);
+    return go2(mx_gemm_pair_kernel<2>);
+  }
 
   const size_t smem = kStages * (kind == kKindNvf4   ? GemmCfg<kKindNvf4>::kStageBytes
                                  : kind == kKindMxf4 ? GemmCfg<kKindMxf4>::kStageBytes

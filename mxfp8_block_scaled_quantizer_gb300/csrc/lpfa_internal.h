@@ -63,6 +63,11 @@ int num_sms();
 // device, set once per (kernel, device).
 lpfa_status set_max_dynamic_smem(const void* func, int bytes);
 
+// Clusters of `func` (compile-time cluster dimensions) resident at once on
+// the current device with this block size and dynamic shared memory; 0 if
+// the query fails.  Cached per (kernel, device).
+int max_active_clusters(const void* func, int threads, int smem_bytes);
+
 // cuTensorMapEncodeTiled through the driver entry point.
 lpfa_status encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype,
                         uint32_t rank, const void* base, const uint64_t* dims,

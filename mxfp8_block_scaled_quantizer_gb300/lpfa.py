@@ -393,7 +393,7 @@ def rmsnorm_bwd_mx_quantize(y, dz, gamma, rstd, stream=None):
     rows, cols = y.shape
     m = _mxt_empty(rows, cols, y.device)
     rp = m.data_t.shape[1]
-    part = torch.empty((rp // 32, cols), dtype=torch.float32, device=y.device)
+    part = torch.empty((rp // 32) * cols + rp, dtype=torch.float32, device=y.device)
     dgamma = torch.empty(cols, dtype=torch.float32, device=y.device)
     _ok(_norm_bwd_q(_ptr(y), _ptr(dz), _ptr(gamma), _ptr(rstd), rows, cols, _ptr(m.data),
                     _ptr(m.data_t), _ptr(m.sf), _ptr(m.sf_mma), _ptr(m.sf_mma_t), _ptr(part),

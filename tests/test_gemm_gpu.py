@@ -21,15 +21,17 @@ def L():
 def _gemm_sf_layout(sc):
     """[R, K/32] compact scales -> [R/128][K/128][512] tensor-core tiles."""
     R, nk = sc.shape
-    out = np.zeros((R // 128, nk // 4, 512), dtype=np.uint8)
+    out = np.zeros((-(-R // 128), nk // 4, 512), dtype=np.uint8)
     r, kb = np.meshgrid(np.arange(R), np.arange(nk), indexing="ij")
     out[r // 128, kb // 4, layouts.atom_offset(r % 128, kb % 4)] = sc[r, kb]
     return out
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 512),
-                                   (384, 768, 1024)])
+                                   (384, 768, 1024), (1000, 512, 256), (2560, 2048, 512)])
 def test_mx_gemm_matches_oracle(L, M, N, K):
+    """CTA-pair tiles of 256 rows: a half-empty pair (M = 128, 384), a ragged
+    M and more tiles than resident pairs."""
     rng = np.random.default_rng(M + N + K)
     a = rng.standard_normal((M, K)) * np.exp(rng.uniform(-4, 4, (M, 1)))
     b = rng.standard_normal((N, K)) * np.exp(rng.uniform(-4, 4, (1, K)))
@@ -61,7 +63,7 @@ def _dev(z):
 
 
 @pytest.mark.parametrize("block", ["1x32", "32x32"])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (384, 768, 512)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (384, 768, 512), (512, 1024, 256)])
 def test_mx_gemm_quantize_matches_oracle(L, block, M, N, K):
     """The fused output equals the oracle's quantization of the kernel's own
     fp32 result bit for bit (the codes are decided on those values), and the
