@@ -362,7 +362,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     epilogues;
 //   epilogue (warps 2-9, both CTAs)  as above on this CTA's rows; the odd
 //     CTA releases the accumulator by a remote arrive.
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 5;
+constexpr int kPairStageOut = 32 * 128;                         // epilogue slot per warp
+constexpr int kGroupM = 8;                                      // raster group (M tiles)
+
+// Tile t of the persistent loop -> (M tile, N tile): groups of kGroupM M
+// tiles walked along N, so the pairs resident at once share A and B tiles
+// in L2.
+__device__ __forceinline__ void pair_tile(int t, int tiles_m2, int tiles_n, int& tm, int& tn) {
+  const int per_group = kGroupM * tiles_n;
+  const int grp = t / per_group, first = grp * kGroupM;
+  const int gm = min(kGroupM, tiles_m2 - first);
+  const int w = t - grp * per_group;
+  tm = first + w % gm;
+  tn = w / gm;
+}
 constexpr int kPairBBytes = 128 * kBK;                          // B half, 16 KB
 constexpr int kPairSfBytes = 3 * kSfBytes;                      // A + two B tiles
 constexpr int kPairTx = kABytes + kPairBBytes + kPairSfBytes;   // per CTA
@@ -375,7 +389,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
                         const __grid_constant__ CUtensorMap tma_sfa,
-                        const __grid_constant__ CUtensorMap tma_sfb, const GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tma_sfb,
+                        const __grid_constant__ CUtensorMap tma_d, const GemmArgs g) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -388,7 +403,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t tmem_base;
     int abort;
   };
-  PairSmem* sh = reinterpret_cast<PairSmem*>(stage_base + kPairStages * kPairStageBytes);
+  uint8_t* out_base = stage_base + kPairStages * kPairStageBytes;   // 8 epilogue slots
+  PairSmem* sh = reinterpret_cast<PairSmem*>(out_base + 8 * kPairStageOut);
   volatile int* abort = &sh->abort;
 
   const int warp = threadIdx.x >> 5;
@@ -430,7 +446,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int t = pair; t < ntiles && ok; t += npairs) {
-        const int tm = t % tiles_m2, tn = t / tiles_m2;
+        int tm, tn;
+        pair_tile(t, tiles_m2, g.tiles_n, tm, tn);
         const int tm128 = 2 * tm + static_cast<int>(rank);
         for (int kt = 0; kt < g.kt && ok; ++kt) {
           ok = mbar_wait(&sh->empty[stage], phase ^ 1, g.err, abort, 11);
@@ -505,10 +522,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const uint32_t acc_empty0 = mapa_shared(smem_u32(&sh->acc_empty), 0);
+    uint8_t* slot = out_base + (warp - 2) * kPairStageOut;
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int t = pair; t < ntiles && ok; t += npairs) {
-      const int tm = t % tiles_m2, tn = t / tiles_m2;
+      int tm, tn;
+      pair_tile(t, tiles_m2, g.tiles_n, tm, tn);
       ok = mbar_wait(&sh->acc_full, acc_phase, g.err, abort, 14);
       if (!ok) break;
       acc_phase ^= 1;
@@ -521,8 +540,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(acc_empty0);
-      epilogue_store<kQuant>(g, r, 2 * tm + static_cast<int>(rank), tn, q, h, lane);
+      if constexpr (kQuant < 0) {
+        // fp32 rows through this warp's 4 KB slot (128-byte swizzle: 16-byte
+        // chunk j of row r at j ^ (r % 8)) and a TMA store per 32x32 chunk
+        const int row0 = (2 * tm + static_cast<int>(rank)) * kBM + q * 32;
+        const int col0 = tn * kBN + h * (kBN / 2);
+#pragma unroll
+        for (int c = 0; c < kEpiChunks; ++c) {
+          if (lane == 0) bulk_wait_read0();          // the slot's last store has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(slot + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
+                            __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && row0 < g.M) {
+            tma_store_2d(&tma_d, col0 + 32 * c, row0, slot);
+            bulk_commit();
+          }
+        }
+      } else {
+        epilogue_store<kQuant>(g, r, 2 * tm + static_cast<int>(rank), tn, q, h, lane);
+      }
     }
+    if (kQuant < 0 && lane == 0) bulk_wait0();
   }
 
   tc_fence_before();
@@ -638,8 +681,19 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                                    strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
       if (st != LPFA_OK) return st;
     }
+    // fp32 D as 32x32 boxes (128-byte rows, 128-byte swizzle); rows past M
+    // are not written.  The quantizing epilogue stores from registers.
+    CUtensorMap td = tsa;
+    if (quant < 0) {
+      uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+      uint64_t strides[1] = {static_cast<uint64_t>(N) * 4};
+      uint32_t box[2] = {32, 32};
+      lpfa_status st = encode_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims, strides, box,
+                                   CU_TENSOR_MAP_SWIZZLE_128B);
+      if (st != LPFA_OK) return st;
+    }
     g.idesc = idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt));
-    const size_t psmem = kPairStages * kPairStageBytes + 256 + 1024;
+    const size_t psmem = kPairStages * kPairStageBytes + 8 * kPairStageOut + 256 + 1024;
     auto go2 = [&](auto kernel) -> lpfa_status {
       lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
                                             static_cast<int>(psmem));
@@ -649,7 +703,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
       if (clusters <= 0) return LPFA_ERR_UNSUPPORTED;
       const int64_t ptiles = ceil_div(M, 2 * kBM) * g.tiles_n;
       const int pairs = static_cast<int>(ptiles < clusters ? ptiles : clusters);
-      kernel<<<2 * pairs, kThreads, psmem, cs>>>(ta, tb2, tsa, tsf_b, g);
+      kernel<<<2 * pairs, kThreads, psmem, cs>>>(ta, tb2, tsa, tsf_b, td, g);
       LPFA_CHECK_CUDA(cudaGetLastError());
       return LPFA_OK;
     };

@@ -164,6 +164,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap,
       : "memory");
 }
 
+// TMA tile store shared -> global (bulk group; out-of-range rows and
+// columns of the box are not written).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t x, int32_t y,
+                                             const void* smem_src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+          tmap),
+      "r"(x), "r"(y), "r"(smem_u32(smem_src))
+      : "memory");
+}
+
 // Untiled bulk copy global -> shared (16-byte aligned, bytes % 16 == 0).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc,
                                           uint32_t bytes, uint64_t* bar) {
