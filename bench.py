@@ -18,9 +18,9 @@ Beside the step the JSON line reports, each measured in the same run: the
 bf16 variants of the forward and backward kernels on the same inputs (the
 MXFP8 / bf16 ratio), the fused RMSNorm + MX quantizer, the tensor pipe's
 block-scaled MMA rate, this library's and cuBLAS's MXFP8 GEMM 8192^3 (the
-fastest of the two is the roofline's peak), the quantizing GEMM, the jagged
-GEMM-Norm backward, the end-to-end rate from pinned host memory with the copy
-rates that bound it, and the SM clocks sampled by nvidia-smi during the run
+fastest of the two is the roofline's peak), the quantizing GEMM, the MXFP4,
+NVFP4 and MXFP6 GEMMs, the jagged GEMM-Norm backward, the end-to-end rate
+from pinned host memory with the copy rates that bound it, and the SM clocks sampled by nvidia-smi during the run
 (raw samples in $LPFA_CLOCK_LOG_DIR, default the system temp directory).
 """
 from __future__ import annotations
@@ -538,6 +538,44 @@ def run_lpfa(args, world, rank, local):
         except Exception as exc:  # library path not available in this torch
             mma["cublas_mxfp8_tflops"] = None
             mma["cublas_note"] = repr(exc)[:160]
+        # the other block-scale formats on the same pair kernel (f3): dense
+        # FP4 with MXFP4 and NVFP4 scales (kind::mxf4nvf4) and MXFP6 (E2M3)
+        def _rate(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            g0.record()
+            for _ in range(10):
+                fn()
+            g1.record()
+            torch.cuda.synchronize()
+            return 2.0 * M * N * K / (g0.elapsed_time(g1) / 10) / 1e9
+        try:
+            na, _, nsa = L.nvfp4_quantize(a)
+            nb, _, nsb = L.nvfp4_quantize(b)
+            mma["lpfa_nvfp4_gemm_tflops"] = _rate(
+                lambda: L.lpfa_mx_gemm_fp4(na, nsa, nb, nsb, dmat, nvfp4=True))
+            del na, nb, nsa, nsb
+            fa = L.mx_quantize(a.view(M, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, M),
+                               compact=False, fmt=L.LPFA_ELEM_E2M1)
+            fb = L.mx_quantize(b.view(N, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, N),
+                               compact=False, fmt=L.LPFA_ELEM_E2M1)
+            pa4, pb4 = L.fp4_pack_dense(fa.data.view(M, K)), L.fp4_pack_dense(fb.data.view(N, K))
+            mma["lpfa_mxfp4_gemm_tflops"] = _rate(
+                lambda: L.lpfa_mx_gemm_fp4(pa4, fa.sf_mma, pb4, fb.sf_mma, dmat, nvfp4=False))
+            del fa, fb, pa4, pb4
+            sa6 = L.mx_quantize(a.view(M, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, M),
+                                compact=False, fmt=L.LPFA_ELEM_E2M3)
+            sb6 = L.mx_quantize(b.view(N, K // 128, 128), L.LPFA_BLK_1X32, L.dense_seqs(1, N),
+                                compact=False, fmt=L.LPFA_ELEM_E2M3)
+            pa6 = L.mx_pack_operand(sa6.data.view(M, K), L.LPFA_ELEM_E2M3)
+            pb6 = L.mx_pack_operand(sb6.data.view(N, K), L.LPFA_ELEM_E2M3)
+            mma["lpfa_mxfp6_gemm_tflops"] = _rate(
+                lambda: L.lpfa_mx_gemm_fmt(pa6, sa6.sf_mma, pb6, sb6.sf_mma, dmat,
+                                           L.LPFA_ELEM_E2M3, L.LPFA_ELEM_E2M3))
+            del sa6, sb6, pa6, pb6
+        except Exception as exc:
+            mma["other_formats_note"] = repr(exc)[:160]
         del a, b, ga, gb, dmat
     except Exception as exc:
         mma["error"] = repr(exc)[:160]

@@ -378,13 +378,21 @@ __device__ __forceinline__ void pair_tile(int t, int tiles_m2, int tiles_n, int&
   tn = w / gm;
 }
 constexpr int kPairBBytes = 128 * kBK;                          // B half, 16 KB
-constexpr int kPairSfBytes = 3 * kSfBytes;                      // A + two B tiles
-constexpr int kPairTx = kABytes + kPairBBytes + kPairSfBytes;   // per CTA
-constexpr int kPairStageBytes = (kPairTx + 1023) / 1024 * 1024;
-constexpr int kPairSfCols = 12;                                 // per stage
-static_assert(kSfCol0 + kPairStages * kPairSfCols <= kTmemCols, "TMEM columns");
 
-template <int kQuant>
+// Per-kind pair stage: A 128 rows, B 128 rows (one N half), the A scale
+// tiles and the scale tiles of both B halves (kSfA tiles per 128 rows).
+template <int kKind>
+struct PairCfg {
+  static constexpr int kSfA = GemmCfg<kKind>::kSfA;
+  static constexpr int kTx = kABytes + kPairBBytes + 3 * kSfA * kSfBytes;   // per CTA
+  static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
+  static constexpr int kSfCols = 12 * kSfA;                                // TMEM, per stage
+  static constexpr int kSmem = kPairStages * kStageBytes + 8 * kPairStageOut + 256 + 1024;
+  static_assert(kSfCol0 + kPairStages * kSfCols <= kTmemCols, "TMEM columns");
+  static_assert(kSmem <= 232448, "shared memory");
+};
+
+template <int kQuant, int kKind>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b,
@@ -403,7 +411,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t tmem_base;
     int abort;
   };
-  uint8_t* out_base = stage_base + kPairStages * kPairStageBytes;   // 8 epilogue slots
+  using PC = PairCfg<kKind>;
+  constexpr int kSfA = PC::kSfA;
+  constexpr int kStageBytes = PC::kStageBytes;
+  uint8_t* out_base = stage_base + kPairStages * kStageBytes;       // 8 epilogue slots
   PairSmem* sh = reinterpret_cast<PairSmem*>(out_base + 8 * kPairStageOut);
   volatile int* abort = &sh->abort;
 
@@ -452,16 +463,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int kt = 0; kt < g.kt && ok; ++kt) {
           ok = mbar_wait(&sh->empty[stage], phase ^ 1, g.err, abort, 11);
           if (!ok) break;
-          uint8_t* buf = stage_base + stage * kPairStageBytes;
+          uint8_t* buf = stage_base + stage * kStageBytes;
           const uint32_t bar = mapa_shared(smem_u32(&sh->full[stage]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * kPairTx);
+          if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * PC::kTx);
           tma_load_2d_pair(buf, &tma_a, kt * kBK, tm128 * kBM, bar);
           tma_load_2d_pair(buf + kABytes, &tma_b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
                            bar);
+          // scale tiles: A's kSfA, then each B half's kSfA (a row tile's
+          // tiles are consecutive along K in global memory)
           uint8_t* sf = buf + kABytes + kPairBBytes;
-          tma_load_2d_pair(sf, &tma_sfa, 0, tm128 * g.kt + kt, bar);
-          tma_load_2d_pair(sf + kSfBytes, &tma_sfb, 0, (2 * tn) * g.kt + kt, bar);
-          tma_load_2d_pair(sf + 2 * kSfBytes, &tma_sfb, 0, (2 * tn + 1) * g.kt + kt, bar);
+          const int kts = g.kt * kSfA;
+#pragma unroll
+          for (int u = 0; u < kSfA; ++u) {
+            tma_load_2d_pair(sf + u * kSfBytes, &tma_sfa, 0, tm128 * kts + kt * kSfA + u, bar);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+              tma_load_2d_pair(sf + (kSfA * (1 + hb) + u) * kSfBytes, &tma_sfb, 0,
+                               (2 * tn + hb) * kts + kt * kSfA + u, bar);
+          }
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -472,7 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // issues (fewer issue cycles per tcgen05 instruction than a lane branch)
     if (rank == 0) {
       const uint32_t idesc = g.idesc;
-      // descriptors of stage 0; a stage adds kPairStageBytes >> 4, a K-step
+      // descriptors of stage 0; a stage adds kStageBytes >> 4, a K-step
       // 32 >> 4 (the 14-bit address field does not carry)
       const uint64_t ad0 = make_sdesc(smem_u32(stage_base), 16, 1024, 2);
       const uint64_t bd0 = make_sdesc(smem_u32(stage_base + kABytes), 16, 1024, 2);
@@ -493,18 +512,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t so = static_cast<uint64_t>(stage * (kPairStageBytes >> 4));
-          // TMEM: A scales at sfa_t, B scales (rows 0-127, 128-255 of N) at
-          // sfa_t + 4, + 8
-          const uint32_t sfa_t = tmem + kSfCol0 + stage * kPairSfCols;
-          tc_cp_pair_32x128b_warpx4_elect(sfa_t, sd0 + so);
-          tc_cp_pair_32x128b_warpx4_elect(sfa_t + 4, sd0 + so + (kSfBytes >> 4));
-          tc_cp_pair_32x128b_warpx4_elect(sfa_t + 8, sd0 + so + (2 * kSfBytes >> 4));
+          const uint64_t so = static_cast<uint64_t>(stage * (kStageBytes >> 4));
+          // TMEM: A scale tile u at sfa_t + 4u; B tile u at sfb_t + 8u (N rows
+          // 0-127) and + 4 (rows 128-255)
+          const uint32_t sfa_t = tmem + kSfCol0 + stage * PC::kSfCols;
+          const uint32_t sfb_t = sfa_t + 4 * kSfA;
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            mma_pair_mxf8_ss_elect(tmem, ad0 + so + 2 * kb, bd0 + so + 2 * kb,
-                                   idesc_sf_ids(idesc, kb, kb), sfa_t, sfa_t + 4,
-                                   (kt | kb) != 0);
+          for (int u = 0; u < kSfA; ++u) {
+            tc_cp_pair_32x128b_warpx4_elect(sfa_t + 4 * u, sd0 + so + ((u * kSfBytes) >> 4));
+            tc_cp_pair_32x128b_warpx4_elect(sfb_t + 8 * u,
+                                            sd0 + so + (((kSfA + u) * kSfBytes) >> 4));
+            tc_cp_pair_32x128b_warpx4_elect(sfb_t + 8 * u + 4,
+                                            sd0 + so + (((2 * kSfA + u) * kSfBytes) >> 4));
+          }
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint64_t ad = ad0 + so + 2 * kb, bd = bd0 + so + 2 * kb;
+            const uint32_t acc = (kt | kb) != 0;
+            if constexpr (kKind == kKindF8F6F4) {
+              mma_pair_mxf8_ss_elect(tmem, ad, bd, idesc_sf_ids(idesc, kb, kb), sfa_t, sfb_t, acc);
+            } else if constexpr (kKind == kKindMxf4) {
+              const uint32_t u = kb >> 1, id = 2 * (kb & 1);
+              mma_pair_mxf4_ss_elect(tmem, ad, bd, idesc_sf_ids(idesc, id, id), sfa_t + 4 * u,
+                                     sfb_t + 8 * u, acc);
+            } else {
+              mma_pair_nvf4_ss_elect(tmem, ad, bd, idesc, sfa_t + 4 * kb, sfb_t + 8 * kb, acc);
+            }
+          }
           tc_commit_pair_mc_elect(&sh->empty[stage], 0x3);
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
         }
@@ -651,9 +685,10 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                 : (idesc_mx_types(kBM, kBN, 1, 1) & ~(1u << 23)) |
                       (kind == kKindMxf4 ? (1u << 23) : 0u);
 
-  // CTA pairs for the MXFP8 / FP6 / FP4-in-byte kinds: any M with the fp32
-  // output, M a multiple of 256 with the quantizing epilogue
-  if (kind == kKindF8F6F4 && (quant < 0 || M % 256 == 0)) {
+  // CTA pairs (every kind): any M with the fp32 output, M a multiple of 256
+  // with the quantizing epilogue
+  if (quant < 0 || M % 256 == 0) {
+    const int sfa_tiles = kind == kKindNvf4 ? 4 : kind == kKindMxf4 ? 2 : 1;
     CUtensorMap tsa, tsf_b, tb2;
     {
       uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
@@ -666,7 +701,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
     // scale tiles as rows of 128 32-bit words (512 bytes); A rows past the
     // last 128-row tile read as zeros
     {
-      uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt};
+      uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt * sfa_tiles};
       uint64_t strides[1] = {512};
       uint32_t box[2] = {128, 1};
       lpfa_status st = encode_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfa_mma, dims, strides,
@@ -674,7 +709,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
       if (st != LPFA_OK) return st;
     }
     {
-      uint64_t dims[2] = {128, static_cast<uint64_t>(N / 128) * g.kt};
+      uint64_t dims[2] = {128, static_cast<uint64_t>(N / 128) * g.kt * sfa_tiles};
       uint64_t strides[1] = {512};
       uint32_t box[2] = {128, 1};
       lpfa_status st = encode_tmap(&tsf_b, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
@@ -692,8 +727,13 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
                                    CU_TENSOR_MAP_SWIZZLE_128B);
       if (st != LPFA_OK) return st;
     }
-    g.idesc = idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt));
-    const size_t psmem = kPairStages * kPairStageBytes + 8 * kPairStageOut + 256 + 1024;
+    g.idesc = kind == kKindF8F6F4
+                  ? idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt))
+                  : (idesc_mx_types(2 * kBM, kBN, 1, 1) & ~(1u << 23)) |
+                        (kind == kKindMxf4 ? (1u << 23) : 0u);
+    const size_t psmem = kind == kKindNvf4   ? PairCfg<kKindNvf4>::kSmem
+                         : kind == kKindMxf4 ? PairCfg<kKindMxf4>::kSmem
+                                             : PairCfg<kKindF8F6F4>::kSmem;
     auto go2 = [&](auto kernel) -> lpfa_status {
       lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
                                             static_cast<int>(psmem));
@@ -707,9 +747,11 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
       LPFA_CHECK_CUDA(cudaGetLastError());
       return LPFA_OK;
     };
-    if (quant < 0) return go2(mx_gemm_pair_kernel<-1>);
-    if (quant == 0) return go2(mx_gemm_pair_kernel<0>);
-    return go2(mx_gemm_pair_kernel<2>);
+    if (kind == kKindMxf4) return go2(mx_gemm_pair_kernel<-1, kKindMxf4>);
+    if (kind == kKindNvf4) return go2(mx_gemm_pair_kernel<-1, kKindNvf4>);
+    if (quant < 0) return go2(mx_gemm_pair_kernel<-1, kKindF8F6F4>);
+    if (quant == 0) return go2(mx_gemm_pair_kernel<0, kKindF8F6F4>);
+    return go2(mx_gemm_pair_kernel<2, kKindF8F6F4>);
   }
 
   const size_t smem = kStages * (kind == kKindNvf4   ? GemmCfg<kKindNvf4>::kStageBytes
@@ -726,9 +768,7 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
     LPFA_CHECK_CUDA(cudaGetLastError());
     return LPFA_OK;
   };
-  if (kind == kKindMxf4) return go(mx_gemm_kernel<-1, kKindMxf4>);
-  if (kind == kKindNvf4) return go(mx_gemm_kernel<-1, kKindNvf4>);
-  if (quant < 0) return go(mx_gemm_kernel<-1, kKindF8F6F4>);
+  // one CTA per 128x256 tile: the quantizing epilogue when M % 256 == 128
   if (quant == 0) return go(mx_gemm_kernel<0, kKindF8F6F4>);
   return go(mx_gemm_kernel<2, kKindF8F6F4>);
 }

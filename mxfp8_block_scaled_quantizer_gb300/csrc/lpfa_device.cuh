@@ -907,4 +907,31 @@ __device__ __forceinline__ void tc_commit_pair_elect(uint64_t* bar) {
       : "memory");
 }
 
+// Dense FP4 pair MMAs (kind::mxf4nvf4, K = 64): MXFP4 (scale_vec::2X) and
+// NVFP4 (scale_vec::4X).
+__device__ __forceinline__ void mma_pair_mxf4_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                       uint64_t b_desc, uint32_t idesc,
+                                                       uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t" LPFA_ELECT
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_pair_nvf4_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                       uint64_t b_desc, uint32_t idesc,
+                                                       uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.u32 p, %6, 0;\n\t" LPFA_ELECT
+      "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 }  // namespace lpfa
