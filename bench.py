@@ -20,8 +20,9 @@ MXFP8 / bf16 ratio), the fused RMSNorm + MX quantizer, the tensor pipe's
 block-scaled MMA rate, this library's and cuBLAS's MXFP8 GEMM 8192^3 (the
 fastest of the two is the roofline's peak), the quantizing GEMM, the MXFP4,
 NVFP4 and MXFP6 GEMMs, the jagged GEMM-Norm backward, the end-to-end rate
-from pinned host memory with the copy rates that bound it, and the SM clocks sampled by nvidia-smi during the run
-(raw samples in $LPFA_CLOCK_LOG_DIR, default the system temp directory).
+from pinned host memory with the copy rates that bound it, and the SM clocks
+sampled by nvidia-smi during the run (raw samples in $LPFA_CLOCK_LOG_DIR,
+default the system temp directory).
 """
 from __future__ import annotations
 
