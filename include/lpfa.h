@@ -303,6 +303,26 @@ lpfa_status lpfa_nvfp4_quantize(const void* x, int64_t rows, int64_t cols, void*
                                 void* out_sf, void* out_sf_mma, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Grouped block-scaled GEMM: one or two independent MXFP8 GEMMs
+ * D_i = A_i B_i^T (E4M3 operands, fp32 output) in one persistent launch, with
+ * the arguments, layouts and errors of lpfa_mx_gemm for each problem.  The
+ * problem with the longer contraction runs first on every CTA pair and the
+ * other's tiles are split so that the pairs finish together (the two
+ * backward GEMMs of the GEMM-Norm backward: dW, with a contraction over the
+ * tokens, and dX).
+ * ---------------------------------------------------------------------- */
+typedef struct lpfa_gemm_problem {
+  const void* a;          /* E4M3 [M, K] */
+  const void* sfa_mma;    /* [ceil(M/128)][K/128][512] */
+  const void* b;          /* E4M3 [N, K] */
+  const void* sfb_mma;    /* [N/128][K/128][512] */
+  float* d;               /* fp32 [M, N] */
+  int64_t M, N, K;
+} lpfa_gemm_problem;
+
+lpfa_status lpfa_mx_gemm_grouped(const lpfa_gemm_problem* problems, int32_t count, void* stream);
+
+/* ------------------------------------------------------------------------
  * Jagged GEMM-Norm backward ([P1] paragraph 4 reports it for throughput
  * only; [P1] paragraph 2: fused RMSNorm + Quantize with dual scale layouts).
  * Reading: over the T tokens of a jagged batch (rows of X [T, K], sequences

@@ -24,6 +24,9 @@
 // N) and, for square blocks, rows = N (contraction over M).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include "lpfa_device.cuh"
 #include "lpfa_internal.h"
 
@@ -392,13 +395,69 @@ struct PairCfg {
   static_assert(kSmem <= 232448, "shared memory");
 };
 
+// Up to two GEMMs of one kind in one persistent launch (a grouped GEMM:
+// the two backward GEMMs of the GEMM-Norm backward).  Problem 1, the one
+// with the longer contraction, goes first: its tiles round-robin over the
+// pairs; then each pair takes a number of problem 0's tiles chosen so that
+// every pair's total stage count is about the same (c_hi for the r pairs
+// that took one more problem-1 tile, c_lo for the others, one more for pairs
+// < extra).  Every role of both CTAs walks the same sequence.
+struct PairMaps {
+  CUtensorMap a, b, sfa, sfb, d;
+};
+struct PairProblem {
+  GemmArgs g;
+  int32_t tiles_m2;     // 256-row tiles
+  int32_t ntiles;       // pair tiles
+};
+struct PairGroup {
+  PairProblem p[2];
+  int32_t nprob;
+  int32_t r, c_hi, c_lo, extra;
+};
+
+// k-th tile of this pair's sequence -> (problem, M tile, N tile); false when
+// the sequence is done.
+__device__ __forceinline__ bool pair_walk(const PairGroup& G, int pair, int npairs, int k,
+                                          int& prob, int& tm, int& tn) {
+  if (G.nprob == 1) {
+    const int t = pair + k * npairs;
+    if (t >= G.p[0].ntiles) return false;
+    prob = 0;
+    pair_tile(t, G.p[0].tiles_m2, G.p[0].g.tiles_n, tm, tn);
+    return true;
+  }
+  const int n1 = G.p[1].ntiles;
+  const int cnt1 = n1 / npairs + (pair < n1 % npairs ? 1 : 0);
+  if (k < cnt1) {
+    prob = 1;
+    pair_tile(pair + k * npairs, G.p[1].tiles_m2, G.p[1].g.tiles_n, tm, tn);
+    return true;
+  }
+  // problem 0 in rounds, so that the pairs running at once work on
+  // neighbouring tiles (shared A and B tiles in L2): first c_lo - c_hi rounds
+  // over the pairs that took fewer problem-1 tiles (they start earlier), then
+  // c_hi rounds over all pairs, then one tile for pairs < extra
+  const int j = k - cnt1;
+  const int cnt0 = (pair < G.r ? G.c_hi : G.c_lo) + (pair < G.extra ? 1 : 0);
+  if (j >= cnt0) return false;
+  const int nlo = npairs - G.r, dlo = G.c_lo - G.c_hi;
+  int t;
+  if (pair >= G.r && j < dlo) {
+    t = j * nlo + (pair - G.r);
+  } else {
+    const int jb = pair >= G.r ? j - dlo : j;
+    t = dlo * nlo + jb * npairs + pair;            // jb == c_hi: the extra tile
+  }
+  prob = 0;
+  pair_tile(t, G.p[0].tiles_m2, G.p[0].g.tiles_n, tm, tn);
+  return true;
+}
+
 template <int kQuant, int kKind>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b,
-                        const __grid_constant__ CUtensorMap tma_sfa,
-                        const __grid_constant__ CUtensorMap tma_sfb,
-                        const __grid_constant__ CUtensorMap tma_d, const GemmArgs g) {
+    mx_gemm_pair_kernel(const __grid_constant__ PairMaps m0, const __grid_constant__ PairMaps m1,
+                        const PairGroup G) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,8 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();           // 0: issues the MMAs
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-  const int tiles_m2 = (g.M + 255) / 256;
-  const int ntiles = tiles_m2 * g.tiles_n;
+  uint32_t* const err = G.p[0].g.err;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -435,10 +493,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tma_a);
-    tma_prefetch_desc(&tma_b);
-    tma_prefetch_desc(&tma_sfa);
-    tma_prefetch_desc(&tma_sfb);
+    for (int q = 0; q < G.nprob; ++q) {
+      const PairMaps& m = q ? m1 : m0;
+      tma_prefetch_desc(&m.a);
+      tma_prefetch_desc(&m.b);
+      tma_prefetch_desc(&m.sfa);
+      tma_prefetch_desc(&m.sfb);
+    }
   }
   if (warp == 1) {
     tmem_alloc_pair(&sh->tmem_base, kTmemCols);
@@ -456,18 +517,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = pair; t < ntiles && ok; t += npairs) {
-        int tm, tn;
-        pair_tile(t, tiles_m2, g.tiles_n, tm, tn);
+      int prob, tm, tn;
+      for (int k = 0; ok && pair_walk(G, pair, npairs, k, prob, tm, tn); ++k) {
+        const GemmArgs& g = G.p[prob].g;
+        const PairMaps& m = prob ? m1 : m0;
         const int tm128 = 2 * tm + static_cast<int>(rank);
         for (int kt = 0; kt < g.kt && ok; ++kt) {
-          ok = mbar_wait(&sh->empty[stage], phase ^ 1, g.err, abort, 11);
+          ok = mbar_wait(&sh->empty[stage], phase ^ 1, err, abort, 11);
           if (!ok) break;
           uint8_t* buf = stage_base + stage * kStageBytes;
           const uint32_t bar = mapa_shared(smem_u32(&sh->full[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * PC::kTx);
-          tma_load_2d_pair(buf, &tma_a, kt * kBK, tm128 * kBM, bar);
-          tma_load_2d_pair(buf + kABytes, &tma_b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
+          tma_load_2d_pair(buf, &m.a, kt * kBK, tm128 * kBM, bar);
+          tma_load_2d_pair(buf + kABytes, &m.b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
                            bar);
           // scale tiles: A's kSfA, then each B half's kSfA (a row tile's
           // tiles are consecutive along K in global memory)
@@ -475,10 +537,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int kts = g.kt * kSfA;
 #pragma unroll
           for (int u = 0; u < kSfA; ++u) {
-            tma_load_2d_pair(sf + u * kSfBytes, &tma_sfa, 0, tm128 * kts + kt * kSfA + u, bar);
+            tma_load_2d_pair(sf + u * kSfBytes, &m.sfa, 0, tm128 * kts + kt * kSfA + u, bar);
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb)
-              tma_load_2d_pair(sf + (kSfA * (1 + hb) + u) * kSfBytes, &tma_sfb, 0,
+              tma_load_2d_pair(sf + (kSfA * (1 + hb) + u) * kSfBytes, &m.sfb, 0,
                                (2 * tn + hb) * kts + kt * kSfA + u, bar);
           }
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
@@ -490,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // the whole warp runs the loop converged; lane 0 waits, the elected lane
     // issues (fewer issue cycles per tcgen05 instruction than a lane branch)
     if (rank == 0) {
-      const uint32_t idesc = g.idesc;
+      const uint32_t idesc = G.p[0].g.idesc;
       // descriptors of stage 0; a stage adds kStageBytes >> 4, a K-step
       // 32 >> 4 (the 14-bit address field does not carry)
       const uint64_t ad0 = make_sdesc(smem_u32(stage_base), 16, 1024, 2);
@@ -500,15 +562,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       int local = 0;
-      for (int t = pair; t < ntiles && ok; t += npairs, ++local) {
+      int prob, tm, tn;
+      for (int k = 0; ok && pair_walk(G, pair, npairs, k, prob, tm, tn); ++k, ++local) {
+        const int nkt = G.p[prob].g.kt;
         if (local > 0) {
-          if (lane == 0) ok = mbar_wait_cluster(&sh->acc_empty, acc_phase ^ 1, g.err, abort, 12);
+          if (lane == 0) ok = mbar_wait_cluster(&sh->acc_empty, acc_phase ^ 1, err, abort, 12);
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
         }
         tc_fence_after();
-        for (int kt = 0; kt < g.kt; ++kt) {
-          if (lane == 0) ok = mbar_wait(&sh->full[stage], phase, g.err, abort, 13);
+        for (int kt = 0; kt < nkt; ++kt) {
+          if (lane == 0) ok = mbar_wait(&sh->full[stage], phase, err, abort, 13);
           ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
           if (!ok) break;
           tc_fence_after();
@@ -559,10 +623,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* slot = out_base + (warp - 2) * kPairStageOut;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int t = pair; t < ntiles && ok; t += npairs) {
-      int tm, tn;
-      pair_tile(t, tiles_m2, g.tiles_n, tm, tn);
-      ok = mbar_wait(&sh->acc_full, acc_phase, g.err, abort, 14);
+    int prob, tm, tn;
+    for (int k = 0; ok && pair_walk(G, pair, npairs, k, prob, tm, tn); ++k) {
+      const GemmArgs& g = G.p[prob].g;
+      ok = mbar_wait(&sh->acc_full, acc_phase, err, abort, 14);
       if (!ok) break;
       acc_phase ^= 1;
       tc_fence_after();
@@ -591,7 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && row0 < g.M) {
-            tma_store_2d(&tma_d, col0 + 32 * c, row0, slot);
+            tma_store_2d(prob ? &m1.d : &m0.d, col0 + 32 * c, row0, slot);
             bulk_commit();
           }
         }
@@ -628,6 +692,115 @@ uint32_t mma_type_code(lpfa_elem f) {
     case LPFA_ELEM_E2M1: return 5;
   }
   return 0;
+}
+
+// One pair-kernel problem from the GEMM's arguments (g: M, N, K, tile counts
+// and outputs already set): the tensor maps of A and B (128-row boxes), of
+// the scale tiles (rows of 128 32-bit words; A rows past the last 128-row
+// tile read as zeros) and of the fp32 D (32x32 boxes, 128-byte swizzle;
+// rows past M are not written), and the M = 256 instruction descriptor.
+lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, const void* sfa_mma,
+                         const void* sfb_mma, float* d, int quant, lpfa_elem a_fmt,
+                         lpfa_elem b_fmt, int kind, PairProblem* pp, PairMaps* pm) {
+  const int sfa_tiles = kind == kKindNvf4 ? 4 : kind == kKindMxf4 ? 2 : 1;
+  const uint64_t M = static_cast<uint64_t>(g.M), N = static_cast<uint64_t>(g.N),
+                 K = static_cast<uint64_t>(g.K);
+  {
+    uint64_t dims[2] = {K, M};
+    uint64_t strides[1] = {K};
+    uint32_t box[2] = {kBK, 128};
+    lpfa_status st = encode_tmap(&pm->a, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a8, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != LPFA_OK) return st;
+  }
+  {
+    uint64_t dims[2] = {K, N};
+    uint64_t strides[1] = {K};
+    uint32_t box[2] = {kBK, 128};
+    lpfa_status st = encode_tmap(&pm->b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b8, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != LPFA_OK) return st;
+  }
+  {
+    uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt * sfa_tiles};
+    uint64_t strides[1] = {512};
+    uint32_t box[2] = {128, 1};
+    lpfa_status st = encode_tmap(&pm->sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfa_mma, dims,
+                                 strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != LPFA_OK) return st;
+  }
+  {
+    uint64_t dims[2] = {128, (N / 128) * g.kt * sfa_tiles};
+    uint64_t strides[1] = {512};
+    uint32_t box[2] = {128, 1};
+    lpfa_status st = encode_tmap(&pm->sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
+                                 strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != LPFA_OK) return st;
+  }
+  pm->d = pm->sfa;
+  if (quant < 0) {
+    uint64_t dims[2] = {N, M};
+    uint64_t strides[1] = {N * 4};
+    uint32_t box[2] = {32, 32};
+    lpfa_status st = encode_tmap(&pm->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != LPFA_OK) return st;
+  }
+  pp->g = g;
+  pp->g.idesc = kind == kKindF8F6F4
+                    ? idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt))
+                    : (idesc_mx_types(2 * kBM, kBN, 1, 1) & ~(1u << 23)) |
+                          (kind == kKindMxf4 ? (1u << 23) : 0u);
+  pp->tiles_m2 = static_cast<int32_t>((g.M + 255) / 256);
+  pp->ntiles = pp->tiles_m2 * g.tiles_n;
+  return LPFA_OK;
+}
+
+// Launches the pair kernel on one or two problems (two: fp32 output, one
+// kind; the longer-contraction problem is put in slot 1 and the split of
+// slot 0's tiles over the pairs balances the stage counts).
+lpfa_status launch_pair(int kind, int quant, PairGroup& G, const PairMaps& m0,
+                        const PairMaps& m1, cudaStream_t cs) {
+  const size_t psmem = kind == kKindNvf4   ? PairCfg<kKindNvf4>::kSmem
+                       : kind == kKindMxf4 ? PairCfg<kKindMxf4>::kSmem
+                                           : PairCfg<kKindF8F6F4>::kSmem;
+  auto go2 = [&](auto kernel) -> lpfa_status {
+    lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
+                                          static_cast<int>(psmem));
+    if (st != LPFA_OK) return st;
+    const int clusters = max_active_clusters(reinterpret_cast<const void*>(kernel), kThreads,
+                                             static_cast<int>(psmem));
+    if (clusters <= 0) return LPFA_ERR_UNSUPPORTED;
+    int64_t ptiles = G.p[0].ntiles + (G.nprob > 1 ? G.p[1].ntiles : 0);
+    const int np = static_cast<int>(ptiles < clusters ? ptiles : clusters);
+    if (G.nprob > 1) {
+      // closed-form balance of the stage counts
+      const int64_t n0 = G.p[0].ntiles, n1 = G.p[1].ntiles;
+      const double kt0 = G.p[0].g.kt, kt1 = G.p[1].g.kt;
+      const double target = (n0 * kt0 + n1 * kt1) / np;
+      const int64_t a1 = n1 / np;
+      G.r = static_cast<int32_t>(n1 % np);
+      G.c_hi = static_cast<int32_t>(std::max(0.0, std::floor((target - (a1 + 1) * kt1) / kt0)));
+      G.c_lo = static_cast<int32_t>(std::max(0.0, std::floor((target - a1 * kt1) / kt0)));
+      const int64_t extra = n0 - (static_cast<int64_t>(G.r) * G.c_hi +
+                                  static_cast<int64_t>(np - G.r) * G.c_lo);
+      if (extra >= 0 && extra <= np) {
+        G.extra = static_cast<int32_t>(extra);
+      } else {                                   // plain even split
+        G.r = 0;
+        G.c_hi = G.c_lo = static_cast<int32_t>(n0 / np);
+        G.extra = static_cast<int32_t>(n0 % np);
+      }
+    }
+    kernel<<<2 * np, kThreads, psmem, cs>>>(m0, m1, G);
+    LPFA_CHECK_CUDA(cudaGetLastError());
+    return LPFA_OK;
+  };
+  if (kind == kKindMxf4) return go2(mx_gemm_pair_kernel<-1, kKindMxf4>);
+  if (kind == kKindNvf4) return go2(mx_gemm_pair_kernel<-1, kKindNvf4>);
+  if (quant < 0) return go2(mx_gemm_pair_kernel<-1, kKindF8F6F4>);
+  if (quant == 0) return go2(mx_gemm_pair_kernel<0, kKindF8F6F4>);
+  return go2(mx_gemm_pair_kernel<2, kKindF8F6F4>);
 }
 
 lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
@@ -688,70 +861,13 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   // CTA pairs (every kind): any M with the fp32 output, M a multiple of 256
   // with the quantizing epilogue
   if (quant < 0 || M % 256 == 0) {
-    const int sfa_tiles = kind == kKindNvf4 ? 4 : kind == kKindMxf4 ? 2 : 1;
-    CUtensorMap tsa, tsf_b, tb2;
-    {
-      uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
-      uint64_t strides[1] = {static_cast<uint64_t>(K)};
-      uint32_t box[2] = {kBK, 128};
-      lpfa_status st = encode_tmap(&tb2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, b8, dims, strides, box,
-                                   CU_TENSOR_MAP_SWIZZLE_128B);
-      if (st != LPFA_OK) return st;
-    }
-    // scale tiles as rows of 128 32-bit words (512 bytes); A rows past the
-    // last 128-row tile read as zeros
-    {
-      uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt * sfa_tiles};
-      uint64_t strides[1] = {512};
-      uint32_t box[2] = {128, 1};
-      lpfa_status st = encode_tmap(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfa_mma, dims, strides,
-                                   box, CU_TENSOR_MAP_SWIZZLE_NONE);
-      if (st != LPFA_OK) return st;
-    }
-    {
-      uint64_t dims[2] = {128, static_cast<uint64_t>(N / 128) * g.kt * sfa_tiles};
-      uint64_t strides[1] = {512};
-      uint32_t box[2] = {128, 1};
-      lpfa_status st = encode_tmap(&tsf_b, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
-                                   strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-      if (st != LPFA_OK) return st;
-    }
-    // fp32 D as 32x32 boxes (128-byte rows, 128-byte swizzle); rows past M
-    // are not written.  The quantizing epilogue stores from registers.
-    CUtensorMap td = tsa;
-    if (quant < 0) {
-      uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
-      uint64_t strides[1] = {static_cast<uint64_t>(N) * 4};
-      uint32_t box[2] = {32, 32};
-      lpfa_status st = encode_tmap(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims, strides, box,
-                                   CU_TENSOR_MAP_SWIZZLE_128B);
-      if (st != LPFA_OK) return st;
-    }
-    g.idesc = kind == kKindF8F6F4
-                  ? idesc_mx_types(2 * kBM, kBN, mma_type_code(a_fmt), mma_type_code(b_fmt))
-                  : (idesc_mx_types(2 * kBM, kBN, 1, 1) & ~(1u << 23)) |
-                        (kind == kKindMxf4 ? (1u << 23) : 0u);
-    const size_t psmem = kind == kKindNvf4   ? PairCfg<kKindNvf4>::kSmem
-                         : kind == kKindMxf4 ? PairCfg<kKindMxf4>::kSmem
-                                             : PairCfg<kKindF8F6F4>::kSmem;
-    auto go2 = [&](auto kernel) -> lpfa_status {
-      lpfa_status st = set_max_dynamic_smem(reinterpret_cast<const void*>(kernel),
-                                            static_cast<int>(psmem));
-      if (st != LPFA_OK) return st;
-      const int clusters = max_active_clusters(reinterpret_cast<const void*>(kernel), kThreads,
-                                               static_cast<int>(psmem));
-      if (clusters <= 0) return LPFA_ERR_UNSUPPORTED;
-      const int64_t ptiles = ceil_div(M, 2 * kBM) * g.tiles_n;
-      const int pairs = static_cast<int>(ptiles < clusters ? ptiles : clusters);
-      kernel<<<2 * pairs, kThreads, psmem, cs>>>(ta, tb2, tsa, tsf_b, td, g);
-      LPFA_CHECK_CUDA(cudaGetLastError());
-      return LPFA_OK;
-    };
-    if (kind == kKindMxf4) return go2(mx_gemm_pair_kernel<-1, kKindMxf4>);
-    if (kind == kKindNvf4) return go2(mx_gemm_pair_kernel<-1, kKindNvf4>);
-    if (quant < 0) return go2(mx_gemm_pair_kernel<-1, kKindF8F6F4>);
-    if (quant == 0) return go2(mx_gemm_pair_kernel<0, kKindF8F6F4>);
-    return go2(mx_gemm_pair_kernel<2, kKindF8F6F4>);
+    PairGroup G{};
+    PairMaps m0;
+    lpfa_status st = pair_problem(g, a8, b8, sfa_mma, sfb_mma, d, quant, a_fmt, b_fmt, kind,
+                                  &G.p[0], &m0);
+    if (st != LPFA_OK) return st;
+    G.nprob = 1;
+    return launch_pair(kind, quant, G, m0, m0, cs);
   }
 
   const size_t smem = kStages * (kind == kKindNvf4   ? GemmCfg<kKindNvf4>::kStageBytes
@@ -773,6 +889,41 @@ lpfa_status launch_gemm(const void* a8, const void* sfa_mma, const void* b8,
   return go(mx_gemm_kernel<2, kKindF8F6F4>);
 }
 }  // namespace
+
+extern "C" lpfa_status lpfa_mx_gemm_grouped(const lpfa_gemm_problem* problems, int32_t count,
+                                            void* stream) {
+  LPFA_CHECK_ARG(problems != nullptr && (count == 1 || count == 2));
+  PairGroup G{};
+  PairMaps m[2];
+  for (int i = 0; i < count; ++i) {
+    const lpfa_gemm_problem& pr = problems[i];
+    LPFA_CHECK_ARG(pr.a && pr.sfa_mma && pr.b && pr.sfb_mma && pr.d);
+    LPFA_CHECK_ARG(aligned16(pr.a) && aligned16(pr.b) && aligned16(pr.sfa_mma) &&
+                   aligned16(pr.sfb_mma) && aligned16(pr.d));
+    LPFA_CHECK_ARG(pr.M > 0 && pr.N > 0 && pr.K > 0);
+    LPFA_CHECK_ARG(pr.M < (1 << 20) && pr.N < (1 << 20) && pr.K < (1 << 20));
+    if (pr.N % kBN != 0 || pr.K % kBK != 0) return LPFA_ERR_UNSUPPORTED;
+    GemmArgs g{};
+    g.sfa = static_cast<const uint8_t*>(pr.sfa_mma);
+    g.sfb = static_cast<const uint8_t*>(pr.sfb_mma);
+    g.d = pr.d;
+    g.M = static_cast<int32_t>(pr.M);
+    g.N = static_cast<int32_t>(pr.N);
+    g.K = static_cast<int32_t>(pr.K);
+    g.tiles_m = static_cast<int32_t>(ceil_div(pr.M, kBM));
+    g.tiles_n = static_cast<int32_t>(pr.N / kBN);
+    g.kt = static_cast<int32_t>(pr.K / kBK);
+    lpfa_status st = pair_problem(g, pr.a, pr.b, pr.sfa_mma, pr.sfb_mma, pr.d, -1, LPFA_ELEM_E4M3,
+                                  LPFA_ELEM_E4M3, kKindF8F6F4, &G.p[i], &m[i]);
+    if (st != LPFA_OK) return st;
+  }
+  G.nprob = count;
+  if (count == 2 && G.p[0].g.kt > G.p[1].g.kt) {   // slot 1: the longer contraction
+    std::swap(G.p[0], G.p[1]);
+    std::swap(m[0], m[1]);
+  }
+  return launch_pair(kKindF8F6F4, -1, G, m[0], m[count - 1], static_cast<cudaStream_t>(stream));
+}
 
 extern "C" lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma,
                                     const void* b8, const void* sfb_mma,

@@ -68,6 +68,13 @@ _mx_quantize_fmt = _sig("lpfa_mx_quantize_fmt", ctypes.c_int,
 _rms_quantize = _sig("lpfa_rmsnorm_mx_quantize", ctypes.c_int,
                      ctypes.POINTER(lpfa_seqs), _vp, _vp, _i64, _i64, ctypes.c_float,
                      ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp)
+class lpfa_gemm_problem(ctypes.Structure):
+    _fields_ = [("a", _vp), ("sfa_mma", _vp), ("b", _vp), ("sfb_mma", _vp), ("d", _vp),
+                ("M", _i64), ("N", _i64), ("K", _i64)]
+
+
+_mx_gemm_grouped = _sig("lpfa_mx_gemm_grouped", ctypes.c_int, ctypes.POINTER(lpfa_gemm_problem),
+                        ctypes.c_int32, _vp)
 _mx_gemm = _sig("lpfa_mx_gemm", ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
                 _i64, _i64, _i64, _vp)
 _mx_gemm_q = _sig("lpfa_mx_gemm_quantize", ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -116,7 +123,7 @@ EXPORTED = ("lpfa_status_string", "lpfa_version", "lpfa_device_supported",
             "lpfa_fwd_wait_expiry_selftest", "lpfa_mma_peak", "lpfa_fwd_bf16",
             "lpfa_bwd_bf16", "lpfa_mx_gemm_fmt", "lpfa_mx_pack_operand",
             "lpfa_mx_gemm_fp4", "lpfa_fp4_pack_dense", "lpfa_nvfp4_quantize",
-            "lpfa_mx_quantize_t", "lpfa_rmsnorm_bwd_mx_quantize")
+            "lpfa_mx_quantize_t", "lpfa_rmsnorm_bwd_mx_quantize", "lpfa_mx_gemm_grouped")
 
 
 class LpfaError(RuntimeError):
@@ -411,9 +418,20 @@ def gemm_norm_backward(xq: MXT, wq: MXT, y, rstd, gamma, dz, stream=None):
     dyq, dgamma = rmsnorm_bwd_mx_quantize(y, dz, gamma, rstd, stream)
     dx = torch.empty((T, K), dtype=torch.float32, device=y.device)
     dw = torch.empty((N, K), dtype=torch.float32, device=y.device)
-    lpfa_mx_gemm(dyq.data, dyq.sf_mma, wq.data_t, wq.sf_mma_t, dx, stream)
-    lpfa_mx_gemm(dyq.data_t, dyq.sf_mma_t, xq.data_t, xq.sf_mma_t, dw, stream)
+    lpfa_mx_gemm_grouped([(dyq.data, dyq.sf_mma, wq.data_t, wq.sf_mma_t, dx),
+                          (dyq.data_t, dyq.sf_mma_t, xq.data_t, xq.sf_mma_t, dw)], stream)
     return dx, dw, dgamma
+
+
+def lpfa_mx_gemm_grouped(problems, stream=None):
+    """One or two D = A B^T MXFP8 GEMMs (fp32 out) in one launch; each
+    problem is (a8 [M, K], sfa_mma, b8 [N, K], sfb_mma, d [M, N])."""
+    arr = (lpfa_gemm_problem * len(problems))()
+    for i, (a8, sfa, b8, sfb, d) in enumerate(problems):
+        M, K = a8.shape
+        arr[i] = lpfa_gemm_problem(_ptr(a8), _ptr(sfa), _ptr(b8), _ptr(sfb), _ptr(d),
+                                   M, b8.shape[0], K)
+    _ok(_mx_gemm_grouped(arr, len(problems), _stream(stream)), "lpfa_mx_gemm_grouped")
 
 
 def lpfa_mx_gemm_quantize(a8, sfa_mma, b8, sfb_mma, block, out, sf=None, sf_mma=None,

@@ -186,3 +186,49 @@ def test_mx_gemm_quantize_codes_against_exact_product(L, block):
     assert not np.any(differ & ~open_)
     # the check decides most blocks
     assert open_.mean() < (0.1 if block == "1x32" else 0.6)
+
+
+# ------------------------------------------------------------ grouped GEMM
+def _mx_operand(R, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = (torch.randn(R, K, generator=g) * torch.exp(torch.randn(R, 1, generator=g))).bfloat16()
+    p, s = mx.quantize_1x32(x.float().numpy().astype(np.float64))
+    dev = lambda z: torch.from_numpy(np.ascontiguousarray(z)).cuda()
+    return dev(p), dev(_gemm_sf_layout(s)), p, s
+
+
+def test_mx_gemm_grouped_equals_separate(L):
+    """Two problems in one launch (a short-contraction one with a ragged M and
+    many tiles, a long-contraction one with few) give bit-for-bit the results
+    of separate launches, which match the oracle."""
+    shapes = [(1284, 512, 256), (256, 768, 1408)]
+    ops = []
+    for i, (M, N, K) in enumerate(shapes):
+        a, sa, pa, qa = _mx_operand(M, K, 10 + i)
+        b, sb, pb, qb = _mx_operand(N, K, 20 + i)
+        ops.append((a, sa, b, sb, M, N, pa, qa, pb, qb))
+    sep = []
+    for a, sa, b, sb, M, N, *_ in ops:
+        d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        L.lpfa_mx_gemm(a, sa, b, sb, d)
+        sep.append(d)
+    grp = [torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+           for _, _, _, _, M, N, *_ in ops]
+    L.lpfa_mx_gemm_grouped([(a, sa, b, sb, d) for (a, sa, b, sb, *_), d in zip(ops, grp)])
+    one = torch.full_like(sep[0], float("nan"))
+    L.lpfa_mx_gemm_grouped([(ops[0][0], ops[0][1], ops[0][2], ops[0][3], one)])
+    torch.cuda.synchronize()
+    for d, e in zip(grp, sep):
+        assert torch.equal(d, e)
+    assert torch.equal(one, sep[0])
+    for (a, sa, b, sb, M, N, pa, qa, pb, qb), d in zip(ops, sep):
+        want = mx.mx_gemm(pa, qa, pb, qb)
+        bound = 1e-5 * (np.abs(mx.dq_1x32(pa, qa)) @ np.abs(mx.dq_1x32(pb, qb)).T)
+        assert np.all(np.abs(d.cpu().numpy().astype(np.float64) - want) <= bound + 1e-30)
+
+
+def test_mx_gemm_grouped_rejects_bad_arguments(L):
+    arr = (L.lpfa_gemm_problem * 3)()
+    assert L._mx_gemm_grouped(arr, 3, None) == L.LPFA_ERR_INVALID_ARG
+    assert L._mx_gemm_grouped(arr, 0, None) == L.LPFA_ERR_INVALID_ARG
+    assert L._mx_gemm_grouped(arr, 1, None) == L.LPFA_ERR_INVALID_ARG   # null pointers
