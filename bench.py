@@ -48,7 +48,7 @@ METRIC = "MXFP8 attn fwd/bwd PFLOP/s (B8 H32 S8192 D128 causal); % of FP8 MMA pe
 WORKLOAD = "llm"
 FP8_OVER_BF16 = 2.0      # nominal dense fp8 : bf16 tensor-core ratio
 NORM_ITERS = 20          # timed launches of the fused RMSNorm + MX quantizer
-E2E_MIN_STEPS = 20       # steps the end-to-end leg times at least
+E2E_MIN_STEPS = 40       # steps the end-to-end leg times at least
 
 
 def _peaks():
