@@ -247,6 +247,93 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32, 2)   // >= 16 warps per S
 }
 
 // ---------------------------------------------------------------------------
+// 32 consecutive tokens per channel (the forward's V), E4M3: a warp takes 32
+// tokens x 64 channels of the token-major [T, H*D] view, lane l on tokens
+// 4i + l/8 (i < 8) and channels 8(l%8)..+7, so each load instruction reads
+// four whole 128-byte row segments.  A channel's block maximum is the
+// maximum over the lane's 8 tokens, then over the 4 lanes holding the same
+// channels (lane distance 8, 16).
+__global__ void __launch_bounds__(128) mx_quantize_32x1_e4m3_kernel(const QuantArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t HD = static_cast<int64_t>(a.H) * a.D;
+  const int64_t c0 = (static_cast<int64_t>(blockIdx.y) * 4 + warp) * 64;
+  if (c0 >= HD) return;
+  const int64_t rb = blockIdx.x, pr0 = rb * 32;
+  const int sq = seq_of_sf_row(a.seqs, pr0);
+  const SeqInfo si = seq_info(a.seqs, sq);
+  const int64_t off = pr0 - si.sf_start;            // token offset in sequence
+  const int64_t nv64 = static_cast<int64_t>(si.len) - off;
+  const int nvalid = nv64 < 0 ? 0 : (nv64 > 32 ? 32 : static_cast<int>(nv64));
+  const int g = lane & 7, rs = lane >> 3;
+  const int64_t col = c0 + 8 * g;
+  uint4 raw[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + rs;
+    raw[i] = r < nvalid ? __ldcs(reinterpret_cast<const uint4*>(a.x + (si.start + off + r) * HD + col))
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+  uint32_t cm[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(&raw[i]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      cm[2 * k] = max(cm[2 * k], (u[k] << 16) & 0x7FFFFFFFu);
+      cm[2 * k + 1] = max(cm[2 * k + 1], u[k] & 0x7FFF0000u);
+    }
+  }
+  uint32_t code[8];
+  float inv[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    cm[k] = max(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 8));
+    cm[k] = max(cm[k], __shfl_xor_sync(0xFFFFFFFFu, cm[k], 16));
+    code[k] = e8m0_code_from_amax_bits(cm[k]);
+    inv[k] = inv_scale_from_code(code[k]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + rs;
+    if (r < nvalid) {
+      const uint32_t* u = reinterpret_cast<const uint32_t*>(&raw[i]);
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        f[2 * k] = __uint_as_float(u[k] << 16);
+        f[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+      }
+      uint32_t w[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        w[h] = cvt_e4m3x4(f[4 * h] * inv[4 * h], f[4 * h + 1] * inv[4 * h + 1],
+                          f[4 * h + 2] * inv[4 * h + 2], f[4 * h + 3] * inv[4 * h + 3]);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (code[4 * h + q] == 0xFFu) w[h] = (w[h] & ~(0xFFu << (8 * q))) | (0x7Fu << (8 * q));
+      }
+      __stcs(reinterpret_cast<uint2*>(a.out + (si.start + off + r) * HD + col), make_uint2(w[0], w[1]));
+    }
+  }
+  if (rs == 0) {
+    if (a.sf != nullptr)
+      *reinterpret_cast<uint2*>(a.sf + rb * HD + col) =
+          make_uint2(code[0] | code[1] << 8 | code[2] << 16 | code[3] << 24,
+                     code[4] | code[5] << 8 | code[6] << 16 | code[7] << 24);
+    if (a.sf_mma != nullptr) {
+      // operand rows = channels of a head, contraction blocks = token blocks
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t cc = col + k;
+        const int64_t h = cc / a.D, d = cc % a.D;
+        a.sf_mma[((rb >> 2) * a.H + h) * 512 + (d % 32) * 16 + (d / 32) * 4 + (rb & 3)] =
+            static_cast<uint8_t>(code[k]);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Fused RMSNorm + MX quantization ("Low Precision Flash Attention 4 ...",
 // paragraph 2: fused RMSNorm+Quantize kernels producing FP8 output with dual
 // scale factor layouts in one pass).  y = x / sqrt(mean(x^2) + eps) * w over
@@ -481,8 +568,15 @@ void launch_quantize(lpfa_block blk, bool d128, dim3 grid, dim3 block, cudaStrea
       else mx_quantize_kernel<0, 2, kFmt><<<grid, block, 0, cs>>>(a);
       break;
     case LPFA_BLK_32X1:
-      if (d128) mx_quantize_kernel<1, 4, kFmt><<<grid, block, 0, cs>>>(a);
-      else mx_quantize_kernel<1, 2, kFmt><<<grid, block, 0, cs>>>(a);
+      if constexpr (kFmt == kFmtE4M3) {
+        const dim3 g2(static_cast<unsigned>(a.seqs.total_sf_rows / 32),
+                      static_cast<unsigned>((static_cast<int64_t>(a.H) * a.D + 255) / 256));
+        mx_quantize_32x1_e4m3_kernel<<<g2, 128, 0, cs>>>(a);
+      } else if (d128) {
+        mx_quantize_kernel<1, 4, kFmt><<<grid, block, 0, cs>>>(a);
+      } else {
+        mx_quantize_kernel<1, 2, kFmt><<<grid, block, 0, cs>>>(a);
+      }
       break;
     case LPFA_BLK_32X32:
       if (d128) mx_quantize_kernel<2, 4, kFmt><<<grid, block, 0, cs>>>(a);
