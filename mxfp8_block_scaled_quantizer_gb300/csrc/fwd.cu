@@ -57,10 +57,9 @@ namespace lpfa {
 namespace {
 
 constexpr int kBlockM = 128;   // queries per CTA
-constexpr int kThreads = 352;
 constexpr int kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
-constexpr uint32_t kColSFQ = 448, kColSFK = 452, kColSFP = 460, kColSFV = 468;
+constexpr uint32_t kColSFQ = 448, kColSFK = 452, kColSFP = 460;   // SFV after SFP
 
 struct FwdParams {
   SeqView seqs;
@@ -89,8 +88,17 @@ struct FwdParams {
 template <int D, bool B16>
 struct FwdCfg {
   static constexpr int kN = B16 ? 128 : 256;              // keys per tile
-  static constexpr int kHalfN = kN / 2;                   // keys per softmax warpgroup
-  static constexpr int kChunks = kHalfN / 32;             // 32-key chunks per warpgroup
+  // softmax warpgroups: each takes kWgN keys of every tile (all 128 query
+  // rows, one per thread): 2 x 128 keys (MXFP8), 2 x 64 keys (bf16).  Four
+  // warpgroups of 64 keys (608 threads, 96 registers) were measured slower
+  // on the llm workload (2.88 against 2.73 ms): the four-way row-maximum
+  // exchange and the 16-warp barriers cost more than the shorter chains gain.
+  static constexpr int kWG = 2;
+  static constexpr int kWgN = kN / kWG;                   // keys per softmax warpgroup
+  static constexpr int kChunks = kWgN / 32;               // 32-key chunks per warpgroup
+  static constexpr int kThreads = (3 + 4 * kWG) * 32;     // producer, S issuer, softmax, PV issuer
+  static constexpr int kPvWarp = 2 + 4 * kWG;
+  static constexpr uint32_t kColSFV = kColSFP + 4 * kWG;  // one 4-column SFP group per warpgroup
   static constexpr int kEl = B16 ? 2 : 1;                 // bytes per element
   static constexpr int kRowB = D * kEl;                   // bytes per token row
   static constexpr int kChunkB = kRowB < 128 ? kRowB : 128;
@@ -106,9 +114,9 @@ struct FwdCfg {
   static constexpr int kSfQ = kStage0 + kStages * kStageBytes;
   static constexpr int kSfStage0 = kSfQ + 512;            // SFK[2], SFV[2]
   static constexpr int kSfStageBytes = B16 ? 0 : 2048;
-  static constexpr int kXMax = kSfStage0 + kStages * kSfStageBytes;  // float [2][2][128]
-  static constexpr int kXSum = kXMax + 2 * 2 * 128 * 4;     // float [2][128]
-  static constexpr int kBar = kXSum + 2 * 128 * 4;
+  static constexpr int kXMax = kSfStage0 + kStages * kSfStageBytes;  // float [2][kWG][128]
+  static constexpr int kXSum = kXMax + 2 * kWG * 128 * 4;   // float [kWG][128]
+  static constexpr int kBar = kXSum + kWG * 128 * 4;
   static constexpr int kTotal = kBar + 256;
   // one MMA instruction contracts 32 bytes of K (32 fp8 or 16 bf16 elements)
   static constexpr int kKStepsS = kRowB / 32;             // S = Q K^T over head_dim
@@ -126,7 +134,7 @@ struct FwdBars {
   uint64_t s_free;     // every softmax warp holds its row of S_j (8 arrivals)
   uint64_t p_full;     // P_j, SFP_j in TMEM, O rescaled (8 arrivals)
   uint64_t pv_done;    // PV_j complete (MMA commit)
-  uint64_t xchg[4];    // row-pair exchange, one per TMEM lane quarter (2)
+  uint64_t xchg[4];    // row maxima exchange, one per TMEM lane quarter (kWG)
   uint64_t drain[2];   // per MMA-issuing warp
   uint32_t tmem_base;
   int abort;
@@ -216,7 +224,7 @@ __device__ __forceinline__ constexpr uint64_t kstep_off(int kb, int rows) {
 }
 
 template <int D, bool B16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
     mx_attn_fwd_kernel(const __grid_constant__ CUtensorMap tma_q,
                        const __grid_constant__ CUtensorMap tma_k,
                        const __grid_constant__ CUtensorMap tma_v,
@@ -224,7 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = FwdCfg<D, B16>;
   constexpr int kStages = C::kStages;
   constexpr int kBlockN = C::kN;
-  constexpr int kHalfN = C::kHalfN;
+  constexpr int kWG = C::kWG;
+  constexpr int kWgN = C::kWgN;
+  constexpr uint32_t kColSFV = C::kColSFV;
   constexpr uint32_t kSw = C::kSw;
   constexpr uint32_t kSbo = C::kSbo;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -244,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->kv_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->s_free, 8);
-    mbar_init(&bars->p_full, 8);
+    mbar_init(&bars->s_free, 4 * kWG);
+    mbar_init(&bars->p_full, 4 * kWG);
     mbar_init(&bars->pv_done, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&bars->xchg[q], 2);
+    for (int q = 0; q < 4; ++q) mbar_init(&bars->xchg[q], kWG);
     mbar_init(&bars->drain[0], 1);
     mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
@@ -345,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_sleep(&bars->kv_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
     if (q_issued >= 0)
       mbar_wait_sleep(&bars->q_full, static_cast<uint32_t>(q_issued), nullptr, nullptr, 0);
-  } else if (warp == 1 || warp == 10) {
+  } else if (warp == 1 || warp == C::kPvWarp) {
     // --------------------------------------------------------- MMA issuers
     // A warp issues at most one tcgen05 instruction every ~60-90 cycles, and
     // one tile needs 12 MMAs, 4 scale copies and 2 commits: more than a
@@ -418,6 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      C::kNCh > 1 ? kBlockN * C::kChunkB : 16, kSbo, kSw);
       const uint32_t tO = tmem + kColO, tP = tmem + kColP;
       const uint32_t tSFP = tmem + kColSFP, tSFV = tmem + kColSFV;
+      constexpr int kStepsWg = kWgN / C::kKeysPerStep;   // PV K-steps per softmax warpgroup
       // O (+)= P V over 256 keys (8 K-steps; scale group = K-step / 4); V
       // landed before its S could be computed, and P is written after the
       // softmax saw S, so P-full orders both.  An item's first PV overwrites
@@ -441,9 +452,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_cp_32x128b_warpx4_elect(tSFV + 4, dsf + fo + (1536 >> 4));
 #pragma unroll
           for (int kb = 0; kb < C::kKStepsPV; ++kb)
+            // A (P) scales: warpgroup kb / kStepsWg's column group, byte
+            // kb % kStepsWg; B (V) scales: 128-key tile kb / 4, byte kb % 4
             mma_mxf8_ts_elect(tO, tP + 8 * kb, dv + so + kb * kVStep,
-                              idesc_sf_ids(idesc_o, kb & 3, kb & 3), tSFP + 4 * (kb >> 2),
-                              tSFV + 4 * (kb >> 2), (!first) || (kb > 0));
+                              idesc_sf_ids(idesc_o, kb % kStepsWg, kb & 3),
+                              tSFP + 4 * (kb / kStepsWg), tSFV + 4 * (kb >> 2),
+                              (!first) || (kb > 0));
         }
         tc_commit_elect(&bars->pv_done);
         return true;
@@ -467,9 +481,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                    // TMEM lane quarter
     const int row = quad * 32 + lane;             // query row within tile
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tSrow = tmem + kColS + kHalfN * wg + lane_base;
-    float* xmax = reinterpret_cast<float*>(sm + C::kXMax);   // [2][2][128]
-    float* xsum = reinterpret_cast<float*>(sm + C::kXSum);   // [2][128]
+    const uint32_t tSrow = tmem + kColS + kWgN * wg + lane_base;
+    float* xmax = reinterpret_cast<float*>(sm + C::kXMax);   // [2][kWG][128]
+    float* xsum = reinterpret_cast<float*>(sm + C::kXSum);   // [kWG][128]
     uint64_t* xbar = &bars->xchg[quad];
     const float c2 = p.scale_log2;
     const uint64_t c2x2 = pack2(c2, c2);
@@ -499,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free);
-        const int k0 = j * kBlockN + wg * kHalfN;
-        const bool need_mask = (k0 + kHalfN > w.len) || (p.causal && k0 + kHalfN - 1 > q0);
+        const int k0 = j * kBlockN + wg * kWgN;
+        const bool need_mask = (k0 + kWgN > w.len) || (p.causal && k0 + kWgN - 1 > q0);
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < kCh; ++c)
@@ -522,21 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         float hmax = cmax[0];
 #pragma unroll
         for (int c = 1; c < kCh; ++c) hmax = fmaxf(hmax, cmax[c]);
-        float* xm = xmax + (gx & 1) * 256;
+        float* xm = xmax + (gx & 1) * (kWG * 128);
         xm[wg * 128 + row] = hmax;
         __syncwarp();
         if (lane == 0) mbar_arrive(xbar);
         ok = mbar_wait_sleep(xbar, gx & 1, p.err, abort, 33, p.wait_ns);
         if (!ok) break;
         ++gx;
-        const float tmax = fmaxf(hmax, xm[(1 - wg) * 128 + row]);
+        float tmax = hmax;
+#pragma unroll
+        for (int o = 0; o < kWG; ++o)
+          if (o != wg) tmax = fmaxf(tmax, xm[o * 128 + row]);
         const float mt = __fmul_rn(tmax, c2);
         float m_new = m_ref;
         if (m_ref == -INFINITY || mt > m_ref + p.threshold) m_new = mt;
         const bool moved = (m_new != m_ref);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
-        uint32_t pw[32];
+        constexpr int kPW = B16 ? 16 * kCh : 8 * kCh;   // P words of this warpgroup's keys
+        uint32_t pw[kPW];
         float lsum = 0.f;
         uint32_t sfp = 0;
         if constexpr (B16) {
@@ -563,9 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsum = lo2(acc) + hi2(acc);
         } else {
           // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
-          uint32_t code[4];
+          uint32_t code[kCh];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kCh; ++c) {
             const float amax = ex2(__fsub_rn(__fmul_rn(cmax[c], c2), m_use));
             code[c] = e8m0_code_from_amax_bits(__float_as_uint(amax));
             sfp |= code[c] << (8 * c);
@@ -573,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P * 2^-e = 2^(s*c2 - (m + e)), two elements per instruction; l sums
           // the scaled values per block and rescales by 2^e
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kCh; ++c) {
             const int e = static_cast<int>(code[c]) - 127;
             const float nb = -(m_use + static_cast<float>(e));
             const uint64_t nb2 = pack2(nb, nb);
@@ -604,20 +622,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the previous tile's S and PV are done: its K/V stage may be refilled
           if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
         }
-        tmem_st32(tmem + kColP + 32 * wg + lane_base, pw);
+        if constexpr (kPW == 32) tmem_st32(tmem + kColP + kPW * wg + lane_base, pw);
+        else tmem_st16(tmem + kColP + kPW * wg + lane_base, pw);
         if constexpr (!B16) tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
         // selective rescale of O (and l): only warps holding a moved row; each
         // half rescales half of the columns
         if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
-          uint32_t rr[32];
+          constexpr int kOC = D / kWG;            // O columns of this warpgroup
+          if constexpr (kOC >= 32) {
+            uint32_t rr[32];
 #pragma unroll 1
-          for (int c = 0; c < D / 64; ++c) {
-            const uint32_t ta = tmem + kColO + (D / 2) * wg + 32 * c + lane_base;
-            tmem_ld32(ta, rr);
+            for (int c = 0; c < kOC / 32; ++c) {
+              const uint32_t ta = tmem + kColO + kOC * wg + 32 * c + lane_base;
+              tmem_ld32(ta, rr);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+              tmem_st32(ta, rr);
+            }
+          } else {
+            uint32_t rr[16];
+            const uint32_t ta = tmem + kColO + kOC * wg + lane_base;
+            tmem_ld16(ta, rr);
             tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-            tmem_st32(ta, rr);
+            for (int e = 0; e < 16; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+            tmem_st16(ta, rr);
           }
         }
         tmem_st_wait();
@@ -628,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bars->p_full);
       }
       if (!ok) break;
-      // epilogue: O / l -> bf16 (each half writes half of the columns), LSE
+      // epilogue: O / l -> bf16 (each warpgroup writes D / kWG columns), LSE
       xsum[wg * 128 + row] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(xbar);
@@ -640,29 +670,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the item's last S and PV are done: its K/V stage may be refilled
       if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
-      const float lt = l + xsum[(1 - wg) * 128 + row];
+      // the row's sum over the warpgroups in a fixed order (every warpgroup
+      // scales its O columns by the same 1 / l)
+      float lt = 0.f;
+#pragma unroll
+      for (int o = 0; o < kWG; ++o) lt += xsum[o * 128 + row];
       const float inv_l = (lt > 0.f) ? 1.f / lt : 0.f;
       const bool valid = qi < w.len;
       const int64_t tok = w.start + qi;
-      uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D + (D / 2) * wg);
-      uint32_t rr[32];
+      constexpr int kOC = D / kWG;                // O columns of this warpgroup
+      uint4* dst = reinterpret_cast<uint4*>(p.o + (tok * p.hq + w.head) * D + kOC * wg);
+      auto store8 = [&](const uint32_t* rv, int q) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(rv[2 * kk]) * inv_l,
+                                                    __uint_as_float(rv[2 * kk + 1]) * inv_l);
+          wv[kk] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        dst[q] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+      };
+      if constexpr (kOC >= 32) {
+        uint32_t rr[32];
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(tmem + kColO + (D / 2) * wg + 32 * c + lane_base, rr);
+        for (int c = 0; c < kOC / 32; ++c) {
+          tmem_ld32(tmem + kColO + kOC * wg + 32 * c + lane_base, rr);
+          tmem_ld_wait();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) store8(rr + 8 * i, 4 * c + i);
+          }
+        }
+      } else {
+        uint32_t rr[16];
+        tmem_ld16(tmem + kColO + kOC * wg + lane_base, rr);
         tmem_ld_wait();
         if (valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(
-                  __uint_as_float(rr[8 * i + 2 * kk]) * inv_l,
-                  __uint_as_float(rr[8 * i + 2 * kk + 1]) * inv_l);
-              wv[kk] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            dst[4 * c + i] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          }
+          for (int i = 0; i < 2; ++i) store8(rr + 8 * i, i);
         }
       }
       if (valid && wg == 0) {
@@ -737,7 +782,7 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D, B16>),
                                  static_cast<int>(smem))) != LPFA_OK)
     return st;
-  mx_attn_fwd_kernel<D, B16><<<static_cast<unsigned>(nblocks), kThreads, smem, cs>>>(tq, tk, tv, p);
+  mx_attn_fwd_kernel<D, B16><<<static_cast<unsigned>(nblocks), C::kThreads, smem, cs>>>(tq, tk, tv, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
 }
