@@ -365,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 //     epilogues;
 //   epilogue (warps 2-9, both CTAs)  as above on this CTA's rows; the odd
 //     CTA releases the accumulator by a remote arrive.
-constexpr int kPairStages = 5;
-constexpr int kPairStageOut = 32 * 128;                         // epilogue slot per warp
+constexpr int kPairStageOut = 32 * 64;                          // epilogue slot per warp:
+                                                                // 32 rows x 16 fp32
 constexpr int kGroupM = 8;                                      // raster group (M tiles)
 
 // Tile t of the persistent loop -> (M tile, N tile): groups of kGroupM M
@@ -390,8 +390,11 @@ struct PairCfg {
   static constexpr int kTx = kABytes + kPairBBytes + 3 * kSfA * kSfBytes;   // per CTA
   static constexpr int kStageBytes = (kTx + 1023) / 1024 * 1024;
   static constexpr int kSfCols = 12 * kSfA;                                // TMEM, per stage
-  static constexpr int kSmem = kPairStages * kStageBytes + 8 * kPairStageOut + 256 + 1024;
-  static_assert(kSfCol0 + kPairStages * kSfCols <= kTmemCols, "TMEM columns");
+  // as many stages as shared memory holds (6 for one scale tile per 128
+  // rows, 5 for FP4's two or four)
+  static constexpr int kStages = kSfA == 1 ? 6 : 5;
+  static constexpr int kSmem = kStages * kStageBytes + 8 * kPairStageOut + 256 + 1024;
+  static_assert(kSfCol0 + kStages * kSfCols <= kTmemCols, "TMEM columns");
   static_assert(kSmem <= 232448, "shared memory");
 };
 
@@ -462,8 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint8_t* stage_base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   struct __align__(8) PairSmem {
-    uint64_t full[kPairStages];
-    uint64_t empty[kPairStages];
+    uint64_t full[PairCfg<kKind>::kStages];
+    uint64_t empty[PairCfg<kKind>::kStages];
     uint64_t acc_full;
     uint64_t acc_empty;
     uint64_t drain;
@@ -473,6 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   using PC = PairCfg<kKind>;
   constexpr int kSfA = PC::kSfA;
   constexpr int kStageBytes = PC::kStageBytes;
+  constexpr int kPairStages = PC::kStages;
   uint8_t* out_base = stage_base + kPairStages * kStageBytes;       // 8 epilogue slots
   PairSmem* sh = reinterpret_cast<PairSmem*>(out_base + 8 * kPairStageOut);
   volatile int* abort = &sh->abort;
@@ -639,23 +643,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(acc_empty0);
       if constexpr (kQuant < 0) {
-        // fp32 rows through this warp's 4 KB slot (128-byte swizzle: 16-byte
-        // chunk j of row r at j ^ (r % 8)) and a TMA store per 32x32 chunk
+        // fp32 rows through this warp's 2 KB slot, 16 columns at a time
+        // (64-byte swizzle: 16-byte chunk j of row r at j ^ ((r / 2) % 4)),
+        // and a TMA store per 32x16 chunk
         const int row0 = (2 * tm + static_cast<int>(rank)) * kBM + q * 32;
         const int col0 = tn * kBN + h * (kBN / 2);
 #pragma unroll
-        for (int c = 0; c < kEpiChunks; ++c) {
+        for (int c = 0; c < 2 * kEpiChunks; ++c) {
           if (lane == 0) bulk_wait_read0();          // the slot's last store has read it
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(slot + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_float4(__uint_as_float(r[c][4 * j]), __uint_as_float(r[c][4 * j + 1]),
-                            __uint_as_float(r[c][4 * j + 2]), __uint_as_float(r[c][4 * j + 3]));
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t* v = &r[c >> 1][16 * (c & 1) + 4 * j];
+            *reinterpret_cast<float4*>(slot + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_float4(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]),
+                            __uint_as_float(v[3]));
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && row0 < g.M) {
-            tma_store_2d(prob ? &m1.d : &m0.d, col0 + 32 * c, row0, slot);
+            tma_store_2d(prob ? &m1.d : &m0.d, col0 + 16 * c, row0, slot);
             bulk_commit();
           }
         }
@@ -697,8 +704,9 @@ uint32_t mma_type_code(lpfa_elem f) {
 // One pair-kernel problem from the GEMM's arguments (g: M, N, K, tile counts
 // and outputs already set): the tensor maps of A and B (128-row boxes), of
 // the scale tiles (rows of 128 32-bit words; A rows past the last 128-row
-// tile read as zeros) and of the fp32 D (32x32 boxes, 128-byte swizzle;
-// rows past M are not written), and the M = 256 instruction descriptor.
+// tile read as zeros) and of the fp32 D (32-row x 16-column boxes, 64-byte
+// swizzle; rows past M are not written), and the M = 256 instruction
+// descriptor.
 lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, const void* sfa_mma,
                          const void* sfb_mma, float* d, int quant, lpfa_elem a_fmt,
                          lpfa_elem b_fmt, int kind, PairProblem* pp, PairMaps* pm) {
@@ -741,9 +749,9 @@ lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, cons
   if (quant < 0) {
     uint64_t dims[2] = {N, M};
     uint64_t strides[1] = {N * 4};
-    uint32_t box[2] = {32, 32};
+    uint32_t box[2] = {16, 32};
     lpfa_status st = encode_tmap(&pm->d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, d, dims, strides, box,
-                                 CU_TENSOR_MAP_SWIZZLE_128B);
+                                 CU_TENSOR_MAP_SWIZZLE_64B);
     if (st != LPFA_OK) return st;
   }
   pp->g = g;
