@@ -535,18 +535,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d_pair(buf, &m.a, kt * kBK, tm128 * kBM, bar);
           tma_load_2d_pair(buf + kABytes, &m.b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
                            bar);
-          // scale tiles: A's kSfA, then each B half's kSfA (a row tile's
-          // tiles are consecutive along K in global memory)
+          // scale tiles: A's kSfA, then each B half's kSfA; a row tile's
+          // tiles of one stage are consecutive in global memory, so each
+          // group is one copy (a box of kSfA 512-byte rows)
           uint8_t* sf = buf + kABytes + kPairBBytes;
           const int kts = g.kt * kSfA;
+          tma_load_2d_pair(sf, &m.sfa, 0, tm128 * kts + kt * kSfA, bar);
 #pragma unroll
-          for (int u = 0; u < kSfA; ++u) {
-            tma_load_2d_pair(sf + u * kSfBytes, &m.sfa, 0, tm128 * kts + kt * kSfA + u, bar);
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb)
-              tma_load_2d_pair(sf + (kSfA * (1 + hb) + u) * kSfBytes, &m.sfb, 0,
-                               (2 * tn + hb) * kts + kt * kSfA + u, bar);
-          }
+          for (int hb = 0; hb < 2; ++hb)
+            tma_load_2d_pair(sf + kSfA * (1 + hb) * kSfBytes, &m.sfb, 0,
+                             (2 * tn + hb) * kts + kt * kSfA, bar);
           if (++stage == kPairStages) { stage = 0; phase ^= 1; }
         }
       }
@@ -732,7 +730,7 @@ lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, cons
   {
     uint64_t dims[2] = {128, static_cast<uint64_t>(g.tiles_m) * g.kt * sfa_tiles};
     uint64_t strides[1] = {512};
-    uint32_t box[2] = {128, 1};
+    uint32_t box[2] = {128, static_cast<uint32_t>(sfa_tiles)};
     lpfa_status st = encode_tmap(&pm->sfa, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfa_mma, dims,
                                  strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != LPFA_OK) return st;
@@ -740,7 +738,7 @@ lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, cons
   {
     uint64_t dims[2] = {128, (N / 128) * g.kt * sfa_tiles};
     uint64_t strides[1] = {512};
-    uint32_t box[2] = {128, 1};
+    uint32_t box[2] = {128, static_cast<uint32_t>(sfa_tiles)};
     lpfa_status st = encode_tmap(&pm->sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
                                  strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != LPFA_OK) return st;
