@@ -517,36 +517,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      int prob, tm, tn;
-      for (int k = 0; ok && pair_walk(G, pair, npairs, k, prob, tm, tn); ++k) {
-        const GemmArgs& g = G.p[prob].g;
-        const PairMaps& m = prob ? m1 : m0;
-        const int tm128 = 2 * tm + static_cast<int>(rank);
-        for (int kt = 0; kt < g.kt && ok; ++kt) {
-          ok = mbar_wait(&sh->empty[stage], phase ^ 1, err, abort, 11);
-          if (!ok) break;
-          uint8_t* buf = stage_base + stage * kStageBytes;
-          const uint32_t bar = mapa_shared(smem_u32(&sh->full[stage]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * PC::kTx);
-          tma_load_2d_pair(buf, &m.a, kt * kBK, tm128 * kBM, bar);
-          tma_load_2d_pair(buf + kABytes, &m.b, kt * kBK, (2 * tn + static_cast<int>(rank)) * 128,
-                           bar);
-          // scale tiles: A's kSfA, then each B half's kSfA; a row tile's
-          // tiles of one stage are consecutive in global memory, so each
-          // group is one copy (a box of kSfA 512-byte rows)
-          uint8_t* sf = buf + kABytes + kPairBBytes;
-          const int kts = g.kt * kSfA;
-          tma_load_2d_pair(sf, &m.sfa, 0, tm128 * kts + kt * kSfA, bar);
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb)
-            tma_load_2d_pair(sf + kSfA * (1 + hb) * kSfBytes, &m.sfb, 0,
-                             (2 * tn + hb) * kts + kt * kSfA, bar);
-          if (++stage == kPairStages) { stage = 0; phase ^= 1; }
-        }
+    // the whole warp runs the loop converged; lane 0 waits, the elected lane
+    // issues the copies: A, B, the A scale tiles and both B halves' scale
+    // tiles (one 3D box), four copies per stage
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    int prob, tm, tn;
+    for (int k = 0; ok && pair_walk(G, pair, npairs, k, prob, tm, tn); ++k) {
+      const GemmArgs& g = G.p[prob].g;
+      const PairMaps& m = prob ? m1 : m0;
+      const int tm128 = 2 * tm + static_cast<int>(rank);
+      for (int kt = 0; kt < g.kt && ok; ++kt) {
+        if (lane == 0) ok = mbar_wait(&sh->empty[stage], phase ^ 1, err, abort, 11);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        uint8_t* buf = stage_base + stage * kStageBytes;
+        const uint32_t bar = mapa_shared(smem_u32(&sh->full[stage]), 0);
+        if (rank == 0) mbar_arrive_expect_tx_elect(&sh->full[stage], 2 * PC::kTx);
+        tma_load_2d_pair_elect(buf, &m.a, kt * kBK, tm128 * kBM, bar);
+        tma_load_2d_pair_elect(buf + kABytes, &m.b, kt * kBK,
+                               (2 * tn + static_cast<int>(rank)) * 128, bar);
+        // a row tile's scale tiles of one stage are consecutive in global
+        // memory: A's kSfA as one box, both B halves' as one 3D box
+        uint8_t* sf = buf + kABytes + kPairBBytes;
+        tma_load_2d_pair_elect(sf, &m.sfa, 0, tm128 * g.kt * kSfA + kt * kSfA, bar);
+        tma_load_3d_pair_elect(sf + kSfA * kSfBytes, &m.sfb, 0, kt * kSfA, 2 * tn, bar);
+        if (++stage == kPairStages) { stage = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
@@ -736,10 +733,13 @@ lpfa_status pair_problem(const GemmArgs& g, const void* a8, const void* b8, cons
     if (st != LPFA_OK) return st;
   }
   {
-    uint64_t dims[2] = {128, (N / 128) * g.kt * sfa_tiles};
-    uint64_t strides[1] = {512};
-    uint32_t box[2] = {128, static_cast<uint32_t>(sfa_tiles)};
-    lpfa_status st = encode_tmap(&pm->sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, sfb_mma, dims,
+    // [N/128 row tiles][kt * sfa_tiles tiles][128 words]: both B halves of a
+    // stage in one box
+    const uint64_t tiles_k = static_cast<uint64_t>(g.kt) * sfa_tiles;
+    uint64_t dims[3] = {128, tiles_k, N / 128};
+    uint64_t strides[2] = {512, tiles_k * 512};
+    uint32_t box[3] = {128, static_cast<uint32_t>(sfa_tiles), 2};
+    lpfa_status st = encode_tmap(&pm->sfb, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, sfb_mma, dims,
                                  strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != LPFA_OK) return st;
   }

@@ -934,4 +934,24 @@ __device__ __forceinline__ void mma_pair_nvf4_ss_elect(uint32_t d_tmem, uint64_t
       : "memory");
 }
 
+// Elected-lane forms of the pair TMA loads (whole converged warp calls).
+__device__ __forceinline__ void tma_load_2d_pair_elect(void* smem_dst, const void* tmap, int32_t x,
+                                                       int32_t y, uint32_t bar_cluster) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_elect(void* smem_dst, const void* tmap, int32_t x,
+                                                       int32_t y, int32_t z, uint32_t bar_cluster) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t" LPFA_ELECT
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
 }  // namespace lpfa
