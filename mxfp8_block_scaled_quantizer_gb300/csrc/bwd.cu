@@ -333,40 +333,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int issued[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
-    for (int i = 0; i < nsteps; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (i / kStages) & 1;
-      ok = mbar_wait_sleep(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
-      if (!ok) break;
-      const int h = step_head(i), q0 = step_q0(i);
+    // seed rows of step j (stage s, phase ph) once its -log2 LSE and -D rows
+    // have landed: -LSE_q / c = -log2LSE_q / c2 and -D_q, each as a bf16
+    // pair hi + lo (hi = bf16(v), lo = bf16(v - hi): ~16 significant bits);
+    // then the second q_full arrival (also on abort, so that the phase can
+    // still complete once the copies land)
+    auto build_seed = [&](int s, uint32_t ph) -> bool {
       uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-      uint64_t* bar = &bars->q_full[s];
-      mbar_arrive_expect_tx_elect(bar, 2 * kBQ * C::kRowB + (B16 ? 0 : 4 * 512));
-      const int32_t row_q = static_cast<int32_t>(w.start + q0);
-#pragma unroll
-      for (int c = 0; c < C::kNCh; ++c) {
-        const int32_t x = c * (C::kChunkB / C::kEl);
-        tma_load_3d_elect(st + C::kStQ + c * kBQ * C::kChunkB, &tma_q, x, h, row_q, bar);
-        tma_load_3d_elect(st + C::kStdO + c * kBQ * C::kChunkB, &tma_do, x, h, row_q, bar);
-      }
-      const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
-      if constexpr (!B16) {
-        const int64_t qsf = (pr / 128) * p.hq + h;
-        bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
-        bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
-        bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
-        bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
-      }
-      const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
-      uint64_t* lbar = &bars->lse_full[s];
-      mbar_arrive_expect_tx_elect(lbar, 2 * kBQ * 4);
-      bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, lbar);
-      bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, lbar);
-      issued[s] = static_cast<int>(ph);
-      // seed rows: -LSE_q / c = -log2LSE_q / c2 and -D_q, each as a bf16
-      // pair hi + lo (hi = bf16(v), lo = bf16(v - hi): ~16 significant bits)
-      ok = mbar_wait_sleep(lbar, ph, p.err, abort, 41);
-      if (ok) {
+      const bool lok = mbar_wait_sleep(&bars->lse_full[s], ph, p.err, abort, 41);
+      if (lok) {
         const float* nl = reinterpret_cast<const float*>(st + C::kStLse);
         const float* nd = reinterpret_cast<const float*>(st + C::kStDelta);
         uint8_t* seed = st + C::kStSeed;
@@ -387,10 +362,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      // second arrival (also on abort, so that the phase can still complete
-      // once the copies land)
-      if (lane == 0) mbar_arrive(bar);
-      if (!ok) break;
+      if (lane == 0) mbar_arrive(&bars->q_full[s]);
+      return lok;
+    };
+    // With a deep ring, step i's loads are issued before step i-1's seed is
+    // built, so the wait for step i-1's LSE rows (a full memory round trip)
+    // overlaps step i's copies instead of delaying them; step i's stage was
+    // freed kStages - 1 steps earlier, so the seed is not held back.  A
+    // shallow ring (the bf16 variant) builds each seed right after its loads.
+    constexpr int kLag = kStages >= 4 ? 1 : 0;
+    for (int i = 0; i < nsteps + kLag; ++i) {
+      if (i < nsteps) {
+        const int s = i % kStages;
+        const uint32_t ph = (i / kStages) & 1;
+        ok = mbar_wait_sleep(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
+        if (!ok) {
+          if (kLag > 0 && i > 0) build_seed((i - 1) % kStages, ((i - 1) / kStages) & 1);
+          break;
+        }
+        const int h = step_head(i), q0 = step_q0(i);
+        uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
+        uint64_t* bar = &bars->q_full[s];
+        mbar_arrive_expect_tx_elect(bar, 2 * kBQ * C::kRowB + (B16 ? 0 : 4 * 512));
+        const int32_t row_q = static_cast<int32_t>(w.start + q0);
+#pragma unroll
+        for (int c = 0; c < C::kNCh; ++c) {
+          const int32_t x = c * (C::kChunkB / C::kEl);
+          tma_load_3d_elect(st + C::kStQ + c * kBQ * C::kChunkB, &tma_q, x, h, row_q, bar);
+          tma_load_3d_elect(st + C::kStdO + c * kBQ * C::kChunkB, &tma_do, x, h, row_q, bar);
+        }
+        const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
+        if constexpr (!B16) {
+          const int64_t qsf = (pr / 128) * p.hq + h;
+          bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
+          bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
+          bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
+          bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
+        }
+        const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
+        uint64_t* lbar = &bars->lse_full[s];
+        mbar_arrive_expect_tx_elect(lbar, 2 * kBQ * 4);
+        bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, lbar);
+        bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, lbar);
+        issued[s] = static_cast<int>(ph);
+      }
+      const int j = i - kLag;                      // the step whose seed is built now
+      if (j >= 0) {
+        ok = build_seed(j % kStages, (j / kStages) & 1);
+        if (!ok) {
+          if (kLag > 0 && i < nsteps) build_seed(i % kStages, (i / kStages) & 1);
+          break;
+        }
+      }
     }
     if (!ok) {
       for (int s = 0; s < kStages; ++s)
