@@ -1,27 +1,33 @@
-// Block-scaled MXFP8 GEMM on tcgen05: D[M,N] (fp32) = A[M,K] * B[N,K]^T.
+// Block-scaled GEMM on tcgen05: D[M,N] (fp32) = A[M,K] * B[N,K]^T, MXFP8 and
+// the other MX / NV element formats.
 //
 // Purpose: the dense MX MMA rate of this GPU, measured in the same run as the
 // attention kernels ("Low Precision Flash Attention 4 ...", paragraph 2:
-// tcgen05.mma.block_scale on MXFP8 operands), and the bring-up of the
-// descriptors, TMEM scale layout and pipelines the attention kernels reuse.
+// tcgen05.mma.block_scale on MXFP8, MXFP6, MXFP4 and NVFP4 operands), the
+// GEMM + Quantize producer of the same paragraph, and the two backward GEMMs
+// of the GEMM-Norm backward (paragraph 4).
 //
-// Design (one CTA per SM, persistent over 128x256 output tiles):
+// Two kernels:
+//   mx_gemm_pair_kernel   256x256 tiles on CTA pairs (cta_group::2; below),
+//                         every kind, one or two problems per launch;
+//   mx_gemm_kernel        128x256 tiles, one CTA each: the quantizing
+//                         epilogue when M % 256 == 128.
+// One-CTA design (persistent, one CTA per SM):
 //   warp 0      TMA producer: A tile 128x128 B, B tile 256x128 B (128-byte
 //               swizzle, K-major) + three 512-byte scale tiles per stage.
 //   warp 1      TMEM allocator and MMA issuer: per stage copies the scale
 //               tiles into TMEM (tcgen05.cp) and issues 4 MMAs of K = 32.
 //   warps 2-9   epilogue: two warps per TMEM lane quarter, one per column
 //               half; each reads its 32 rows x 128 columns in four loads and
-//               one wait and releases the accumulator before its fp32 global
+//               one wait and releases the accumulator before its global
 //               stores, so the next tile's main loop overlaps them.
 //
-// Quantizing epilogue (lpfa_mx_gemm_quantize; the fused GEMM+Quantize
-// producer of "Low Precision Flash Attention 4 ...", paragraph 2): the fp32
-// tile is quantized in registers to E4M3 with E8M0 scales, in 1x32 blocks
-// along N (a thread's 32 columns of one row) or 32x32 blocks (a warp's 32
-// rows x 32 columns, maximum by redux.sync), with the scales written in the
-// compact layout and as the next GEMM's operand: rows = M (contraction over
-// N) and, for square blocks, rows = N (contraction over M).
+// Quantizing epilogue (lpfa_mx_gemm_quantize): the fp32 tile is quantized in
+// registers to E4M3 with E8M0 scales, in 1x32 blocks along N (a thread's 32
+// columns of one row) or 32x32 blocks (a warp's 32 rows x 32 columns, maximum
+// by redux.sync), with the scales written in the compact layout and as the
+// next GEMM's operand: rows = M (contraction over N) and, for square blocks,
+// rows = N (contraction over M).
 #include <cuda_runtime.h>
 
 #include <algorithm>
