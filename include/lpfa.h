@@ -227,7 +227,8 @@ lpfa_status lpfa_rmsnorm_mx_quantize(const lpfa_seqs* seqs, const void* x,
  * [M/128][K/128][512] and [N/128][K/128][512] bytes (tile (i, kt) holds rows
  * 128i.. and contraction blocks 4kt..4kt+3).  N a multiple of 256, K of 128;
  * M any positive value (rows past M read as zeros and are not stored; the A
- * scales then hold ceil(M/128) row tiles).  Persistent kernel, one CTA per SM.
+ * scales then hold ceil(M/128) row tiles).  Persistent kernel on CTA pairs
+ * (clusters of two; 256 x 256 output tiles, one CTA pair per two SMs).
  * ---------------------------------------------------------------------- */
 lpfa_status lpfa_mx_gemm(const void* a8, const void* sfa_mma, const void* b8,
                          const void* sfb_mma, float* d, int64_t M, int64_t N,
@@ -380,7 +381,7 @@ lpfa_status lpfa_mma_peak(double* flops_per_s, void* stream);
  * Block-scaled MXFP8 GEMM with a quantizing epilogue ([P1] paragraph 2:
  * fused GEMM+Quantize kernels producing FP8 output with dual scale factor
  * layouts in one pass).  The fp32 result D = A * B^T (operands and
- * constraints as lpfa_mx_gemm; N a multiple of 256) is quantized in
+ * constraints as lpfa_mx_gemm, with M a multiple of 128) is quantized in
  * registers with the quantizer's rule (lpfa_mx_quantize) before it leaves
  * the SM:
  *   blk = LPFA_BLK_1X32   32 consecutive columns of one row;
