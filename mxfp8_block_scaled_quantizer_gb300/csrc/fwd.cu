@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
                               (!first) || (kb > 0));
         }
         tc_commit_elect(&bars->pv_done);
+        // the tile's K / V stage is free once PV_g (and, before it in the
+        // pipe, S_g) has completed
+        tc_commit_elect(&bars->kv_empty[s]);
         return true;
       };
       for (int r = 0; ok; ++r) {
@@ -619,8 +622,6 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
           ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 31, p.wait_ns);
           if (!ok) break;
           tc_fence_after();
-          // the previous tile's S and PV are done: its K/V stage may be refilled
-          if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
         }
         if constexpr (kPW == 32) tmem_st32(tmem + kColP + kPW * wg + lane_base, pw);
         else tmem_st16(tmem + kColP + kPW * wg + lane_base, pw);
@@ -668,8 +669,6 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
       ok = mbar_wait_sleep(&bars->pv_done, (gt - 1) & 1, p.err, abort, 32, p.wait_ns);
       if (!ok) break;
       tc_fence_after();
-      // the item's last S and PV are done: its K/V stage may be refilled
-      if (warp == 2 && lane == 0) mbar_arrive(&bars->kv_empty[(gt - 1) % kStages]);
       // the row's sum over the warpgroups in a fixed order (every warpgroup
       // scales its O columns by the same 1 / l)
       float lt = 0.f;
