@@ -46,6 +46,7 @@ namespace {
 constexpr int kBN = 128;         // keys per CTA
 constexpr int kBQ = 64;          // queries per step
 constexpr int kThreads = 320;
+constexpr int kLseSlotsMax = 4;  // LSE / D row slots (see BwdCfg::kLseSlots)
 constexpr int kTmemCols = 512;
 
 // Layout for head_dim D (64 or 128).  B16 selects the bf16 variant (kind::f16
@@ -62,6 +63,17 @@ struct BwdCfg {
   static constexpr uint32_t kSw = kChunkB == 128 ? 2u : 4u;   // 128B / 64B swizzle
   static constexpr uint32_t kSbo = 8 * kChunkB;               // 8 rows of a chunk
   static constexpr int kStages = B16 ? 3 : 5;   // Q / dO ring: loads run steps ahead
+  // The producer builds a step's accumulator seed kLag steps after issuing
+  // its copies from -log2 LSE / -D rows requested kLseAhead steps before
+  // the copies (measured: the deep MXFP8 ring is fastest with the rows
+  // requested beside the copies and the seed one step behind, the shallow
+  // bf16 ring with the rows two steps ahead and no lag).  A slot is refilled
+  // kLseSlots steps after its previous fill, by which time that fill's seed
+  // must have been built: kLseSlots >= kLseAhead + kLag + 1.
+  static constexpr int kLag = kStages >= 4 ? 1 : 0;
+  static constexpr int kLseAhead = kStages >= 4 ? 0 : 2;
+  static constexpr int kLseSlots = kLseAhead + kLag + 1;
+  static_assert(kLseSlots <= kLseSlotsMax, "LSE slots");
   static constexpr int kDqBufs = B16 ? 2 : 4;   // dQ staging tiles per compute warp
   static constexpr int kKSteps = kRowB / 32;    // MMA K-steps over head_dim (32 bytes each)
   static constexpr int kQPerStep = 32 / kEl;    // queries / keys contracted per MMA
@@ -87,15 +99,13 @@ struct BwdCfg {
   // zeros that are never read back); otherwise the K tile itself
   static constexpr int kSmKT = kSmV + kBN * kRowB;
   static constexpr int kKTBytes = kRowB == 64 ? kBN * 128 : 0;
-  static constexpr int kSmStage0 = kSmKT + kKTBytes;              // Q, dO, SFs, LSE2, Delta
+  static constexpr int kSmStage0 = kSmKT + kKTBytes;              // Q, dO, SFs, seed
   static constexpr int kStQ = 0;
   static constexpr int kStdO = kBQ * kRowB;
   static constexpr int kStSF = 2 * kBQ * kRowB;                   // SFQ, SFQt, SFdO, SFdOt
-  static constexpr int kStLse = kStSF + (B16 ? 0 : 4 * 512);      // 64 floats
-  static constexpr int kStDelta = kStLse + kBQ * 4;               // 64 floats
   // accumulator seeds: [64 queries][16 bf16] K-major, 32-byte swizzle; row q
   // holds hi, lo of -LSE_q / c (k = 0, 1) and of -D_q (k = 2, 3)
-  static constexpr int kStSeed = ((kStDelta + kBQ * 4) + 255) / 256 * 256;
+  static constexpr int kStSeed = ((kStSF + (B16 ? 0 : 4 * 512)) + 255) / 256 * 256;
   static constexpr int kStageBytes = ((kStSeed + kBQ * 32) + 1023) / 1024 * 1024;
   // dS^T tile [128 keys][64 queries]: 64-byte rows, 64B swizzle (fp8) or
   // 128-byte rows, 128B swizzle (bf16)
@@ -106,7 +116,10 @@ struct BwdCfg {
   static constexpr int kSmSFkv = kSmSFdS + 512;                   // SFK, SFKt, SFV
   // dQ staging: per compute warp kDqBufs [32 queries][32 channels] fp16
   // tiles, 64-byte rows, 64B swizzle (2 KB each, 1024-aligned)
-  static constexpr int kSmDQ = (kSmSFkv + 3 * 512 + 1023) / 1024 * 1024;
+  // -log2 LSE and -D rows of a step (64 + 64 floats), kLseSlots of them
+  static constexpr int kLseSlotB = 2 * kBQ * 4;
+  static constexpr int kSmLse = kSmSFkv + 3 * 512;
+  static constexpr int kSmDQ = (kSmLse + kLseSlots * kLseSlotB + 1023) / 1024 * 1024;
   static constexpr int kSmBar = kSmDQ + 8 * kDqBufs * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
 };
@@ -138,7 +151,7 @@ struct BwdBars {
   uint64_t kv_full;
   uint64_t q_full[kStages];    // Q, dO, scales landed and the seed tile written
   uint64_t q_empty[kStages];
-  uint64_t lse_full[kStages];  // the stage's -log2 LSE and -D rows landed
+  uint64_t lse_full[kLseSlotsMax];  // a slot's -log2 LSE and -D rows landed
   uint64_t st_ready;
   uint64_t ds_ready;
   uint64_t dq_full;
@@ -253,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->q_full[s], 2);
       mbar_init(&bars->q_empty[s], 1);
+    }
+    for (int s = 0; s < C::kLseSlots; ++s) {
       mbar_init(&bars->lse_full[s], 1);
     }
     mbar_init(&bars->st_ready, 1);
@@ -333,18 +348,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int issued[kStages];
     for (int s = 0; s < kStages; ++s) issued[s] = -1;
-    // seed rows of step j (stage s, phase ph) once its -log2 LSE and -D rows
-    // have landed: -LSE_q / c = -log2LSE_q / c2 and -D_q, each as a bf16
-    // pair hi + lo (hi = bf16(v), lo = bf16(v - hi): ~16 significant bits);
-    // then the second q_full arrival (also on abort, so that the phase can
-    // still complete once the copies land)
-    auto build_seed = [&](int s, uint32_t ph) -> bool {
-      uint8_t* st = sm + C::kSmStage0 + s * C::kStageBytes;
-      const bool lok = mbar_wait_sleep(&bars->lse_full[s], ph, p.err, abort, 41);
+    // The -log2 LSE and -D rows of a step run in a ring of their own,
+    // requested ahead of the step's copies, so that the seed (and with it
+    // the stage's q_full) does not wait a memory round trip behind them.
+    // Only this warp reads the ring: a slot is free again once its seed is
+    // built.
+    constexpr int kLseAhead = C::kLseAhead, kLseSlots = C::kLseSlots, kLag = C::kLag;
+    int lse_issued = 0, lse_used = 0;
+    auto issue_lse = [&](int j) {
+      const int slot = j % kLseSlots;
+      const int64_t pr = w.sf_tile0 * 128 + step_q0(j);      // padded row of the step
+      const int64_t rowoff = static_cast<int64_t>(step_head(j)) * p.seqs.total_sf_rows + pr;
+      uint8_t* dst = sm + C::kSmLse + slot * C::kLseSlotB;
+      mbar_arrive_expect_tx_elect(&bars->lse_full[slot], 2 * kBQ * 4);
+      bulk_load_elect(dst, p.lse2 + rowoff, kBQ * 4, &bars->lse_full[slot]);
+      bulk_load_elect(dst + kBQ * 4, p.delta + rowoff, kBQ * 4, &bars->lse_full[slot]);
+      ++lse_issued;
+    };
+    // seed rows of step j (stage s) once its rows have landed: -LSE_q / c =
+    // -log2LSE_q / c2 and -D_q, each as a bf16 pair hi + lo (hi = bf16(v),
+    // lo = bf16(v - hi): ~16 significant bits); then the second q_full
+    // arrival (also on abort, so that the phase can still complete once the
+    // copies land)
+    auto build_seed = [&](int j, int s) -> bool {
+      const int slot = j % kLseSlots;
+      const bool lok = mbar_wait_sleep(&bars->lse_full[slot], (j / kLseSlots) & 1, p.err, abort, 41);
       if (lok) {
-        const float* nl = reinterpret_cast<const float*>(st + C::kStLse);
-        const float* nd = reinterpret_cast<const float*>(st + C::kStDelta);
-        uint8_t* seed = st + C::kStSeed;
+        ++lse_used;
+        const float* nl = reinterpret_cast<const float*>(sm + C::kSmLse + slot * C::kLseSlotB);
+        const float* nd = nl + kBQ;
+        uint8_t* seed = sm + C::kSmStage0 + s * C::kStageBytes + C::kStSeed;
 #pragma unroll
         for (int k = 0; k < kBQ / 32; ++k) {
           const int r = lane + 32 * k;
@@ -365,19 +398,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&bars->q_full[s]);
       return lok;
     };
-    // With a deep ring, step i's loads are issued before step i-1's seed is
-    // built, so the wait for step i-1's LSE rows (a full memory round trip)
-    // overlaps step i's copies instead of delaying them; step i's stage was
-    // freed kStages - 1 steps earlier, so the seed is not held back.  A
-    // shallow ring (the bf16 variant) builds each seed right after its loads.
-    constexpr int kLag = kStages >= 4 ? 1 : 0;
+    for (int j = 0; j < kLseAhead && j < nsteps; ++j) issue_lse(j);
     for (int i = 0; i < nsteps + kLag; ++i) {
       if (i < nsteps) {
         const int s = i % kStages;
         const uint32_t ph = (i / kStages) & 1;
         ok = mbar_wait_sleep(&bars->q_empty[s], ph ^ 1, p.err, abort, 40);
         if (!ok) {
-          if (kLag > 0 && i > 0) build_seed((i - 1) % kStages, ((i - 1) / kStages) & 1);
+          // the pending seed still arrives on its stage's q_full
+          if (kLag > 0 && i > 0) build_seed(i - 1, (i - 1) % kStages);
           break;
         }
         const int h = step_head(i), q0 = step_q0(i);
@@ -391,36 +420,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_elect(st + C::kStQ + c * kBQ * C::kChunkB, &tma_q, x, h, row_q, bar);
           tma_load_3d_elect(st + C::kStdO + c * kBQ * C::kChunkB, &tma_do, x, h, row_q, bar);
         }
-        const int64_t pr = w.sf_tile0 * 128 + q0;        // padded row of q0
         if constexpr (!B16) {
-          const int64_t qsf = (pr / 128) * p.hq + h;
+          const int64_t qsf = ((w.sf_tile0 * 128 + q0) / 128) * p.hq + h;
           bulk_load_elect(st + C::kStSF + 0 * 512, p.sfq + qsf * 512, 512, bar);
           bulk_load_elect(st + C::kStSF + 1 * 512, p.sfq_t + qsf * 512, 512, bar);
           bulk_load_elect(st + C::kStSF + 2 * 512, p.sfdo + qsf * 512, 512, bar);
           bulk_load_elect(st + C::kStSF + 3 * 512, p.sfdo_t + qsf * 512, 512, bar);
         }
-        const int64_t rowoff = static_cast<int64_t>(h) * p.seqs.total_sf_rows + pr;
-        uint64_t* lbar = &bars->lse_full[s];
-        mbar_arrive_expect_tx_elect(lbar, 2 * kBQ * 4);
-        bulk_load_elect(st + C::kStLse, p.lse2 + rowoff, kBQ * 4, lbar);
-        bulk_load_elect(st + C::kStDelta, p.delta + rowoff, kBQ * 4, lbar);
         issued[s] = static_cast<int>(ph);
+        if (i + kLseAhead < nsteps) issue_lse(i + kLseAhead);
       }
       const int j = i - kLag;                      // the step whose seed is built now
       if (j >= 0) {
-        ok = build_seed(j % kStages, (j / kStages) & 1);
+        ok = build_seed(j, j % kStages);
         if (!ok) {
-          if (kLag > 0 && i < nsteps) build_seed(i % kStages, (i / kStages) & 1);
+          if (kLag > 0 && i < nsteps) build_seed(i, i % kStages);
           break;
         }
       }
     }
     if (!ok) {
+      // let every copy still in flight land before the CTA exits
       for (int s = 0; s < kStages; ++s)
-        if (issued[s] >= 0) {
-          mbar_wait_sleep(&bars->lse_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
+        if (issued[s] >= 0)
           mbar_wait_sleep(&bars->q_full[s], static_cast<uint32_t>(issued[s]), nullptr, nullptr, 0);
-        }
+      for (int j = lse_used; j < lse_issued; ++j)
+        mbar_wait_sleep(&bars->lse_full[j % kLseSlots], (j / kLseSlots) & 1, nullptr, nullptr, 0);
       mbar_wait_sleep(&bars->kv_full, 0, nullptr, nullptr, 0);
     }
   } else if (warp == 1) {
