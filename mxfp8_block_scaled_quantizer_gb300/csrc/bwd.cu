@@ -30,7 +30,7 @@
 // soon as step i's rows are in registers, and a warpgroup reads back dQ^T of
 // step i-1 after computing step i, so the MMAs of one step overlap the
 // elementwise work of the next.
-//   [448,512) scale factors and the seed MMAs' constant A tiles (kCol* below)
+//   [448,512) scale factors and the seed MMA's constant A tile (kCol* below)
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -88,9 +88,9 @@ struct BwdCfg {
                             kColSFdO = kColSF + 16, kColSFQt = kColSF + 20,
                             kColSFdOt = kColSF + 24, kColSFP = kColSF + 28 /* +4g */,
                             kColSFdS = kColSF + 36 /* +4g */, kColSFdSB = kColSF + 44;
-  // constant A operands of the seed MMAs: [128 keys][16 bf16], 8 columns
-  // each, 1.0 at k = 0, 1 (selects the LSE pair) and at k = 2, 3 (D pair)
-  static constexpr uint32_t kColOnesL = kColSF + 48, kColOnesD = kColSF + 56;
+  // constant A operand of the seed MMA: [128 keys][16 bf16], 8 columns,
+  // 1.0 at k = 0, 1 (selects the hi, lo pair of a seed row)
+  static constexpr uint32_t kColOnes = kColSF + 48;
   // shared memory (bytes from a 1024-aligned base)
   static constexpr int kSmK = 0;                                  // 128 x D
   static constexpr int kSmV = (kBN * kRowB + 1023) / 1024 * 1024; // 128 x D
@@ -103,10 +103,12 @@ struct BwdCfg {
   static constexpr int kStQ = 0;
   static constexpr int kStdO = kBQ * kRowB;
   static constexpr int kStSF = 2 * kBQ * kRowB;                   // SFQ, SFQt, SFdO, SFdOt
-  // accumulator seeds: [64 queries][16 bf16] K-major, 32-byte swizzle; row q
-  // holds hi, lo of -LSE_q / c (k = 0, 1) and of -D_q (k = 2, 3)
+  // accumulator seeds: [128 rows][16 bf16] K-major, 32-byte swizzle; row q
+  // holds hi, lo of -LSE_q / c and row 64 + q those of -D_q (k = 0, 1), so
+  // that one N = 128 MMA seeds the adjacent S^T and dP^T columns
   static constexpr int kStSeed = ((kStSF + (B16 ? 0 : 4 * 512)) + 255) / 256 * 256;
-  static constexpr int kStageBytes = ((kStSeed + kBQ * 32) + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = ((kStSeed + 2 * kBQ * 32) + 1023) / 1024 * 1024;
+  static_assert(kColDP == kColS + kBQ, "the seed MMA spans S^T and dP^T");
   // dS^T tile [128 keys][64 queries]: 64-byte rows, 64B swizzle (fp8) or
   // 128-byte rows, 128B swizzle (bf16)
   static constexpr int kDsRowB = kBQ * kEl;
@@ -122,6 +124,7 @@ struct BwdCfg {
   static constexpr int kSmDQ = (kSmLse + kLseSlots * kLseSlotB + 1023) / 1024 * 1024;
   static constexpr int kSmBar = kSmDQ + 8 * kDqBufs * 32 * 32 * 2;
   static constexpr int kSmTotal = kSmBar + 256;
+  static_assert(kSmTotal + 1024 <= 227 * 1024, "shared memory per CTA");
 };
 
 struct BwdParams {
@@ -288,14 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  // the seed MMAs' constant A operands (one warpgroup covers the 128 lanes)
+  // the seed MMA's constant A operand (one warpgroup covers the 128 lanes)
   if (warp >= 2 && warp < 6) {
     const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t one2 = 0x3F803F80u;   // bf16 pair (1.0, 1.0)
     const uint32_t ol[8] = {one2, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    const uint32_t od[8] = {0u, one2, 0u, 0u, 0u, 0u, 0u, 0u};
-    tmem_st8(tmem + lanes + C::kColOnesL, ol);
-    tmem_st8(tmem + lanes + C::kColOnesD, od);
+    tmem_st8(tmem + lanes + C::kColOnes, ol);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       for (int st = 0; st < kStages; ++st) {
         uint32_t* seed = reinterpret_cast<uint32_t*>(sm + C::kSmStage0 + st * C::kStageBytes + C::kStSeed);
-        for (int i = lane; i < kBQ * 8; i += 32) seed[i] = 0u;
+        for (int i = lane; i < 2 * kBQ * 8; i += 32) seed[i] = 0u;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -390,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                               (static_cast<uint32_t>(__bfloat16_as_ushort(ll)) << 16);
           const uint32_t w1 = static_cast<uint32_t>(__bfloat16_as_ushort(hd)) |
                               (static_cast<uint32_t>(__bfloat16_as_ushort(ld)) << 16);
-          *reinterpret_cast<uint2*>(seed + r * 32 + ((r >> 2) & 1) * 16) = make_uint2(w0, w1);
+          // k = 0, 1 of rows r and 64 + r (same swizzle phase: 64 is a
+          // multiple of 8 rows)
+          *reinterpret_cast<uint32_t*>(seed + r * 32 + ((r >> 2) & 1) * 16) = w0;
+          *reinterpret_cast<uint32_t*>(seed + (kBQ + r) * 32 + ((r >> 2) & 1) * 16) = w1;
         }
         fence_proxy_async_smem();
       }
@@ -475,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dq_ = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStQ), kQLbo, C::kSbo, C::kSw);
     const uint64_t ddo = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStdO), kQLbo, C::kSbo, C::kSw);
     const uint64_t dsf = sf_tile_desc(smem_u32(sm + C::kSmStage0 + C::kStSF));
-    // seed MMAs (bf16, K = 16): S^T <- -LSE / c, dP^T <- -D, broadcast over keys
-    constexpr uint32_t id_seed = idesc_bf16(128, kBQ, 0, 0);
+    // seed MMA (bf16, K = 16, N = 128 over S^T and dP^T)
+    constexpr uint32_t id_seed = idesc_bf16(128, 2 * kBQ, 0, 0);
     const uint64_t dseed = make_sdesc(smem_u32(sm + C::kSmStage0 + C::kStSeed), 16, 256, 6);
     const uint64_t dsfds = sf_tile_desc(smem_u32(sm + C::kSmSFdS));
     bool ok = mbar_wait_sleep(&bars->kv_full, 0, p.err, abort, 50);
@@ -498,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_cp_32x128b_warpx4_elect(tmem + C::kColSFQ, dsf + so);
         tc_cp_32x128b_warpx4_elect(tmem + C::kColSFdO, dsf + so + (1024 >> 4));
       }
-      mma_bf16_ts_elect(tmem + C::kColS, tmem + C::kColOnesL, dseed + so, id_seed, 0);
+      // S^T <- -LSE / c and dP^T <- -D, broadcast over keys, in one MMA
+      mma_bf16_ts_elect(tmem + C::kColS, tmem + C::kColOnes, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < C::kKSteps; ++kb) {
         const uint64_t ka = kstep_off<C::kChunkB>(kb, kBN), kq = kstep_off<C::kChunkB>(kb, kBQ);
@@ -509,7 +514,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             idesc_sf_ids(id_st, kb, kb), tmem + C::kColSFK,
                             tmem + C::kColSFQ + 2 * half, 1);
       }
-      mma_bf16_ts_elect(tmem + C::kColDP, tmem + C::kColOnesD, dseed + so, id_seed, 0);
 #pragma unroll
       for (int kb = 0; kb < C::kKSteps; ++kb) {
         const uint64_t ka = kstep_off<C::kChunkB>(kb, kBN), kq = kstep_off<C::kChunkB>(kb, kBQ);
