@@ -31,6 +31,9 @@
 //              keys [128,256); thread = query row = TMEM lane.  The two
 //              threads of a row exchange their partial maxima (and, at the
 //              end, their partial sums) through shared memory.
+// The bf16 forward (fwd_pair.cu) keeps two query tiles in flight instead;
+// for MXFP8 that structure leaves room in TMEM only for 64-key tiles beside
+// the scale factors and measured slower (2.86 against 2.67 ms).
 //
 // Pipeline.  S has its own 256 columns and P its own 64, so S_{j+1} = Q
 // K_{j+1}^T is issued as soon as the softmax has the row of S_j in
@@ -80,16 +83,13 @@ struct FwdParams {
                         // (-1 normally), so the waits on it must expire
 };
 
-// Tile plan for head_dim D; B16 selects the bf16 variant (kind::f16 MMAs on
-// bf16 operands, no scale factors), which exists to measure the MXFP8 kernel
-// against the same algorithm in bf16.  Operand tiles are stored as chunks of
-// at most 128 bytes per row (one swizzle span): a bf16 row of 128 channels
-// is two chunks, [chunk][rows][128 B].
-template <int D, bool B16>
+// Tile plan for head_dim D.  Operand tiles are stored as chunks of at most
+// 128 bytes per row (one swizzle span).
+template <int D>
 struct FwdCfg {
-  static constexpr int kN = B16 ? 128 : 256;              // keys per tile
+  static constexpr int kN = 256;                          // keys per tile
   // softmax warpgroups: each takes kWgN keys of every tile (all 128 query
-  // rows, one per thread): 2 x 128 keys (MXFP8), 2 x 64 keys (bf16).  Four
+  // rows, one per thread): 2 x 128 keys.  Four
   // warpgroups of 64 keys (608 threads, 96 registers) were measured slower
   // on the llm workload (2.88 against 2.73 ms): the four-way row-maximum
   // exchange and the 16-warp barriers cost more than the shorter chains gain.
@@ -99,13 +99,13 @@ struct FwdCfg {
   static constexpr int kThreads = (3 + 4 * kWG) * 32;     // producer, S issuer, softmax, PV issuer
   static constexpr int kPvWarp = 2 + 4 * kWG;
   static constexpr uint32_t kColSFV = kColSFP + 4 * kWG;  // one 4-column SFP group per warpgroup
-  static constexpr int kEl = B16 ? 2 : 1;                 // bytes per element
+  static constexpr int kEl = 1;                           // bytes per element
   static constexpr int kRowB = D * kEl;                   // bytes per token row
   static constexpr int kChunkB = kRowB < 128 ? kRowB : 128;
   static constexpr int kNCh = kRowB / kChunkB;            // chunks per row
   static constexpr uint32_t kSw = kChunkB == 128 ? 2u : 4u;   // 128B / 64B swizzle
   static constexpr uint32_t kSbo = 8 * kChunkB;               // 8 rows of a chunk
-  static constexpr int kStages = D == 128 ? (B16 ? 2 : 3) : 4;
+  static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kQBytes = kBlockM * kRowB;
   static constexpr int kKVBytes = kN * kRowB;             // one of K, V
   static constexpr int kQ = 0;
@@ -113,12 +113,12 @@ struct FwdCfg {
   static constexpr int kStageBytes = 2 * kKVBytes;
   static constexpr int kSfQ = kStage0 + kStages * kStageBytes;
   static constexpr int kSfStage0 = kSfQ + 512;            // SFK[2], SFV[2]
-  static constexpr int kSfStageBytes = B16 ? 0 : 2048;
+  static constexpr int kSfStageBytes = 2048;
   static constexpr int kXMax = kSfStage0 + kStages * kSfStageBytes;  // float [2][kWG][128]
   static constexpr int kXSum = kXMax + 2 * kWG * 128 * 4;   // float [kWG][128]
   static constexpr int kBar = kXSum + kWG * 128 * 4;
   static constexpr int kTotal = kBar + 256;
-  // one MMA instruction contracts 32 bytes of K (32 fp8 or 16 bf16 elements)
+  // one MMA instruction contracts 32 bytes of K (32 fp8 elements)
   static constexpr int kKStepsS = kRowB / 32;             // S = Q K^T over head_dim
   static constexpr int kKStepsPV = kN * kEl / 32;         // O += P V over the tile's keys
   static constexpr int kKeysPerStep = 32 / kEl;
@@ -223,13 +223,13 @@ __device__ __forceinline__ constexpr uint64_t kstep_off(int kb, int rows) {
                                (kb % (kChunkB / 32)) * 32) >> 4;
 }
 
-template <int D, bool B16>
-__global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
+template <int D>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mx_attn_fwd_kernel(const __grid_constant__ CUtensorMap tma_q,
                        const __grid_constant__ CUtensorMap tma_k,
                        const __grid_constant__ CUtensorMap tma_v,
                        const FwdParams p) {
-  using C = FwdCfg<D, B16>;
+  using C = FwdCfg<D>;
   constexpr int kStages = C::kStages;
   constexpr int kBlockN = C::kN;
   constexpr int kWG = C::kWG;
@@ -302,14 +302,13 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11, p.wait_ns);
         if (!ok) break;
       }
-      mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + (B16 ? 0 : 512));
+      mbar_arrive_expect_tx_elect(&bars->q_full, C::kQBytes + 512);
 #pragma unroll
       for (int c = 0; c < C::kNCh; ++c)
         tma_load_3d_elect(sm + C::kQ + c * kBlockM * C::kChunkB, &tma_q,
                           c * (C::kChunkB / C::kEl), w.head,
                           static_cast<int32_t>(w.start + q0), &bars->q_full);
-      if constexpr (!B16)
-        bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
+      bulk_load_elect(sm + C::kSfQ, p.sfq + (w.sf_tile * p.hq + w.head) * 512, 512,
                         &bars->q_full);
       q_issued = k & 1;
       ++k;
@@ -334,7 +333,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
           tma_load_3d_elect(kbuf + C::kKVBytes + c * kBlockN * C::kChunkB, &tma_v, x, kvh,
                             row_k, bar);
         }
-        if constexpr (!B16) {
+        {
           uint8_t* sfb = sm + C::kSfStage0 + s * 2048;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -371,8 +370,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
     bool ok = true;
     int gt = 0, k = 0;
     if (warp == 1) {
-      constexpr uint32_t idesc_s = B16 ? idesc_bf16(kBlockM, kBlockN, 0, 0)
-                                       : idesc_mxf8(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t idesc_s = idesc_mxf8(kBlockM, kBlockN, 0, 0);
       const uint64_t dq = make_sdesc(smem_u32(sm + C::kQ), 16, kSbo, kSw);
       const uint64_t dk = make_sdesc(smem_u32(sm + C::kStage0), 16, kSbo, kSw);
       const uint32_t tS = tmem + kColS, tSFQ = tmem + kColSFQ, tSFK = tmem + kColSFK;
@@ -385,12 +383,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         if (!mbar_wait_sleep(&bars->kv_full[s], (g / kStages) & 1, p.err, abort, 21, p.wait_ns)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(s) * (C::kStageBytes >> 4);
-        if constexpr (B16) {
-#pragma unroll
-          for (int kb = 0; kb < C::kKStepsS; ++kb)
-            mma_bf16_ss_elect(tS, dq + kstep_off<C::kChunkB>(kb, kBlockM),
-                              dk + so + kstep_off<C::kChunkB>(kb, kBlockN), idesc_s, kb > 0);
-        } else {
+        {
           const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
           tc_cp_32x128b_warpx4_elect(tSFK, dsf + fo);
           tc_cp_32x128b_warpx4_elect(tSFK + 4, dsf + fo + (512 >> 4));
@@ -412,7 +405,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         ok = mbar_wait_sleep(&bars->q_full, k & 1, p.err, abort, 20, p.wait_ns);
         if (!ok) break;
         tc_fence_after();
-        if constexpr (!B16) tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
+        tc_cp_32x128b_warpx4_elect(tSFQ, sf_tile_desc(smem_u32(sm + C::kSfQ)));
         for (int j = 0; j < ntiles && ok; ++j, ++gt) ok = issue_s(gt);
         // the item's last reader of the Q tile is issued: the tile is free
         // once it completes
@@ -420,8 +413,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         ++k;
       }
     } else {
-      constexpr uint32_t idesc_o = B16 ? idesc_bf16(kBlockM, D, 0, 1)
-                                       : idesc_mxf8(kBlockM, D, 0, 1);
+      constexpr uint32_t idesc_o = idesc_mxf8(kBlockM, D, 0, 1);
       // V is MN-major (channels contiguous); a row of several 128-byte chunks
       // repeats the swizzle pattern along N every chunk (the leading offset)
       const uint64_t dv = make_sdesc(smem_u32(sm + C::kStage0 + C::kKVBytes),
@@ -441,12 +433,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         // K-step kb: P columns 8 kb (32 bytes of keys per lane), V rows
         // kKeysPerStep * kb of every chunk
         constexpr uint64_t kVStep = (C::kKeysPerStep * C::kChunkB) >> 4;
-        if constexpr (B16) {
-#pragma unroll
-          for (int kb = 0; kb < C::kKStepsPV; ++kb)
-            mma_bf16_ts_elect(tO, tP + 8 * kb, dv + so + kb * kVStep, idesc_o,
-                              (!first) || (kb > 0));
-        } else {
+        {
           const uint64_t fo = static_cast<uint64_t>(s) * (2048 >> 4);
           tc_cp_32x128b_warpx4_elect(tSFV, dsf + fo + (1024 >> 4));
           tc_cp_32x128b_warpx4_elect(tSFV + 4, dsf + fo + (1536 >> 4));
@@ -556,33 +543,11 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         const bool moved = (m_new != m_ref);
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
         const float alpha = (moved && m_ref != -INFINITY) ? ex2(m_ref - m_new) : 1.f;
-        constexpr int kPW = B16 ? 16 * kCh : 8 * kCh;   // P words of this warpgroup's keys
+        constexpr int kPW = 8 * kCh;                   // P words of this warpgroup's keys
         uint32_t pw[kPW];
         float lsum = 0.f;
         uint32_t sfp = 0;
-        if constexpr (B16) {
-          // P = 2^(s*c2 - m) rounded to bf16 for the PV MMA; l sums the fp32
-          // values
-          const uint64_t nb2 = pack2(-m_use, -m_use);
-          uint64_t acc = 0;
-#pragma unroll
-          for (int c = 0; c < kCh; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < 32; kk += 4) {
-              const uint64_t x0 = fma2(pack2(__uint_as_float(sv[c][kk]), __uint_as_float(sv[c][kk + 1])), c2x2, nb2);
-              const uint64_t x1 = fma2(pack2(__uint_as_float(sv[c][kk + 2]), __uint_as_float(sv[c][kk + 3])), c2x2, nb2);
-              const float p0 = ex2(lo2(x0)), p1 = ex2(hi2(x0));
-              const float p2 = ex2(lo2(x1)), p3 = ex2(hi2(x1));
-              acc = add2(acc, pack2(p0, p1));
-              acc = add2(acc, pack2(p2, p3));
-              const __nv_bfloat162 b0 = __floats2bfloat162_rn(p0, p1);
-              const __nv_bfloat162 b1 = __floats2bfloat162_rn(p2, p3);
-              pw[16 * c + kk / 2] = *reinterpret_cast<const uint32_t*>(&b0);
-              pw[16 * c + kk / 2 + 1] = *reinterpret_cast<const uint32_t*>(&b1);
-            }
-          }
-          lsum = lo2(acc) + hi2(acc);
-        } else {
+        {
           // per-block scale codes: the exact decision 2^(fl(cmax*c2) - m)
           uint32_t code[kCh];
 #pragma unroll
@@ -625,7 +590,7 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
         }
         if constexpr (kPW == 32) tmem_st32(tmem + kColP + kPW * wg + lane_base, pw);
         else tmem_st16(tmem + kColP + kPW * wg + lane_base, pw);
-        if constexpr (!B16) tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
+        tmem_st1(tmem + kColSFP + 4 * wg + quad + lane_base, sfp);
         // selective rescale of O (and l): only warps holding a moved row; each
         // half rescales half of the columns
         if (j > 0 && __any_sync(0xFFFFFFFFu, moved)) {
@@ -725,13 +690,13 @@ __global__ void __launch_bounds__(FwdCfg<D, B16>::kThreads, 1)
   }
 }
 
-template <int D, bool B16>
+template <int D>
 lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
                        const void* q8, const void* sfq, const void* k8,
                        const void* sfk, const void* v8, const void* sfv,
                        void* o, float* lse, uint32_t* err, uint64_t wait_ns,
                        int32_t withhold_kv, cudaStream_t cs) {
-  using C = FwdCfg<D, B16>;
+  using C = FwdCfg<D>;
   const CUtensorMapSwizzle sw =
       C::kChunkB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUtensorMap tq, tk, tv;
@@ -743,7 +708,7 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
     uint64_t strides[2] = {static_cast<uint64_t>(C::kRowB),
                            static_cast<uint64_t>(heads * C::kRowB)};
     uint32_t box[3] = {static_cast<uint32_t>(C::kChunkB / C::kEl), 1u, rows};
-    return encode_tmap(m, B16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8,
                        3, base, dims, strides, box, sw);
   };
   lpfa_status st;
@@ -778,10 +743,10 @@ lpfa_status launch_fwd(const lpfa_attn_desc* desc, const SeqView& sv,
   const int nsm = num_sms();
   const int64_t nblocks = nitems < nsm ? nitems : nsm;   // one CTA per SM
   const size_t smem = C::kTotal + 1024;
-  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D, B16>),
+  if ((st = set_max_dynamic_smem(reinterpret_cast<const void*>(&mx_attn_fwd_kernel<D>),
                                  static_cast<int>(smem))) != LPFA_OK)
     return st;
-  mx_attn_fwd_kernel<D, B16><<<static_cast<unsigned>(nblocks), C::kThreads, smem, cs>>>(tq, tk, tv, p);
+  mx_attn_fwd_kernel<D><<<static_cast<unsigned>(nblocks), C::kThreads, smem, cs>>>(tq, tk, tv, p);
   LPFA_CHECK_CUDA(cudaGetLastError());
   return LPFA_OK;
 }
@@ -830,18 +795,13 @@ lpfa_status fwd_impl(const lpfa_attn_desc* desc, const void* q8, const void* sfq
   if (sv.total_tokens == 0) return LPFA_OK;
   LPFA_CHECK_CUDA(cudaMemsetAsync(workspace, 0, 256, cs));
   uint32_t* err = static_cast<uint32_t*>(workspace);
-  if (bf16) {
-    if (desc->head_dim == 128)
-      return launch_fwd<128, true>(desc, sv, q8, nullptr, k8, nullptr, v8, nullptr, o, lse,
-                                   err, wait_ns, withhold_kv, cs);
-    return launch_fwd<64, true>(desc, sv, q8, nullptr, k8, nullptr, v8, nullptr, o, lse, err,
-                                wait_ns, withhold_kv, cs);
-  }
+  // bf16: the two-query-tile kernel (fwd_pair.cu), its faster structure
+  if (bf16) return launch_fwd_pair_bf16(desc, sv, q8, k8, v8, o, lse, err, cs);
   if (desc->head_dim == 128)
-    return launch_fwd<128, false>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse,
-                                  err, wait_ns, withhold_kv, cs);
-  return launch_fwd<64, false>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
-                               wait_ns, withhold_kv, cs);
+    return launch_fwd<128>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err,
+                           wait_ns, withhold_kv, cs);
+  return launch_fwd<64>(desc, sv, q8, sfq_mma, k8, sfk_mma, v8, sfv_mma, o, lse, err, wait_ns,
+                        withhold_kv, cs);
 }
 
 }  // namespace

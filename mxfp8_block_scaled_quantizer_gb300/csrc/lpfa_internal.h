@@ -55,6 +55,11 @@ lpfa_status make_seq_view(const lpfa_seqs* s, SeqView* out);
 
 // Validates an attention descriptor and builds its sequence view.
 lpfa_status validate_attn(const lpfa_attn_desc* desc, SeqView* sv);
+// The bf16 forward with two query tiles in flight (fwd_pair.cu), called by
+// lpfa_fwd_bf16 after validation; err is the workspace's error word.
+lpfa_status launch_fwd_pair_bf16(const lpfa_attn_desc* desc, const SeqView& sv,
+                                 const void* q, const void* k, const void* v, void* o,
+                                 float* lse, uint32_t* err, cudaStream_t cs);
 
 // Number of SMs of the current device (cached per device).
 int num_sms();
