@@ -452,10 +452,11 @@ lpfa_status lpfa_fwd(const lpfa_attn_desc* desc, const void* q8,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward in bf16 ([P1] paragraph 1: the MXFP8 kernels are measured against
- * their bf16 counterparts).  The same algorithm and kernel structure as
- * lpfa_fwd with kind::f16 MMAs on bf16 operands and no block scales: S = c q
- * k^T in fp32, the same online softmax (rescale_threshold as in the
- * descriptor), P rounded to bf16 for the PV product, l summed in fp32.
+ * their bf16 counterparts).  The same algorithm as lpfa_fwd with kind::f16
+ * MMAs on bf16 operands and no block scales: S = c q k^T in fp32, the same
+ * online softmax (rescale_threshold as in the descriptor) over 64-key tiles,
+ * P rounded to bf16 for the PV product, l summed in fp32.  Its kernel keeps
+ * two 128-query tiles in flight per CTA (its faster structure).
  *  q [T, Hq, D], k, v [T, Hkv, D]: bf16, token-major, 16-byte aligned.
  *  o, lse, workspace, errors: as lpfa_fwd. */
 lpfa_status lpfa_fwd_bf16(const lpfa_attn_desc* desc, const void* q, const void* k,
