@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(PairCfg<D>::kThreads, 1)
       if (!work_item(p, idx, w)) continue;
       const int kvh = w.head / p.group;
       const int nt = max(side_tiles<kBlockN>(p, w, 0), side_tiles<kBlockN>(p, w, 1));
-      // the Q tiles (and their scale tiles) are free once the previous
+      // the Q tiles are free once the previous
       // item's last S MMA has completed
       if (k > 0) {
         ok = mbar_wait_sleep(&bars->q_empty, (k - 1) & 1, p.err, abort, 11, p.wait_ns);
