@@ -750,6 +750,25 @@ def run_profile_case(iters: int):
     return 0
 
 
+def run_profile_case_bf16(iters: int):
+    """The bf16 forward (the two-query-tile kernel) on the profile case's
+    attention shape, B4 H16 S8192 D128 causal, ``iters`` times, no timing."""
+    from mxfp8_block_scaled_quantizer_gb300 import build
+    build()
+    from mxfp8_block_scaled_quantizer_gb300 import lpfa as L
+    B, S, H, D = 4, 8192, 16, 128
+    g = torch.Generator(device="cuda").manual_seed(0)
+    mk = lambda: torch.randn(B * S, H, D, device="cuda", dtype=torch.bfloat16, generator=g)
+    q, k, v = mk(), mk(), mk()
+    seqs = L.dense_seqs(B, S)
+    desc = L.attn_desc(seqs, H, H, D, True, D ** -0.5)
+    for _ in range(iters):
+        o, lse, ws = L.attention_forward_bf16(q, k, v, desc)
+    torch.cuda.synchronize()
+    L.lpfa_check(ws)
+    return 0
+
+
 def run_profile_case_gemm_norm(iters: int):
     """One small pass of the jagged GEMM-Norm backward for ncu captures: 4
     jagged sequences (lengths U[128, 8192], seed 5), hidden 4096 (X, Y, dZ
@@ -782,12 +801,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", type=int, default=0, metavar="ITERS",
                     help="run the small ncu capture case ITERS times and exit")
-    ap.add_argument("--case", default="attention", choices=["attention", "gemm_norm"],
+    ap.add_argument("--case", default="attention", choices=["attention", "gemm_norm", "bf16_fwd"],
                     help="which small case --profile-case runs")
     args = ap.parse_args()
     if args.profile_case:
         if args.case == "gemm_norm":
             return run_profile_case_gemm_norm(args.profile_case)
+        if args.case == "bf16_fwd":
+            return run_profile_case_bf16(args.profile_case)
         return run_profile_case(args.profile_case)
     world, rank, local = _dist()
     try:
