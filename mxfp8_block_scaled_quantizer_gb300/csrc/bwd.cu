@@ -74,7 +74,7 @@ struct BwdCfg {
   static constexpr int kLseAhead = kStages >= 4 ? 0 : 2;
   static constexpr int kLseSlots = kLseAhead + kLag + 1;
   static_assert(kLseSlots <= kLseSlotsMax, "LSE slots");
-  static constexpr int kDqBufs = 2;            // dQ staging tiles per compute warp (four ran 0.9 % slower)
+  static constexpr int kDqBufs = 1;            // dQ staging tiles per compute warp (two ran 0.3 %, four 1.2 % slower)
   static constexpr int kKSteps = kRowB / 32;    // MMA K-steps over head_dim (32 bytes each)
   static constexpr int kQPerStep = 32 / kEl;    // queries / keys contracted per MMA
   // P^T and dS^T of a warpgroup's 32 queries: TMEM columns per key row
@@ -644,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // step j-kDqBufs's reduce has read the slot
       if (lane == 0) {
         if constexpr (kDqBufs == 4) bulk_wait_read_le3();
-        else bulk_wait_read_le1();
+        else if constexpr (kDqBufs == 2) bulk_wait_read_le1();
+        else bulk_wait_read0();
       }
       __syncwarp();
       const uint64_t mul = pack2(p.dq_mult, p.dq_mult);
